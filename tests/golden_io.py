@@ -1,0 +1,43 @@
+"""Reader for the hand-worked example fixtures under tests/golden/."""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+
+GOLDEN_DIR = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _hex_list(text: str):
+    out = []
+    for tok in text.split():
+        if "*" in tok:
+            v, n = tok.split("*")
+            out.extend([int(v, 16)] * int(n))
+        else:
+            out.append(int(tok, 16))
+    return out
+
+
+def load_quant_examples(name: str = "quant_examples.txt"):
+    cases, cur = [], None
+    with open(os.path.join(GOLDEN_DIR, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, _, val = (s.strip() for s in line.partition("="))
+            if key == "case":
+                cur = {"case": val}
+                cases.append(cur)
+            elif key in ("x",):
+                cur[key] = np.array(_hex_list(val), np.uint16)
+            elif key in ("q",):
+                cur[key] = np.array(_hex_list(val), np.uint8)
+            elif key == "scale":
+                cur[key] = int(val, 16)
+            elif key == "clamped":
+                cur[key] = int(val)
+            else:
+                cur[key] = val
+    return cases
