@@ -1,0 +1,252 @@
+"""Hybrid-granularity FP8 quantization and block-scaled FP8 GEMM for GB300.
+
+Python binding of the C ABI in ``include/fp8hg.h`` (library ``libfp8hg.so``,
+built in-tree from ``csrc/``).  This module only marshals arguments: every
+step of the computation runs in the CUDA kernels.  PyTorch supplies device
+memory and the current stream.  There is no CPU fallback: if the library is
+missing or fails to load, every call raises.
+
+Tensor-level API (same names as the C entry points):
+
+  fp8_quant_token(x, group=0|128, fmt, transpose=False) -> QTensor
+  fp8_quant_block128(x, fmt, transposed_copy=False)     -> QTensor[, QTensor]
+  fp8_quant_mx32(x, fmt, clamp_count=None)              -> QTensor
+  fp8_gemm_scaled(op, a, b, out=None, out_dtype=bf16, accumulate=False)
+  fp8hg_get_device_error(stream=None)
+
+Scale arrays are allocated with their column count rounded up to a multiple
+of four (the GEMM reads scale bytes four at a time); ``QTensor.scales()``
+returns the unpadded view.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+from dataclasses import dataclass
+from typing import Optional
+
+from . import build as _build
+
+E4M3, E5M2 = 0, 1
+GRAN_ROW, GRAN_1x128, GRAN_128x128, GRAN_MX32 = 0, 1, 2, 3
+FPROP, DGRAD, WGRAD = 0, 1, 2
+OUT_BF16, OUT_FP32 = 0, 1
+
+STATUS = {0: "FP8HG_OK", 1: "FP8HG_ERR_INVALID_ARG", 2: "FP8HG_ERR_ALIGNMENT",
+          3: "FP8HG_ERR_SHAPE", 4: "FP8HG_ERR_UNSUPPORTED", 5: "FP8HG_ERR_CUDA",
+          6: "FP8HG_ERR_TIMEOUT"}
+
+HEADER = os.path.join(_build.INCLUDE, "fp8hg.h")
+
+
+class Fp8hgError(RuntimeError):
+    def __init__(self, what: str, status: int):
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+class Operand(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scale", ctypes.c_void_p),
+                ("rows", ctypes.c_int64), ("k", ctypes.c_int64), ("ld", ctypes.c_int64),
+                ("ld_scale", ctypes.c_int64), ("fmt", ctypes.c_int32), ("gran", ctypes.c_int32)]
+
+
+class GemmOpts(ctypes.Structure):
+    _fields_ = [("wait_limit_ns", ctypes.c_uint64), ("inject_fault", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def declared_functions():
+    """Names of the functions include/fp8hg.h declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
+
+
+def load_library(build_if_stale: bool = True):
+    """Load libfp8hg.so (building it first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if build_if_stale and _build.is_stale():
+            _build.build()
+        if not os.path.exists(_build.LIB_PATH):
+            raise RuntimeError(f"CUDA library not built: {_build.LIB_PATH}")
+        lib = ctypes.CDLL(_build.LIB_PATH)
+        P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        lib.fp8_quant_token.argtypes = [P, I64, I64, I64, I, I, I, P, I64, P, I64, P]
+        lib.fp8_quant_block128.argtypes = [P, I64, I64, I64, I, P, I64, P, I64, P, I64, P, I64, P]
+        lib.fp8_quant_mx32.argtypes = [P, I64, I64, I64, I, P, I64, P, I64, P, P]
+        lib.fp8_gemm_scaled.argtypes = [I, ctypes.POINTER(Operand), ctypes.POINTER(Operand), P,
+                                        I64, I, I, P]
+        lib.fp8_gemm_scaled_ex.argtypes = [I, ctypes.POINTER(Operand), ctypes.POINTER(Operand), P,
+                                           I64, I, I, ctypes.POINTER(GemmOpts), P]
+        lib.fp8hg_get_device_error.argtypes = [P]
+        lib.fp8hg_status_str.restype = ctypes.c_char_p
+        lib.fp8hg_status_str.argtypes = [I]
+        for fn in ("fp8_quant_token", "fp8_quant_block128", "fp8_quant_mx32", "fp8_gemm_scaled",
+                   "fp8_gemm_scaled_ex", "fp8hg_get_device_error", "fp8hg_version"):
+            getattr(lib, fn).restype = I
+        _lib = lib
+        return lib
+
+
+def lib():
+    return _lib if _lib is not None else load_library()
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise Fp8hgError(what, rc)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _round4(n: int) -> int:
+    return (n + 3) // 4 * 4
+
+
+@dataclass
+class QTensor:
+    """FP8 codes [rows, k] (K-contiguous) and their scale bytes.
+
+    ``scale`` holds the padded storage; ``ncols_scale`` its meaningful
+    columns.  ``gran`` says how scale bytes map onto elements."""
+    codes: "object"
+    scale: "object"
+    fmt: int
+    gran: int
+    ncols_scale: int
+
+    def scales(self):
+        return self.scale[:, :self.ncols_scale]
+
+    def operand(self) -> Operand:
+        c, s = self.codes, self.scale
+        return Operand(c.data_ptr(), s.data_ptr(), c.shape[0], c.shape[1], c.stride(0),
+                       s.stride(0), self.fmt, self.gran)
+
+
+def _check_bf16(x):
+    import torch
+    if x.dtype != torch.bfloat16 or not x.is_cuda or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D CUDA bfloat16 tensor with unit column stride")
+
+
+def fp8_quant_token(x, group: int = 0, fmt: int = E4M3, transpose: bool = False,
+                    q=None, scale=None, stream=None) -> QTensor:
+    """Per-token (group=0) or per-1x128 (group=128) UE8M0 quantization;
+    transpose=True quantizes 128-row groups and writes [cols, rows]."""
+    import torch
+    _check_bf16(x)
+    rows, cols = x.shape
+    if transpose:
+        ncs = rows // 128
+        q = q if q is not None else torch.empty((cols, rows), dtype=torch.uint8, device=x.device)
+        scale = scale if scale is not None else torch.empty((cols, _round4(ncs)), dtype=torch.uint8,
+                                                            device=x.device)
+    else:
+        ncs = 1 if group == 0 else cols // 128
+        q = q if q is not None else torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+        if scale is None:
+            scale = torch.empty((rows, 1 if group == 0 else _round4(ncs)), dtype=torch.uint8,
+                                device=x.device)
+    rc = lib().fp8_quant_token(_ptr(x), rows, cols, x.stride(0), group, 1 if transpose else 0,
+                               fmt, _ptr(q), q.stride(0), _ptr(scale), scale.stride(0),
+                               _stream(stream))
+    _check(rc, "fp8_quant_token")
+    gran = GRAN_1x128 if (transpose or group == 128) else GRAN_ROW
+    return QTensor(q, scale, fmt, gran, ncs)
+
+
+def fp8_quant_block128(x, fmt: int = E4M3, transposed_copy: bool = False, stream=None):
+    """Per-128x128-block UE8M0 quantization; with transposed_copy=True also
+    returns the codes of x^T and the transposed scale grid."""
+    import torch
+    _check_bf16(x)
+    rows, cols = x.shape
+    dev = x.device
+    q = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+    s = torch.empty((max(rows // 128, 1), _round4(max(cols // 128, 1))), dtype=torch.uint8, device=dev)
+    qt = st = None
+    if transposed_copy:
+        qt = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
+        st = torch.empty((max(cols // 128, 1), _round4(max(rows // 128, 1))), dtype=torch.uint8,
+                         device=dev)
+    rc = lib().fp8_quant_block128(_ptr(x), rows, cols, x.stride(0), fmt, _ptr(q), q.stride(0),
+                                  _ptr(s), s.stride(0), _ptr(qt), qt.stride(0) if qt is not None else 0,
+                                  _ptr(st), st.stride(0) if st is not None else 0, _stream(stream))
+    _check(rc, "fp8_quant_block128")
+    out = QTensor(q, s, fmt, GRAN_128x128, cols // 128)
+    if transposed_copy:
+        return out, QTensor(qt, st, fmt, GRAN_128x128, rows // 128)
+    return out
+
+
+def fp8_quant_mx32(x, fmt: int = E4M3, clamp_count=None, stream=None) -> QTensor:
+    """MXFP8 quantization (32-element blocks, saturating).  clamp_count: an
+    optional int64 CUDA tensor of one element that receives (+=) the number
+    of clamped elements."""
+    import torch
+    _check_bf16(x)
+    rows, cols = x.shape
+    q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    s = torch.empty((rows, _round4(cols // 32)), dtype=torch.uint8, device=x.device)
+    rc = lib().fp8_quant_mx32(_ptr(x), rows, cols, x.stride(0), fmt, _ptr(q), q.stride(0), _ptr(s),
+                              s.stride(0), _ptr(clamp_count), _stream(stream))
+    _check(rc, "fp8_quant_mx32")
+    return QTensor(q, s, fmt, GRAN_MX32, cols // 32)
+
+
+def fp8_gemm_scaled(op: int, a: QTensor, b: QTensor, out=None, out_dtype=None,
+                    accumulate: bool = False, wait_limit_ns: int = 0, inject_fault: int = 0,
+                    stream=None):
+    """C = A * B^T (or C += A * B^T) on block-scaled FP8 operands."""
+    import torch
+    if out is None:
+        dt = out_dtype if out_dtype is not None else torch.bfloat16
+        out = torch.empty((a.codes.shape[0], b.codes.shape[0]), dtype=dt, device=a.codes.device)
+    if out.dtype == torch.bfloat16:
+        kind = OUT_BF16
+    elif out.dtype == torch.float32:
+        kind = OUT_FP32
+    else:
+        raise ValueError("out must be bfloat16 or float32")
+    oa, ob = a.operand(), b.operand()
+    if wait_limit_ns or inject_fault:
+        opts = GemmOpts(wait_limit_ns, inject_fault, 0)
+        rc = lib().fp8_gemm_scaled_ex(op, ctypes.byref(oa), ctypes.byref(ob), _ptr(out),
+                                      out.stride(0), kind, 1 if accumulate else 0,
+                                      ctypes.byref(opts), _stream(stream))
+    else:
+        rc = lib().fp8_gemm_scaled(op, ctypes.byref(oa), ctypes.byref(ob), _ptr(out),
+                                   out.stride(0), kind, 1 if accumulate else 0, _stream(stream))
+    _check(rc, "fp8_gemm_scaled")
+    return out
+
+
+def fp8hg_get_device_error(stream=None) -> int:
+    """Synchronize and return (and clear) the device error status."""
+    return int(lib().fp8hg_get_device_error(_stream(stream)))
+
+
+def fp8hg_status_str(status: int) -> str:
+    return lib().fp8hg_status_str(int(status)).decode()

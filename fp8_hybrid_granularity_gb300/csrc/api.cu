@@ -1,0 +1,214 @@
+// C-ABI entry points (declared in include/fp8hg.h): argument validation, then
+// one launch each.  Nothing here allocates device memory or synchronizes,
+// except fp8hg_get_device_error.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/fp8hg.h"
+#include "internal.h"
+
+namespace {
+
+inline bool aligned(const void *p, uintptr_t a) {
+    return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+inline int status_from_cuda(cudaError_t e) { return e == cudaSuccess ? FP8HG_OK : FP8HG_ERR_CUDA; }
+
+inline bool valid_fmt(int f) { return f == FP8HG_E4M3 || f == FP8HG_E5M2; }
+
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
+
+int validate_operand(const fp8hg_operand *o) {
+    if (!o || !o->codes || !o->scale) return FP8HG_ERR_INVALID_ARG;
+    if (!valid_fmt(o->fmt)) return FP8HG_ERR_INVALID_ARG;
+    if (o->gran < FP8HG_GRAN_ROW || o->gran > FP8HG_GRAN_MX32) return FP8HG_ERR_INVALID_ARG;
+    if (o->rows <= 0 || o->k <= 0) return FP8HG_ERR_SHAPE;
+    if (o->rows % 128 || o->k % 128) return FP8HG_ERR_SHAPE;
+    if (o->rows > (int64_t(1) << 30) || o->k > (int64_t(1) << 30)) return FP8HG_ERR_SHAPE;
+    if (o->ld < o->k || o->ld % 16) return FP8HG_ERR_ALIGNMENT;
+    if (!aligned(o->codes, 16)) return FP8HG_ERR_ALIGNMENT;
+    int64_t scale_cols = 1;
+    switch (o->gran) {
+    case FP8HG_GRAN_ROW: scale_cols = 1; break;
+    case FP8HG_GRAN_1x128:
+    case FP8HG_GRAN_128x128: scale_cols = o->k / 128; break;
+    default: scale_cols = o->k / 32; break;
+    }
+    if (o->gran == FP8HG_GRAN_ROW) {
+        if (o->ld_scale < 1) return FP8HG_ERR_INVALID_ARG;
+    } else {
+        const int64_t padded = (scale_cols + 3) / 4 * 4;
+        if (o->ld_scale < padded || o->ld_scale % 4) return FP8HG_ERR_ALIGNMENT;
+        if (!aligned(o->scale, 4)) return FP8HG_ERR_ALIGNMENT;
+    }
+    return FP8HG_OK;
+}
+
+bool gran_pair_ok(int op, int ga, int gb) {
+    if (ga == FP8HG_GRAN_MX32 && gb == FP8HG_GRAN_MX32) return true;
+    if (ga == FP8HG_GRAN_MX32 || gb == FP8HG_GRAN_MX32) return false;
+    switch (op) {
+    case FP8HG_FPROP:
+    case FP8HG_DGRAD:
+        return (ga == FP8HG_GRAN_ROW || ga == FP8HG_GRAN_1x128) && gb == FP8HG_GRAN_128x128;
+    case FP8HG_WGRAD: return ga == FP8HG_GRAN_1x128 && gb == FP8HG_GRAN_1x128;
+    default: return false;
+    }
+}
+
+int check_quant_common(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
+                       const uint8_t *q, int64_t ld_q, const uint8_t *s) {
+    if (!valid_fmt(fmt)) return FP8HG_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0) return FP8HG_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return FP8HG_OK;  // nothing is read or written
+    if (!x || !q || !s) return FP8HG_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(q, 16)) return FP8HG_ERR_ALIGNMENT;
+    if (ld_x % 8 || ld_q % 16) return FP8HG_ERR_ALIGNMENT;
+    return FP8HG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fp8_quant_token(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int group,
+                    int transpose, int fmt, uint8_t *q, int64_t ld_q, uint8_t *scale, int64_t ld_s,
+                    void *stream) {
+    int st = check_quant_common(x, rows, cols, ld_x, fmt, q, ld_q, scale);
+    if (st != FP8HG_OK) return st;
+    if (group != 0 && group != 128) return FP8HG_ERR_INVALID_ARG;
+    if (transpose != 0 && transpose != 1) return FP8HG_ERR_INVALID_ARG;
+    if (transpose && group != 128) return FP8HG_ERR_UNSUPPORTED;
+    if (rows == 0 || cols == 0) return FP8HG_OK;
+    if (transpose) {
+        if (rows % 128 || cols % 64) return FP8HG_ERR_SHAPE;
+        if (rows / 128 > 65535) return FP8HG_ERR_SHAPE;
+        if (ld_x < cols || ld_q < rows || ld_s < rows / 128) return FP8HG_ERR_INVALID_ARG;
+    } else {
+        if (cols % 128) return FP8HG_ERR_SHAPE;
+        if (ld_x < cols || ld_q < cols) return FP8HG_ERR_INVALID_ARG;
+        if (ld_s < (group ? cols / 128 : 1)) return FP8HG_ERR_INVALID_ARG;
+        if (group == 0 && rows > 2147483647LL) return FP8HG_ERR_SHAPE;
+    }
+    return status_from_cuda(fp8hg::launch_quant_token(x, rows, cols, ld_x, group, transpose, fmt, q,
+                                                      ld_q, scale, ld_s,
+                                                      static_cast<cudaStream_t>(stream)));
+}
+
+int fp8_quant_block128(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
+                       uint8_t *q, int64_t ld_q, uint8_t *scale, int64_t ld_s, uint8_t *q_t,
+                       int64_t ld_qt, uint8_t *scale_t, int64_t ld_st, void *stream) {
+    int st = check_quant_common(x, rows, cols, ld_x, fmt, q, ld_q, scale);
+    if (st != FP8HG_OK) return st;
+    if (rows == 0 || cols == 0) return FP8HG_OK;
+    if ((q_t == nullptr) != (scale_t == nullptr)) return FP8HG_ERR_INVALID_ARG;
+    if (rows % 128 || cols % 128) return FP8HG_ERR_SHAPE;
+    if (rows / 128 > 65535) return FP8HG_ERR_SHAPE;
+    if (ld_x < cols || ld_q < cols || ld_s < cols / 128) return FP8HG_ERR_INVALID_ARG;
+    if (q_t) {
+        if (!aligned(q_t, 16) || ld_qt % 16) return FP8HG_ERR_ALIGNMENT;
+        if (ld_qt < rows || ld_st < rows / 128) return FP8HG_ERR_INVALID_ARG;
+    }
+    return status_from_cuda(fp8hg::launch_quant_block128(x, rows, cols, ld_x, fmt, q, ld_q, scale,
+                                                         ld_s, q_t, ld_qt, scale_t, ld_st,
+                                                         static_cast<cudaStream_t>(stream)));
+}
+
+int fp8_quant_mx32(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt, uint8_t *q,
+                   int64_t ld_q, uint8_t *scale, int64_t ld_s, unsigned long long *clamp_count,
+                   void *stream) {
+    int st = check_quant_common(x, rows, cols, ld_x, fmt, q, ld_q, scale);
+    if (st != FP8HG_OK) return st;
+    if (rows == 0 || cols == 0) return FP8HG_OK;
+    if (cols % 32) return FP8HG_ERR_SHAPE;
+    if (ld_x < cols || ld_q < cols || ld_s < cols / 32) return FP8HG_ERR_INVALID_ARG;
+    if (clamp_count && !aligned(clamp_count, 8)) return FP8HG_ERR_ALIGNMENT;
+    return status_from_cuda(fp8hg::launch_quant_mx32(x, rows, cols, ld_x, fmt, q, ld_q, scale, ld_s,
+                                                     clamp_count,
+                                                     static_cast<cudaStream_t>(stream)));
+}
+
+int fp8_gemm_scaled_ex(int op, const fp8hg_operand *a, const fp8hg_operand *b, void *c, int64_t ldc,
+                       int out, int accumulate, const fp8hg_gemm_opts *opts, void *stream) {
+    if (op < FP8HG_FPROP || op > FP8HG_WGRAD) return FP8HG_ERR_INVALID_ARG;
+    if (out != FP8HG_OUT_BF16 && out != FP8HG_OUT_FP32) return FP8HG_ERR_INVALID_ARG;
+    if (accumulate != 0 && accumulate != 1) return FP8HG_ERR_INVALID_ARG;
+    int st = validate_operand(a);
+    if (st != FP8HG_OK) return st;
+    st = validate_operand(b);
+    if (st != FP8HG_OK) return st;
+    if (a->k != b->k) return FP8HG_ERR_SHAPE;
+    if (!gran_pair_ok(op, a->gran, b->gran)) return FP8HG_ERR_UNSUPPORTED;
+    if (!c) return FP8HG_ERR_INVALID_ARG;
+    if (!aligned(c, 16)) return FP8HG_ERR_ALIGNMENT;
+    if (ldc < b->rows) return FP8HG_ERR_INVALID_ARG;
+    if (ldc % (out == FP8HG_OUT_BF16 ? 8 : 4)) return FP8HG_ERR_ALIGNMENT;
+    if (opts && (opts->inject_fault < 0 || opts->inject_fault > 1)) return FP8HG_ERR_INVALID_ARG;
+
+    unsigned int *err = fp8hg::device_error_word();
+    if (!err) return FP8HG_ERR_CUDA;
+    fp8hg::GemmArgs g;
+    g.a_codes = a->codes;
+    g.b_codes = b->codes;
+    g.a_scale = a->scale;
+    g.b_scale = b->scale;
+    g.M = a->rows;
+    g.N = b->rows;
+    g.K = a->k;
+    g.lda = a->ld;
+    g.ldb = b->ld;
+    g.ld_sa = a->ld_scale;
+    g.ld_sb = b->ld_scale;
+    g.fmt_a = a->fmt;
+    g.fmt_b = b->fmt;
+    g.gran_a = a->gran;
+    g.gran_b = b->gran;
+    g.c = c;
+    g.ldc = ldc;
+    g.out_fp32 = out == FP8HG_OUT_FP32;
+    g.accumulate = accumulate;
+    g.wait_limit_ns = (opts && opts->wait_limit_ns) ? opts->wait_limit_ns : kDefaultWaitNs;
+    g.inject_fault = opts ? opts->inject_fault : 0;
+    g.err = err;
+    const int rc = fp8hg::launch_gemm_scaled(g, static_cast<cudaStream_t>(stream));
+    if (rc == 1) return FP8HG_ERR_UNSUPPORTED;  // tensor map could not be encoded
+    return rc == 0 ? FP8HG_OK : FP8HG_ERR_CUDA;
+}
+
+int fp8_gemm_scaled(int op, const fp8hg_operand *a, const fp8hg_operand *b, void *c, int64_t ldc,
+                    int out, int accumulate, void *stream) {
+    return fp8_gemm_scaled_ex(op, a, b, c, ldc, out, accumulate, nullptr, stream);
+}
+
+int fp8hg_get_device_error(void *stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8HG_ERR_CUDA;
+    unsigned int *err = fp8hg::device_error_word();
+    if (!err) return FP8HG_ERR_CUDA;
+    unsigned int host[2] = {0, 0};
+    if (cudaMemcpy(host, err, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return FP8HG_ERR_CUDA;
+    if (host[0] == 0) return FP8HG_OK;
+    const unsigned int zero[2] = {0, 0};
+    if (cudaMemcpy(err, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+        return FP8HG_ERR_CUDA;
+    return FP8HG_ERR_TIMEOUT;
+}
+
+const char *fp8hg_status_str(int status) {
+    switch (status) {
+    case FP8HG_OK: return "FP8HG_OK";
+    case FP8HG_ERR_INVALID_ARG: return "FP8HG_ERR_INVALID_ARG";
+    case FP8HG_ERR_ALIGNMENT: return "FP8HG_ERR_ALIGNMENT";
+    case FP8HG_ERR_SHAPE: return "FP8HG_ERR_SHAPE";
+    case FP8HG_ERR_UNSUPPORTED: return "FP8HG_ERR_UNSUPPORTED";
+    case FP8HG_ERR_CUDA: return "FP8HG_ERR_CUDA";
+    case FP8HG_ERR_TIMEOUT: return "FP8HG_ERR_TIMEOUT";
+    default: return "FP8HG_UNKNOWN_STATUS";
+    }
+}
+
+int fp8hg_version(void) { return (1 << 16) | 0; }
+
+}  // extern "C"

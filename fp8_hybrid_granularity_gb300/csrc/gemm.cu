@@ -1,0 +1,484 @@
+// Block-scaled FP8 GEMM on the 5th-generation tensor cores (tcgen05).
+//
+//   C[M, N] (+)= A[M, K] * B[N, K]^T,  A and B FP8 (E4M3 / E5M2), K-contiguous,
+//   each element carrying a UE8M0 power-of-two scale.
+//
+// "A Comprehensive FP8 Training Recipe for Reasoning-Enhanced Language
+// Models" ("What carries the argument", referee summary): the forward and
+// backward GEMMs run on FP8 operands scaled per 128x128 weight block and per
+// token (or 1x128 group) of the activations, with FP32 accumulation.
+//
+// Design (GB300, sm_103a):
+//  * Every granularity becomes one UE8M0 scale per 32 K elements per row,
+//    which is exactly the operand of tcgen05.mma.kind::mxf8f6f4.block_scale
+//    (scale_vec::1X).  The scales are applied inside the MMA while it
+//    accumulates into tensor memory in FP32: no CUDA-core promotion pass.
+//      ROW      the row's byte repeated in all four 32-K slots
+//      1x128    the group's byte; all four 32-K MMAs of a 128-K stage use it
+//      128x128  the block's byte, the same for the tile's 128 rows
+//      MX32     four distinct bytes per 128-K stage
+//    The kernel reads the caller's compact scale arrays directly: a scale
+//    warp copies one 32-bit word per row and stage (cp.async, 4 bytes) into
+//    the shared-memory layout tcgen05.cp expects, and the MMA's scale-factor
+//    id picks the byte of that word that belongs to the stage.
+//  * Tile 128 x 256 x 128 (one CTA per SM, 4-stage TMA/mbarrier pipeline,
+//    128-byte swizzled operand tiles), persistent over output tiles.
+//  * Warp roles (256 threads): warp 0 TMA producer, warp 1 MMA issuer and
+//    tensor-memory owner, warp 2 scale loader, warps 4-7 epilogue
+//    (tensor memory -> registers -> BF16/FP32 global stores).
+//  * Tensor memory (512 columns): accumulator in columns [0, 256), then per
+//    pipeline stage 4 columns of A scales and 8 of B scales.
+//  * Every wait is bounded (globaltimer); on expiry the kernel records a
+//    timeout in the device error word, drains its in-flight copies and MMAs,
+//    frees tensor memory and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8hg {
+
+__device__ unsigned int g_fp8hg_err[2];
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
+constexpr uint32_t A_TILE = BM * BK;  // bytes per stage
+constexpr uint32_t B_TILE = BN * BK;
+constexpr uint32_t SFA_TILE = 512;    // 128 rows x 4 scale bytes
+constexpr uint32_t SFB_TILE = 1024;   // 256 rows x 4 scale bytes
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t ACC_COL = 0;
+constexpr uint32_t SFA_COL = 256;                // + 4 * stage
+constexpr uint32_t SFB_COL = 256 + 4 * STAGES;   // + 8 * stage
+constexpr int NUM_THREADS = 256;
+
+constexpr uint32_t OFF_A = 0;
+constexpr uint32_t OFF_B = OFF_A + STAGES * A_TILE;
+constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_TILE;
+constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_TILE;
+constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_TILE;
+constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + 96;
+constexpr uint32_t OFF_ABORT = OFF_BAR + 100;
+constexpr uint32_t SMEM_USED = OFF_BAR + 128;
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
+
+enum { GRAN_ROW = 0, GRAN_1x128 = 1, GRAN_128x128 = 2, GRAN_MX32 = 3 };
+enum { WHO_PRODUCER = 1, WHO_MMA = 2, WHO_SCALES = 3, WHO_EPILOGUE = 4 };
+
+struct KParams {
+    int M, N, nk, num_nb, num_tiles;
+    int gran_a, gran_b;
+    int out_fp32, accumulate, inject;
+    const uint8_t *sa, *sb;
+    int64_t ld_sa, ld_sb;
+    void *c;
+    int64_t ldc;
+    uint32_t idesc;
+    uint64_t wait_limit_ns;
+    unsigned int *err;
+};
+
+// Shared-memory matrix descriptor for a K-major operand tile stored with the
+// 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address
+    d |= static_cast<uint64_t>(1) << 16;                  // leading byte offset (unused)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;          // stride byte offset
+    d |= static_cast<uint64_t>(1) << 46;                  // descriptor version
+    d |= static_cast<uint64_t>(2) << 61;                  // 128-byte swizzle
+    return d;
+}
+
+// Descriptor of a 32-row x 16-byte scale tile (no swizzle; 8-row core
+// matrices of 128 contiguous bytes).
+__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(128 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    return d;
+}
+
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting or
+// the limit ran out (then the abort flag and the device error word are set).
+// check_abort = false is used while draining: keep waiting for the phase up
+// to `limit` even though an abort is in progress, and report nothing.
+__device__ bool wait_phase(uint32_t bar, uint32_t parity, uint64_t limit,
+                           volatile uint32_t *abort_flag, unsigned int *err, uint32_t who,
+                           bool check_abort = true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    uint32_t it = 0;
+    while (true) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((++it & 15u) == 0) {
+            if (check_abort && *abort_flag) return false;
+            if (ptx::globaltimer() - t0 > limit) {
+                if (check_abort) {
+                    *abort_flag = 1u;
+                    atomicOr(err, 1u);
+                    atomicCAS(err + 1, 0u, who);
+                }
+                return false;
+            }
+        }
+    }
+}
+
+// Address of the 32-bit scale word holding row r's scale(s) for 128-K block kb.
+__device__ __forceinline__ const uint8_t *scale_word(const uint8_t *s, int64_t ld, int gran,
+                                                     int64_t r, int kb) {
+    if (gran == GRAN_MX32) return s + r * ld + 4 * kb;
+    if (gran == GRAN_128x128) return s + (r >> 7) * ld + (kb & ~3);
+    return s + r * ld + (kb & ~3);  // 1x128
+}
+
+__device__ __forceinline__ uint32_t sf_id(int gran, int kb, int j) {
+    return (gran == GRAN_1x128 || gran == GRAN_128x128) ? static_cast<uint32_t>(kb & 3)
+                                                        : static_cast<uint32_t>(j);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_gemm_mxf8(const __grid_constant__ CUtensorMap tmap_a,
+                const __grid_constant__ CUtensorMap tmap_b, const KParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    const uint32_t sA = base + OFF_A, sB = base + OFF_B;
+    const uint32_t sSFA = base + OFF_SFA, sSFB = base + OFF_SFB, sBAR = base + OFF_BAR;
+    const uint32_t tfull = sBAR + 64, tempty = sBAR + 72, drain = sBAR + 80;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + OFF_TMEM_SLOT);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + OFF_ABORT);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t limit = p.wait_limit_ns;
+    const uint64_t drain_limit = 2000000ull;  // 2 ms: copies and MMAs finish in microseconds
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(sBAR + 8 * s, 1 + 64);  // TMA expect_tx + 32 cp.async + 32 plain arrivals
+            ptx::mbar_init(sBAR + 32 + 8 * s, 1);  // tcgen05.commit
+        }
+        ptx::mbar_init(tfull, 1);
+        ptx::mbar_init(tempty, 128);
+        ptx::mbar_init(drain, 1);
+        *abort_flag = 0u;
+        ptx::fence_mbar_init();
+        ptx::prefetch_tmap(&tmap_a);
+        ptx::prefetch_tmap(&tmap_b);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+            const int mb = tile / p.num_nb, nb = tile % p.num_nb;
+            for (int kb = 0; kb < p.nk; ++kb) {
+                const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                ok = wait_phase(sBAR + 32 + 8 * s, ph ^ 1u, limit, abort_flag, p.err, WHO_PRODUCER);
+                ok = __all_sync(0xFFFFFFFFu, ok);
+                if (!ok) break;
+                if (lane == 0) {
+                    ptx::mbar_arrive_expect_tx(sBAR + 8 * s, A_TILE + B_TILE);
+                    ptx::tma_load_2d(sA + s * A_TILE, &tmap_a, sBAR + 8 * s, kb * BK, mb * BM);
+                    ptx::tma_load_2d(sB + s * B_TILE, &tmap_b, sBAR + 8 * s, kb * BK, nb * BN);
+                }
+                __syncwarp();
+                ++it;
+            }
+        }
+        // wait for the last loads to land before the CTA may exit
+        const uint32_t nd = it < static_cast<uint32_t>(STAGES) ? it : static_cast<uint32_t>(STAGES);
+        for (uint32_t i = it - nd; i < it; ++i)
+            wait_phase(sBAR + 8 * (i % STAGES), (i / STAGES) & 1u, drain_limit, abort_flag, p.err,
+                       WHO_PRODUCER, false);
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        uint32_t it = 0, tcount = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+            ok = wait_phase(tempty, (tcount & 1u) ^ 1u, limit, abort_flag, p.err, WHO_MMA);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            for (int kb = 0; kb < p.nk; ++kb) {
+                const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                ok = wait_phase(sBAR + 8 * s, ph, limit, abort_flag, p.err, WHO_MMA);
+                ok = __all_sync(0xFFFFFFFFu, ok);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                if (lane == 0) {
+                    ptx::fence_proxy_async_smem();  // scale words written by cp.async
+                    const uint32_t tsfa = tmem + SFA_COL + 4 * s;
+                    const uint32_t tsfb = tmem + SFB_COL + 8 * s;
+                    ptx::tc_cp_32x128b_warpx4(tsfa, desc_sf(sSFA + s * SFA_TILE));
+                    ptx::tc_cp_32x128b_warpx4(tsfb, desc_sf(sSFB + s * SFB_TILE));
+                    ptx::tc_cp_32x128b_warpx4(tsfb + 4, desc_sf(sSFB + s * SFB_TILE + 512));
+                    const uint64_t ad = desc_sw128(sA + s * A_TILE);
+                    const uint64_t bd = desc_sw128(sB + s * B_TILE);
+#pragma unroll
+                    for (int j = 0; j < BK / 32; ++j) {
+                        const uint32_t idesc = p.idesc | (sf_id(p.gran_a, kb, j) << 29) |
+                                               (sf_id(p.gran_b, kb, j) << 4);
+                        // +32 bytes along K inside the swizzled 128-byte rows
+                        ptx::tc_mma_mxf8(tmem + ACC_COL, ad + 2 * j, bd + 2 * j, idesc, tsfa, tsfb,
+                                         (kb | j) != 0 ? 1u : 0u);
+                    }
+                    ptx::tc_commit(sBAR + 32 + 8 * s);  // frees the smem stage when done
+                }
+                __syncwarp();
+                ++it;
+            }
+            if (!ok) break;
+            if (lane == 0) ptx::tc_commit(tfull);
+            __syncwarp();
+            ++tcount;
+        }
+        // all issued MMAs must finish before tensor memory is released
+        if (lane == 0) ptx::tc_commit(drain);
+        __syncwarp();
+        wait_phase(drain, 0u, drain_limit, abort_flag, p.err, WHO_MMA, false);
+    } else if (warp == 2) {
+        // ------------------------------------------------------ scale loader
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+            const int mb = tile / p.num_nb, nb = tile % p.num_nb;
+            // row-constant scales (per-token granularity): one load per tile
+            uint32_t rowA[4], rowB[8];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const int64_t m = static_cast<int64_t>(mb) * BM + 32 * a + lane;
+                rowA[a] = (p.gran_a == GRAN_ROW) ? p.sa[m * p.ld_sa] * 0x01010101u : 0u;
+            }
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                const int64_t n = static_cast<int64_t>(nb) * BN + 32 * h + lane;
+                rowB[h] = (p.gran_b == GRAN_ROW && n < p.N) ? p.sb[n * p.ld_sb] * 0x01010101u
+                                                             : 0x7F7F7F7Fu;
+            }
+            for (int kb = 0; kb < p.nk; ++kb) {
+                const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                ok = wait_phase(sBAR + 32 + 8 * s, ph ^ 1u, limit, abort_flag, p.err, WHO_SCALES);
+                ok = __all_sync(0xFFFFFFFFu, ok);
+                if (!ok) break;
+                // Row r = 32a + lane of a 128-row chunk goes to byte offset
+                // lane*16 + a*4: the 32x128-bit layout tcgen05.cp broadcasts.
+                const uint32_t dA = sSFA + s * SFA_TILE + lane * 16;
+                const uint32_t dB = sSFB + s * SFB_TILE + lane * 16;
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    const int64_t m = static_cast<int64_t>(mb) * BM + 32 * a + lane;
+                    if (p.gran_a == GRAN_ROW) st_shared_u32(dA + 4 * a, rowA[a]);
+                    else ptx::cp_async_4(dA + 4 * a, scale_word(p.sa, p.ld_sa, p.gran_a, m, kb));
+                }
+#pragma unroll
+                for (int h = 0; h < 8; ++h) {
+                    const int64_t n = static_cast<int64_t>(nb) * BN + 32 * h + lane;
+                    const uint32_t dst = dB + (h >> 2) * 512 + (h & 3) * 4;
+                    if (p.gran_b == GRAN_ROW || n >= p.N) st_shared_u32(dst, rowB[h]);
+                    else ptx::cp_async_4(dst, scale_word(p.sb, p.ld_sb, p.gran_b, n, kb));
+                }
+                if (!(p.inject == 1 && it == 0)) {
+                    ptx::fence_proxy_async_smem();
+                    ptx::mbar_arrive(sBAR + 8 * s);
+                    ptx::cp_async_mbar_arrive_noinc(sBAR + 8 * s);
+                }
+                ++it;
+            }
+        }
+        ptx::cp_async_wait_all();
+    } else if (warp >= 4) {
+        // --------------------------------------------------------- epilogue
+        const int q = warp & 3;  // tensor-memory lane quarter this warp may read
+        uint32_t tcount = 0;
+        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+            const int mb = tile / p.num_nb, nb = tile % p.num_nb;
+            bool ok = wait_phase(tfull, tcount & 1u, limit, abort_flag, p.err, WHO_EPILOGUE);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const int64_t row = static_cast<int64_t>(mb) * BM + q * 32 + lane;
+#pragma unroll 1
+            for (int chunk = 0; chunk < BN / 32; ++chunk) {
+                uint32_t r[32];
+                ptx::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + ACC_COL +
+                                            chunk * 32,
+                                        r);
+                ptx::tmem_wait_ld();
+                if (chunk == BN / 32 - 1) {
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(tempty);  // accumulator may be overwritten now
+                }
+                const int64_t n0 = static_cast<int64_t>(nb) * BN + chunk * 32;
+                if (n0 >= p.N) continue;
+                if (p.out_fp32) {
+                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.c) + row * p.ldc + n0);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        float4 o = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                               __uint_as_float(r[4 * v + 2]),
+                                               __uint_as_float(r[4 * v + 3]));
+                        if (p.accumulate) {
+                            const float4 old = dst[v];
+                            o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
+                        }
+                        dst[v] = o;
+                    }
+                } else {
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.c) + row * p.ldc + n0);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        float f[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(r[8 * v + e]);
+                        if (p.accumulate) {
+                            const uint4 old = dst[v];
+                            f[0] += bf16_lo(old.x); f[1] += bf16_hi(old.x);
+                            f[2] += bf16_lo(old.y); f[3] += bf16_hi(old.y);
+                            f[4] += bf16_lo(old.z); f[5] += bf16_hi(old.z);
+                            f[6] += bf16_lo(old.w); f[7] += bf16_hi(old.w);
+                        }
+                        dst[v] = make_uint4(ptx::cvt_bf16x2(f[0], f[1]), ptx::cvt_bf16x2(f[2], f[3]),
+                                            ptx::cvt_bf16x2(f[4], f[5]), ptx::cvt_bf16x2(f[6], f[7]));
+                    }
+                }
+            }
+            ++tcount;
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+bool make_tmap(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t k, uint64_t ld,
+               uint32_t box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {k, rows};
+    const cuuint64_t strides[1] = {ld};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int g_sms[64] = {0};
+bool g_attr_set[64] = {false};
+std::mutex g_mu;
+
+}  // namespace
+
+unsigned int *device_error_word() {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fp8hg_err) != cudaSuccess) return nullptr;
+    return static_cast<unsigned int *>(p);
+}
+
+int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
+    CUtensorMap ta, tb;
+    std::memset(&ta, 0, sizeof(ta));
+    std::memset(&tb, 0, sizeof(tb));
+    if (!make_tmap(&ta, g.a_codes, g.M, g.K, g.lda, BM)) return 1;
+    if (!make_tmap(&tb, g.b_codes, g.N, g.K, g.ldb, BN)) return 1;
+
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!g_attr_set[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(k_gemm_mxf8, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(SMEM_BYTES));
+            if (e != cudaSuccess) return 2 + static_cast<int>(e);
+            int n = 0;
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+            g_sms[dev] = n > 0 ? n : 1;
+            g_attr_set[dev] = true;
+        }
+    }
+
+    KParams p;
+    p.M = static_cast<int>(g.M);
+    p.N = static_cast<int>(g.N);
+    p.nk = static_cast<int>(g.K / BK);
+    p.num_nb = static_cast<int>((g.N + BN - 1) / BN);
+    p.num_tiles = static_cast<int>(g.M / BM) * p.num_nb;
+    p.gran_a = g.gran_a;
+    p.gran_b = g.gran_b;
+    p.out_fp32 = g.out_fp32;
+    p.accumulate = g.accumulate;
+    p.inject = g.inject_fault;
+    p.sa = g.a_scale;
+    p.sb = g.b_scale;
+    p.ld_sa = g.ld_sa;
+    p.ld_sb = g.ld_sb;
+    p.c = g.c;
+    p.ldc = g.ldc;
+    // instruction descriptor, kind::mxf8f6f4 with block scaling: A/B formats
+    // (E4M3 = 0, E5M2 = 1) in bits 7-9 / 10-12, K-major A and B, N >> 3 in
+    // bits 17-22, UE8M0 scale type in bit 23, M >> 4 in bits 24-28; the
+    // scale-factor byte ids (bits 4-5 for B, 29-30 for A) are set per MMA.
+    p.idesc = (1u << 23) | (static_cast<uint32_t>(BN >> 3) << 17) |
+              (static_cast<uint32_t>(BM >> 4) << 24) | (static_cast<uint32_t>(g.fmt_a) << 7) |
+              (static_cast<uint32_t>(g.fmt_b) << 10);
+    p.wait_limit_ns = g.wait_limit_ns;
+    p.err = g.err;
+
+    int grid = g_sms[dev];
+    if (grid > p.num_tiles) grid = p.num_tiles;
+    k_gemm_mxf8<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? 0 : 2 + static_cast<int>(e);
+}
+
+}  // namespace fp8hg

@@ -1,0 +1,44 @@
+// Launchers shared between the C-ABI layer (api.cu) and the kernel files.
+// Arguments are validated by the caller; these only configure and launch.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace fp8hg {
+
+cudaError_t launch_quant_token(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
+                               int group, int transpose, int fmt, uint8_t *q, int64_t ld_q,
+                               uint8_t *s, int64_t ld_s, cudaStream_t stream);
+
+cudaError_t launch_quant_mx32(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
+                              uint8_t *q, int64_t ld_q, uint8_t *s, int64_t ld_s,
+                              unsigned long long *cnt, cudaStream_t stream);
+
+cudaError_t launch_quant_block128(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
+                                  int fmt, uint8_t *q, int64_t ld_q, uint8_t *s, int64_t ld_s,
+                                  uint8_t *qt, int64_t ld_qt, uint8_t *st, int64_t ld_st,
+                                  cudaStream_t stream);
+
+struct GemmArgs {
+    const uint8_t *a_codes, *b_codes;
+    const uint8_t *a_scale, *b_scale;
+    int64_t M, N, K;
+    int64_t lda, ldb, ld_sa, ld_sb;
+    int fmt_a, fmt_b, gran_a, gran_b;
+    void *c;
+    int64_t ldc;
+    int out_fp32, accumulate;
+    uint64_t wait_limit_ns;
+    int inject_fault;
+    unsigned int *err;  // device error word
+};
+
+// Returns 0 on success, 1 if the tensor maps could not be encoded, or a
+// cudaError_t + 2 on a launch failure.
+int launch_gemm_scaled(const GemmArgs &args, cudaStream_t stream);
+
+// Device address of the error word of the current device (null on failure).
+unsigned int *device_error_word();
+
+}  // namespace fp8hg

@@ -1,0 +1,427 @@
+// Quantizer kernels: BF16 -> FP8 codes + UE8M0 / E8M0 scale bytes.
+//
+// All four are HBM-bound streaming kernels (3 bytes of traffic per element:
+// 2 read, 1 written, plus one scale byte per group).  Each reads every input
+// element exactly once with 16-byte vector loads, reduces the group amax with
+// warp shuffles (integer max on BF16 patterns), derives the scale exponent
+// from the amax's bit fields and casts with the hardware RNE FP8 conversion.
+//
+//  k_quant_row       one scale per token ("A Comprehensive FP8 Training
+//                    Recipe ...", "What carries the argument": token-wise
+//                    activation scales).  One CTA per row, the row kept in
+//                    registers between the amax and the cast.
+//  k_quant_groups    one scale per 1x128 group (tiled activations) or per
+//                    32-element MX block ("Characterization and Mitigation of
+//                    Training Instabilities in Microscaling Formats", "What
+//                    carries the argument").  A group is 16 (resp. 4) lanes.
+//  k_quant_t         1x128 groups along the ROWS (tokens) of x, written
+//                    transposed: the weight-gradient GEMM's operand layout.
+//  k_quant_block128  one scale per 128x128 block (block-wise weights), with
+//                    an optional transposed copy for the data-gradient GEMM.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+#include "quant_math.cuh"
+
+namespace fp8hg {
+
+// ------------------------------------------------------------------ per row
+template <int FMT, int NV>
+__global__ void __launch_bounds__(512) k_quant_row(const uint16_t *__restrict__ x, int nvec,
+                                                   int64_t ld_x, uint8_t *__restrict__ q,
+                                                   int64_t ld_q, uint8_t *__restrict__ s,
+                                                   int64_t ld_s) {
+    __shared__ uint32_t red[16];
+    __shared__ uint32_t bcast;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const int64_t row = blockIdx.x;
+    const uint4 *xr = reinterpret_cast<const uint4 *>(x + row * ld_x);
+    uint4 v[NV];
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int c = tid + i * blockDim.x;
+        if (c < nvec) {
+            v[i] = ptx::ld_stream_v4(xr + c);
+            m = max(m, bf16_abs_max8(v[i]));
+        }
+    }
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t t = (lane < nwarps) ? red[lane] : 0u;
+        t = __reduce_max_sync(0xFFFFFFFFu, t);
+        if (lane == 0) bcast = t;
+    }
+    __syncthreads();
+    float mul;
+    const uint32_t sbyte = group_scale<FMT, false>(bcast, mul);
+    uint2 *qr = reinterpret_cast<uint2 *>(q + row * ld_q);
+    uint32_t unused = 0;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int c = tid + i * blockDim.x;
+        if (c < nvec) {
+            qr[c] = (sbyte == 0xFFu) ? make_uint2(kNanCodes, kNanCodes)
+                                     : quant8<FMT, false>(v[i], mul, unused);
+        }
+    }
+    if (tid == 0) s[row * ld_s] = static_cast<uint8_t>(sbyte);
+}
+
+// Rows too long to keep in registers: the amax pass and the cast pass read the
+// row twice (the second read is served from L2).
+template <int FMT>
+__global__ void __launch_bounds__(512) k_quant_row_2pass(const uint16_t *__restrict__ x, int nvec,
+                                                         int64_t ld_x, uint8_t *__restrict__ q,
+                                                         int64_t ld_q, uint8_t *__restrict__ s,
+                                                         int64_t ld_s) {
+    __shared__ uint32_t red[16];
+    __shared__ uint32_t bcast;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const int64_t row = blockIdx.x;
+    const uint4 *xr = reinterpret_cast<const uint4 *>(x + row * ld_x);
+    uint32_t m = 0;
+    for (int c = tid; c < nvec; c += blockDim.x) m = max(m, bf16_abs_max8(xr[c]));
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t t = (lane < nwarps) ? red[lane] : 0u;
+        t = __reduce_max_sync(0xFFFFFFFFu, t);
+        if (lane == 0) bcast = t;
+    }
+    __syncthreads();
+    float mul;
+    const uint32_t sbyte = group_scale<FMT, false>(bcast, mul);
+    uint2 *qr = reinterpret_cast<uint2 *>(q + row * ld_q);
+    uint32_t unused = 0;
+    for (int c = tid; c < nvec; c += blockDim.x) {
+        qr[c] = (sbyte == 0xFFu) ? make_uint2(kNanCodes, kNanCodes)
+                                 : quant8<FMT, false>(xr[c], mul, unused);
+    }
+    if (tid == 0) s[row * ld_s] = static_cast<uint8_t>(sbyte);
+}
+
+// ------------------------------------------------------ groups along a row
+// GV = 16-byte vectors per group: 16 (1x128) or 4 (MX 32).  Lanes
+// [g*GV, g*GV + GV) of a warp hold one group; the loop is warp-uniform so
+// every lane reaches the shuffles.
+template <int FMT, int GV, bool MX, bool COUNT>
+__global__ void __launch_bounds__(256) k_quant_groups(const uint16_t *__restrict__ x, int64_t rows,
+                                                      int64_t vpr, int64_t ld_x,
+                                                      uint8_t *__restrict__ q, int64_t ld_q,
+                                                      uint8_t *__restrict__ s, int64_t ld_s,
+                                                      unsigned long long *__restrict__ cnt) {
+    constexpr int U = 4;
+    const int lane = threadIdx.x & 31;
+    const int64_t total = rows * vpr;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t wbase0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
+    uint32_t nsat = 0;
+    for (int64_t wbase = wbase0; wbase < total; wbase += stride * U) {
+        uint4 v[U];
+        int64_t row[U], cv[U];
+        bool ok[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t idx = wbase + lane + u * stride;
+            ok[u] = idx < total;
+            row[u] = ok[u] ? idx / vpr : 0;
+            cv[u] = idx - row[u] * vpr;
+            if (ok[u]) v[u] = ptx::ld_stream_v4(x + row[u] * ld_x + cv[u] * 8);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            uint32_t m = ok[u] ? bf16_abs_max8(v[u]) : 0u;
+#pragma unroll
+            for (int o = GV / 2; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+            if (ok[u]) {
+                float mul;
+                const uint32_t sbyte = group_scale<FMT, MX>(m, mul);
+                uint2 out = (sbyte == 0xFFu) ? make_uint2(kNanCodes, kNanCodes)
+                                             : quant8<FMT, COUNT>(v[u], mul, nsat);
+                *reinterpret_cast<uint2 *>(q + row[u] * ld_q + cv[u] * 8) = out;
+                if ((lane % GV) == 0) s[row[u] * ld_s + cv[u] / GV] = static_cast<uint8_t>(sbyte);
+            }
+        }
+    }
+    if constexpr (COUNT) {
+        nsat = __reduce_add_sync(0xFFFFFFFFu, nsat);
+        if (lane == 0 && nsat) atomicAdd(cnt, static_cast<unsigned long long>(nsat));
+    }
+}
+
+// ------------------------------------------- 1x128 along rows, transposed out
+// One CTA per 128-row x 64-column tile of x.  The tile is staged in shared
+// memory, each column's amax over the 128 rows is reduced, and the codes are
+// staged again so that the transposed output rows (64 of 128 bytes) are
+// written with full, coalesced 16-byte stores.
+constexpr int kTC = 64;  // tile columns
+template <int FMT>
+__global__ void __launch_bounds__(256) k_quant_t(const uint16_t *__restrict__ x, int64_t ld_x,
+                                                 uint8_t *__restrict__ qt, int64_t ld_q,
+                                                 uint8_t *__restrict__ st, int64_t ld_s) {
+    __shared__ __align__(16) uint16_t tile[128][kTC + 8];
+    __shared__ __align__(16) uint8_t codes[kTC][128 + 16];
+    __shared__ uint32_t red[4][kTC];
+    const int tid = threadIdx.x;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kTC;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int idx = tid + 256 * i;
+        const int r = idx >> 3, cv = idx & 7;
+        const uint4 v = ptx::ld_stream_v4(x + (r0 + r) * ld_x + c0 + cv * 8);
+        *reinterpret_cast<uint4 *>(&tile[r][cv * 8]) = v;
+    }
+    __syncthreads();
+    const int c = tid & (kTC - 1), rq = tid >> 6;
+    uint32_t vals[16];  // this thread's 32 elements, two per word
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t lo = tile[rq * 32 + 2 * i][c];
+        const uint32_t hi = tile[rq * 32 + 2 * i + 1][c];
+        vals[i] = lo | (hi << 16);
+        m = max(m, max(lo & 0x7FFFu, hi & 0x7FFFu));
+    }
+    red[rq][c] = m;
+    __syncthreads();
+    m = max(max(red[0][c], red[1][c]), max(red[2][c], red[3][c]));
+    float mul;
+    const uint32_t sbyte = group_scale<FMT, false>(m, mul);
+    uint32_t w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        if (sbyte == 0xFFu) {
+            w[j] = kNanCodes;
+        } else {
+            const uint32_t a = vals[2 * j], b = vals[2 * j + 1];
+            const uint32_t p0 = cvt2<FMT>(__uint_as_float(a << 16) * mul,
+                                          __uint_as_float(a & 0xFFFF0000u) * mul);
+            const uint32_t p1 = cvt2<FMT>(__uint_as_float(b << 16) * mul,
+                                          __uint_as_float(b & 0xFFFF0000u) * mul);
+            w[j] = p0 | (p1 << 16);
+        }
+    }
+    *reinterpret_cast<uint4 *>(&codes[c][rq * 32]) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4 *>(&codes[c][rq * 32 + 16]) = make_uint4(w[4], w[5], w[6], w[7]);
+    if (rq == 0) st[(c0 + c) * ld_s + blockIdx.y] = static_cast<uint8_t>(sbyte);
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int idx = tid + 256 * i;
+        const int row = idx >> 3, ch = idx & 7;
+        *reinterpret_cast<uint4 *>(qt + (c0 + row) * ld_q + r0 + ch * 16) =
+            *reinterpret_cast<const uint4 *>(&codes[row][ch * 16]);
+    }
+}
+
+// ------------------------------------------------------------ 128x128 blocks
+// 4x4 byte transpose of four 32-bit rows: result word j = byte j of each row.
+__device__ __forceinline__ void transpose4x4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t (&c)[4]) {
+    const uint32_t t0 = __byte_perm(a0, a1, 0x5140), t1 = __byte_perm(a0, a1, 0x7362);
+    const uint32_t t2 = __byte_perm(a2, a3, 0x5140), t3 = __byte_perm(a2, a3, 0x7362);
+    c[0] = __byte_perm(t0, t2, 0x5410);
+    c[1] = __byte_perm(t0, t2, 0x7632);
+    c[2] = __byte_perm(t1, t3, 0x5410);
+    c[3] = __byte_perm(t1, t3, 0x7632);
+}
+
+// One CTA per 128x128 block; thread (rsub, csub) owns an 8x8 sub-block.
+template <int FMT, bool TRANS>
+__global__ void __launch_bounds__(256) k_quant_block128(const uint16_t *__restrict__ x,
+                                                        int64_t ld_x, uint8_t *__restrict__ q,
+                                                        int64_t ld_q, uint8_t *__restrict__ s,
+                                                        int64_t ld_s, uint8_t *__restrict__ qt,
+                                                        int64_t ld_qt, uint8_t *__restrict__ st,
+                                                        int64_t ld_st) {
+    __shared__ uint32_t red[8];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t rb = blockIdx.y, cb = blockIdx.x;
+    const int rsub = tid >> 4, csub = tid & 15;
+    const int64_t r_first = rb * 128 + rsub * 8, c_first = cb * 128 + csub * 8;
+    const uint16_t *xb = x + r_first * ld_x + c_first;
+    uint4 v[8];
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        v[i] = ptx::ld_stream_v4(xb + i * ld_x);
+        m = max(m, bf16_abs_max8(v[i]));
+    }
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    m = red[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) m = max(m, red[i]);
+    float mul;
+    const uint32_t sbyte = group_scale<FMT, false>(m, mul);
+    uint2 o[8];
+    uint32_t unused = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        o[i] = (sbyte == 0xFFu) ? make_uint2(kNanCodes, kNanCodes)
+                                : quant8<FMT, false>(v[i], mul, unused);
+        *reinterpret_cast<uint2 *>(q + (r_first + i) * ld_q + c_first) = o[i];
+    }
+    if (tid == 0) {
+        s[rb * ld_s + cb] = static_cast<uint8_t>(sbyte);
+        if constexpr (TRANS) st[cb * ld_st + rb] = static_cast<uint8_t>(sbyte);
+    }
+    if constexpr (TRANS) {
+        uint32_t lo03[4], lo47[4], hi03[4], hi47[4];
+        transpose4x4(o[0].x, o[1].x, o[2].x, o[3].x, lo03);
+        transpose4x4(o[4].x, o[5].x, o[6].x, o[7].x, lo47);
+        transpose4x4(o[0].y, o[1].y, o[2].y, o[3].y, hi03);
+        transpose4x4(o[4].y, o[5].y, o[6].y, o[7].y, hi47);
+        uint8_t *qtb = qt + c_first * ld_qt + r_first;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            *reinterpret_cast<uint2 *>(qtb + j * ld_qt) = make_uint2(lo03[j], lo47[j]);
+            *reinterpret_cast<uint2 *>(qtb + (j + 4) * ld_qt) = make_uint2(hi03[j], hi47[j]);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ launchers
+namespace {
+int g_num_sms[64] = {0};
+
+int num_sms() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (g_num_sms[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        g_num_sms[dev] = n > 0 ? n : 1;
+    }
+    return g_num_sms[dev];
+}
+
+template <int FMT>
+cudaError_t launch_row(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, uint8_t *q,
+                       int64_t ld_q, uint8_t *s, int64_t ld_s, cudaStream_t stream) {
+    const int nvec = static_cast<int>(cols / 8);
+    // choose NV (vectors per thread) and T (threads) so that T*NV covers the
+    // row with the least idle slots, T <= 512
+    const int nvs[5] = {1, 2, 4, 8, 16};
+    int best_nv = -1, best_t = 0;
+    int64_t best_waste = -1;
+    for (int k = 0; k < 5; ++k) {
+        const int nv = nvs[k];
+        int t = (nvec + nv - 1) / nv;
+        t = ((t + 31) / 32) * 32;
+        if (t > 512) continue;
+        if (t < 64 && nv > 1) continue;
+        const int64_t waste = static_cast<int64_t>(t) * nv - nvec;
+        if (best_nv < 0 || waste < best_waste) {
+            best_nv = nv;
+            best_t = t;
+            best_waste = waste;
+        }
+    }
+    const dim3 grid(static_cast<unsigned>(rows));
+    if (best_nv < 0) {
+        k_quant_row_2pass<FMT><<<grid, 512, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s);
+        return cudaGetLastError();
+    }
+    switch (best_nv) {
+    case 1: k_quant_row<FMT, 1><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
+    case 2: k_quant_row<FMT, 2><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
+    case 4: k_quant_row<FMT, 4><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
+    case 8: k_quant_row<FMT, 8><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
+    default: k_quant_row<FMT, 16><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
+    }
+    return cudaGetLastError();
+}
+
+template <int FMT, int GV, bool MX, bool COUNT>
+cudaError_t launch_groups(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, uint8_t *q,
+                          int64_t ld_q, uint8_t *s, int64_t ld_s, unsigned long long *cnt,
+                          cudaStream_t stream) {
+    const int64_t vpr = cols / 8;
+    const int64_t total = rows * vpr;
+    const int threads = 256;
+    int64_t blocks = (total + threads * 4 - 1) / (threads * 4);
+    const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    k_quant_groups<FMT, GV, MX, COUNT><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+        x, rows, vpr, ld_x, q, ld_q, s, ld_s, cnt);
+    return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_quant_token(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
+                               int group, int transpose, int fmt, uint8_t *q, int64_t ld_q,
+                               uint8_t *s, int64_t ld_s, cudaStream_t stream) {
+    if (rows == 0 || cols == 0) return cudaSuccess;
+    if (transpose) {
+        const dim3 grid(static_cast<unsigned>(cols / kTC), static_cast<unsigned>(rows / 128));
+        if (fmt == FMT_E4M3) k_quant_t<FMT_E4M3><<<grid, 256, 0, stream>>>(x, ld_x, q, ld_q, s, ld_s);
+        else k_quant_t<FMT_E5M2><<<grid, 256, 0, stream>>>(x, ld_x, q, ld_q, s, ld_s);
+        return cudaGetLastError();
+    }
+    if (group == 0) {
+        return fmt == FMT_E4M3 ? launch_row<FMT_E4M3>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream)
+                               : launch_row<FMT_E5M2>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream);
+    }
+    return fmt == FMT_E4M3
+               ? launch_groups<FMT_E4M3, 16, false, false>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
+                                                           nullptr, stream)
+               : launch_groups<FMT_E5M2, 16, false, false>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
+                                                           nullptr, stream);
+}
+
+cudaError_t launch_quant_mx32(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
+                              uint8_t *q, int64_t ld_q, uint8_t *s, int64_t ld_s,
+                              unsigned long long *cnt, cudaStream_t stream) {
+    if (rows == 0 || cols == 0) return cudaSuccess;
+    if (cnt) {
+        return fmt == FMT_E4M3
+                   ? launch_groups<FMT_E4M3, 4, true, true>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
+                                                            cnt, stream)
+                   : launch_groups<FMT_E5M2, 4, true, true>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
+                                                            cnt, stream);
+    }
+    return fmt == FMT_E4M3
+               ? launch_groups<FMT_E4M3, 4, true, false>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
+                                                         nullptr, stream)
+               : launch_groups<FMT_E5M2, 4, true, false>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
+                                                         nullptr, stream);
+}
+
+cudaError_t launch_quant_block128(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
+                                  int fmt, uint8_t *q, int64_t ld_q, uint8_t *s, int64_t ld_s,
+                                  uint8_t *qt, int64_t ld_qt, uint8_t *st, int64_t ld_st,
+                                  cudaStream_t stream) {
+    if (rows == 0 || cols == 0) return cudaSuccess;
+    const dim3 grid(static_cast<unsigned>(cols / 128), static_cast<unsigned>(rows / 128));
+    if (qt) {
+        if (fmt == FMT_E4M3)
+            k_quant_block128<FMT_E4M3, true><<<grid, 256, 0, stream>>>(x, ld_x, q, ld_q, s, ld_s, qt,
+                                                                       ld_qt, st, ld_st);
+        else
+            k_quant_block128<FMT_E5M2, true><<<grid, 256, 0, stream>>>(x, ld_x, q, ld_q, s, ld_s, qt,
+                                                                       ld_qt, st, ld_st);
+    } else {
+        if (fmt == FMT_E4M3)
+            k_quant_block128<FMT_E4M3, false><<<grid, 256, 0, stream>>>(x, ld_x, q, ld_q, s, ld_s,
+                                                                        nullptr, 0, nullptr, 0);
+        else
+            k_quant_block128<FMT_E5M2, false><<<grid, 256, 0, stream>>>(x, ld_x, q, ld_q, s, ld_s,
+                                                                        nullptr, 0, nullptr, 0);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace fp8hg

@@ -1,0 +1,253 @@
+/*
+ * fp8hg — hybrid-granularity FP8 quantization and block-scaled FP8 GEMM for
+ * GB300 (sm_103a).  Plain C ABI: raw pointers, sizes and enums, no C++ or
+ * framework types.
+ *
+ * What the library computes
+ * -------------------------
+ * The data-parallel hot path of the FP8 training recipe in "A Comprehensive
+ * FP8 Training Recipe for Reasoning-Enhanced Language Models" ("Core claim",
+ * "What carries the argument"): weights are quantized with one scale per
+ * 128x128 block, activations with one scale per token (or per 1x128 group in
+ * the tiled variant); every scale is an exponent-only UE8M0 power of two
+ * rounded UP, so that amax/scale never exceeds the FP8 format's largest value;
+ * the FP8 GEMMs of the forward and backward passes consume the codes and
+ * scales and accumulate in FP32.  An MXFP8 mode ("Characterization and
+ * Mitigation of Training Instabilities in Microscaling Formats", "What carries
+ * the argument") shares one E8M0 scale per 32 elements, taken as
+ * floor(log2 amax) - emax, and clamps scaled magnitudes beyond the largest
+ * code.  The codes follow "FP8 Formats for Deep Learning" (abstract / core
+ * claim): E4M3 without infinities and with a single NaN pattern, E5M2 with
+ * IEEE-754 specials, round to nearest even.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers on the current CUDA device.  The
+ *    caller allocates and owns every buffer; the library never allocates or
+ *    frees memory and never synchronizes, except in fp8hg_get_device_error.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *    enqueued asynchronously; the entry points return once it is launched.
+ *  - BF16 inputs are passed as uint16_t bit patterns, row-major with a row
+ *    stride `ld_*` in ELEMENTS.  FP8 codes and scale bytes are uint8_t,
+ *    row-major with row strides in BYTES.
+ *  - Scale byte b means 2^(b - 127) (UE8M0 / E8M0); b = 0xFF marks a group
+ *    that held a NaN or an infinity, in which case every code of the group is
+ *    0x7F (a NaN in both encodings).  A dequantized element is
+ *    decode(code) * 2^(b - 127).
+ *  - Return value: an fp8hg_status.  Argument, shape and alignment errors are
+ *    reported before anything is launched and leave every buffer untouched.
+ *    FP8HG_ERR_CUDA reports a failed launch (the CUDA error is left for the
+ *    caller to query).  Errors raised inside a running kernel (a bounded wait
+ *    that expired) are recorded in a device error word and reported by
+ *    fp8hg_get_device_error.
+ *  - Thread safety: entry points keep no host state and may be called from
+ *    several threads.  Calls that write the same output buffers must be
+ *    ordered by the caller (same stream or events).
+ */
+#ifndef FP8HG_H
+#define FP8HG_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8HG_OK = 0,
+    FP8HG_ERR_INVALID_ARG = 1, /* null pointer, bad enum, negative size */
+    FP8HG_ERR_ALIGNMENT = 2,   /* pointer or stride misaligned */
+    FP8HG_ERR_SHAPE = 3,       /* sizes not multiples of the tile / group */
+    FP8HG_ERR_UNSUPPORTED = 4, /* valid request the library does not offer */
+    FP8HG_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
+    FP8HG_ERR_TIMEOUT = 6      /* a kernel's bounded wait expired */
+} fp8hg_status;
+
+typedef enum { FP8HG_E4M3 = 0, FP8HG_E5M2 = 1 } fp8hg_format;
+
+typedef enum {
+    FP8HG_GRAN_ROW = 0,      /* one scale per row (per token) */
+    FP8HG_GRAN_1x128 = 1,    /* one scale per 128 consecutive K elements of a row */
+    FP8HG_GRAN_128x128 = 2,  /* one scale per 128x128 block (weights) */
+    FP8HG_GRAN_MX32 = 3      /* MXFP8: one scale per 32 consecutive K elements */
+} fp8hg_gran;
+
+typedef enum { FP8HG_FPROP = 0, FP8HG_DGRAD = 1, FP8HG_WGRAD = 2 } fp8hg_op;
+
+typedef enum { FP8HG_OUT_BF16 = 0, FP8HG_OUT_FP32 = 1 } fp8hg_out;
+
+/*
+ * fp8_quant_token — per-token (group = 0) or per-1x128-group (group = 128)
+ * activation quantizer with UE8M0 round-up scales.
+ *
+ * Passage: "A Comprehensive FP8 Training Recipe ...", "What carries the
+ * argument" (token-wise activation scales; E8M0 exponent-only scales rounded
+ * up to a power of two); the 1x128 tiled variant and the transposed wgrad
+ * re-quantization are this library's reading of where the recipe's
+ * activations go in the weight-gradient GEMM.
+ *
+ * For each group the scale exponent is the smallest e in [-127, 127] with
+ * amax <= FMAX * 2^e (FMAX = 448 for E4M3, 57344 for E5M2; amax = 0 gives
+ * -127), and each code is the round-to-nearest-even FP8 encoding of
+ * x * 2^-e, which never overflows.
+ *
+ *   x         [rows, cols] BF16, row stride ld_x elements
+ *   group     0 (whole row) or 128
+ *   transpose 0: q [rows, cols] (ld_q bytes), scale [rows, G] (ld_s), G = 1
+ *                or cols/128.
+ *             1 (group must be 128): the groups are 128 consecutive ROWS of
+ *                one column, and the result is written transposed:
+ *                q [cols, rows] (ld_q), scale [cols, rows/128] (ld_s).  This
+ *                is the operand layout of the weight-gradient GEMM, whose
+ *                contraction runs over tokens.
+ *   fmt       FP8HG_E4M3 or FP8HG_E5M2
+ * Requirements: transpose = 0: cols % 128 == 0; transpose = 1: rows % 128 == 0
+ * and cols % 64 == 0.  x and q 16-byte aligned, ld_x % 8 == 0,
+ * ld_q % 16 == 0; ld_s >= number of scale columns.  rows or cols may be 0.
+ */
+int fp8_quant_token(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int group,
+                    int transpose, int fmt, uint8_t *q, int64_t ld_q, uint8_t *scale,
+                    int64_t ld_s, void *stream);
+
+/*
+ * fp8_quant_block128 — weight quantizer, one UE8M0 round-up scale per
+ * 128x128 block (the whole block's amax is taken before any element is cast).
+ *
+ * Passage: "A Comprehensive FP8 Training Recipe ...", "What carries the
+ * argument" (block-wise weight scales); block size 128x128 is this library's
+ * reading (the recipe leaves the block size unreported).
+ *
+ *   x        [rows, cols] BF16 (ld_x elements)
+ *   q        [rows, cols] codes (ld_q bytes)
+ *   scale    [rows/128, cols/128] (ld_s bytes)
+ *   q_t      optional (may be NULL): the same codes transposed, [cols, rows]
+ *            (ld_qt bytes) — the B operand of the data-gradient GEMM
+ *   scale_t  optional (must be non-NULL iff q_t is): the scale grid transposed,
+ *            [cols/128, rows/128] (ld_st bytes)
+ * Requirements: rows % 128 == 0, cols % 128 == 0; x, q, q_t 16-byte aligned;
+ * ld_x % 8 == 0, ld_q % 16 == 0, ld_qt % 16 == 0.
+ */
+int fp8_quant_block128(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
+                       uint8_t *q, int64_t ld_q, uint8_t *scale, int64_t ld_s, uint8_t *q_t,
+                       int64_t ld_qt, uint8_t *scale_t, int64_t ld_st, void *stream);
+
+/*
+ * fp8_quant_mx32 — MXFP8 quantizer: 32 consecutive elements of a row share
+ * one E8M0 scale 2^e with e = floor(log2 amax) - emax (emax = 8 for E4M3,
+ * 15 for E5M2), clamped to [-127, 127]; codes are the saturating
+ * round-to-nearest-even encoding of x * 2^-e (magnitudes beyond the largest
+ * code clamp to it).
+ *
+ * Passage: "Characterization and Mitigation of Training Instabilities in
+ * Microscaling Formats", "What carries the argument" (shared power-of-two
+ * block scale; values beyond the representable limit clamp to the largest
+ * code).  Block size 32 is this library's reading.
+ *
+ *   q            [rows, cols] codes (ld_q bytes); scale [rows, cols/32] (ld_s)
+ *   clamp_count  optional device pointer; if non-NULL, the number of elements
+ *                whose scaled magnitude exceeded the largest value is ADDED
+ *                to *clamp_count (the caller zeroes it).
+ * Requirements: cols % 32 == 0; x, q 16-byte aligned; ld_x % 8 == 0,
+ * ld_q % 16 == 0.
+ */
+int fp8_quant_mx32(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
+                   uint8_t *q, int64_t ld_q, uint8_t *scale, int64_t ld_s,
+                   unsigned long long *clamp_count, void *stream);
+
+/*
+ * One quantized GEMM operand: `rows` rows of `k` FP8 codes, K-contiguous.
+ *   codes     device pointer, 16-byte aligned, row stride ld bytes (ld % 16 == 0)
+ *   scale     device pointer to the scale bytes of `gran`:
+ *               ROW      [rows]         at scale[r * ld_scale]
+ *               1x128    [rows, k/128]  at scale[r * ld_scale + k/128]
+ *               128x128  [rows/128, k/128]
+ *               MX32     [rows, k/32]
+ *             For 1x128, 128x128 and MX32 the GEMM reads the scale bytes four
+ *             at a time: scale must be 4-byte aligned, ld_scale % 4 == 0 and
+ *             ld_scale >= the column count rounded up to a multiple of 4
+ *             (the padding bytes are read and ignored).
+ *   fmt       FP8HG_E4M3 / FP8HG_E5M2;  gran  fp8hg_gran
+ */
+typedef struct {
+    const uint8_t *codes;
+    const uint8_t *scale;
+    int64_t rows;
+    int64_t k;
+    int64_t ld;
+    int64_t ld_scale;
+    int32_t fmt;
+    int32_t gran;
+} fp8hg_operand;
+
+/*
+ * fp8_gemm_scaled — C = A * B^T on block-scaled FP8 operands, FP32
+ * accumulation on the tensor cores, BF16 or FP32 output.
+ *
+ *   C[i, j] = sum_k (qa[i,k] * 2^ea(i,k)) * (qb[j,k] * 2^eb(j,k))
+ *
+ * Passage: "A Comprehensive FP8 Training Recipe ...", referee summary and
+ * "What carries the argument" (E4M3 GEMMs in the forward and backward passes
+ * over block-scaled weights and token-scaled activations; FP32 master
+ * weights and weight gradients).  All three GEMMs of a linear layer reduce to
+ * this one form once the quantizers have put both operands K-contiguous:
+ *   FPROP  Y  = X W^T      A = X  [M, K] (ROW or 1x128), B = W  [N, K] (128x128)
+ *   DGRAD  dX = dY W       A = dY [M, N] (ROW or 1x128), B = W^T [K, N] (128x128,
+ *                          the transposed copy from fp8_quant_block128)
+ *   WGRAD  dW = dY^T X     A = dY^T [N, M] (1x128), B = X^T [K, M] (1x128), both
+ *                          from fp8_quant_token(transpose = 1)
+ * MX32 x MX32 is accepted under any op.
+ *
+ *   op          fp8hg_op; only selects which granularity pairs are accepted
+ *   a, b        operands; M = a->rows, N = b->rows, K = a->k = b->k
+ *   c           device output [M, N], row stride ldc ELEMENTS, 16-byte aligned,
+ *               ldc % 8 == 0 (BF16) or % 4 == 0 (FP32)
+ *   out         FP8HG_OUT_BF16 (round to nearest even) or FP8HG_OUT_FP32
+ *   accumulate  0: C = A B^T;  1: C = C + A B^T (gradient accumulation)
+ * Requirements: M % 128 == 0, N % 128 == 0, K % 128 == 0, K > 0.
+ * Scale bytes of 0xFF (non-finite groups) make the affected outputs NaN.
+ */
+int fp8_gemm_scaled(int op, const fp8hg_operand *a, const fp8hg_operand *b, void *c,
+                    int64_t ldc, int out, int accumulate, void *stream);
+
+/*
+ * Options for fp8_gemm_scaled_ex.
+ *   wait_limit_ns  upper bound on any single pipeline wait inside the GEMM
+ *                  kernel (0 = the default, 2 s).  When a wait runs out the
+ *                  kernel stops, drains its in-flight copies, releases its
+ *                  tensor memory, records FP8HG_ERR_TIMEOUT in the device
+ *                  error word and returns; C is then unspecified.
+ *   inject_fault   0 = none.  1 = the scale-loading warp withholds its first
+ *                  arrival, so the first wait of the MMA warp can never
+ *                  complete: a host-chosen, GPU-safe way to exercise the
+ *                  timeout path in tests.
+ */
+typedef struct {
+    uint64_t wait_limit_ns;
+    int32_t inject_fault;
+    int32_t reserved;
+} fp8hg_gemm_opts;
+
+/* fp8_gemm_scaled with options (opts may be NULL = defaults). */
+int fp8_gemm_scaled_ex(int op, const fp8hg_operand *a, const fp8hg_operand *b, void *c,
+                       int64_t ldc, int out, int accumulate, const fp8hg_gemm_opts *opts,
+                       void *stream);
+
+/*
+ * fp8hg_get_device_error — synchronizes `stream`, then reads and clears the
+ * device error word of the current device.  Returns FP8HG_OK,
+ * FP8HG_ERR_TIMEOUT (a kernel's bounded wait expired since the last call) or
+ * FP8HG_ERR_CUDA (the synchronization itself failed).
+ */
+int fp8hg_get_device_error(void *stream);
+
+/* Human-readable name of an fp8hg_status value (static storage). */
+const char *fp8hg_status_str(int status);
+
+/* ABI version of this header / library: (major << 16) | minor. */
+int fp8hg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8HG_H */

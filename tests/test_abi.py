@@ -1,0 +1,92 @@
+"""The C-ABI library loads without a GPU, exports every function the header
+declares, and rejects bad arguments before launching anything.  No call here
+reaches the device."""
+import ctypes
+
+import pytest
+
+import fp8_hybrid_granularity_gb300 as fp8hg
+from fp8_hybrid_granularity_gb300 import Operand, E4M3, GRAN_ROW, GRAN_1x128, GRAN_128x128, GRAN_MX32
+
+EXPECTED = {"fp8_quant_token", "fp8_quant_block128", "fp8_quant_mx32", "fp8_gemm_scaled",
+            "fp8_gemm_scaled_ex", "fp8hg_get_device_error", "fp8hg_status_str", "fp8hg_version"}
+
+OK, INVALID, ALIGN, SHAPE, UNSUP = 0, 1, 2, 3, 4
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return fp8hg.load_library()
+
+
+def test_header_declares_the_expected_api():
+    assert set(fp8hg.declared_functions()) == EXPECTED
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in fp8hg.declared_functions():
+        assert hasattr(lib, name), name
+    assert lib.fp8hg_version() == (1 << 16)
+
+
+def test_status_strings(lib):
+    for code, name in fp8hg.STATUS.items():
+        assert lib.fp8hg_status_str(code).decode() == name
+    assert lib.fp8hg_status_str(99).decode() == "FP8HG_UNKNOWN_STATUS"
+
+
+def test_quant_token_validation(lib):
+    q = lib.fp8_quant_token
+    assert q(None, 4, 128, 128, 0, 0, E4M3, FAKE, 128, FAKE, 1, None) == INVALID
+    assert q(FAKE, 4, 128, 128, 64, 0, E4M3, FAKE, 128, FAKE, 1, None) == INVALID     # group
+    assert q(FAKE, 4, 128, 128, 0, 0, 7, FAKE, 128, FAKE, 1, None) == INVALID         # fmt
+    assert q(FAKE + 8, 4, 128, 128, 0, 0, E4M3, FAKE, 128, FAKE, 1, None) == ALIGN    # x align
+    assert q(FAKE, 4, 128, 130, 0, 0, E4M3, FAKE, 128, FAKE, 1, None) == ALIGN        # ld_x
+    assert q(FAKE, 4, 100, 104, 0, 0, E4M3, FAKE, 112, FAKE, 1, None) == SHAPE        # cols
+    assert q(FAKE, 4, 128, 128, 0, 1, E4M3, FAKE, 128, FAKE, 1, None) == UNSUP        # ROW^T
+    assert q(FAKE, 100, 128, 128, 128, 1, E4M3, FAKE, 128, FAKE, 1, None) == SHAPE    # rows%128
+    assert q(FAKE, 4, 256, 128, 0, 0, E4M3, FAKE, 256, FAKE, 1, None) == INVALID      # ld_x < cols
+    assert q(FAKE, 4, 256, 256, 128, 0, E4M3, FAKE, 256, FAKE, 1, None) == INVALID    # ld_s < 2
+
+
+def test_block128_and_mx_validation(lib):
+    b = lib.fp8_quant_block128
+    assert b(FAKE, 100, 128, 128, E4M3, FAKE, 128, FAKE, 1, None, 0, None, 0, None) == SHAPE
+    assert b(FAKE, 128, 128, 128, E4M3, FAKE, 128, FAKE, 1, FAKE, 128, None, 0, None) == INVALID
+    assert b(FAKE, 128, 128, 128, E4M3, FAKE, 128, FAKE, 1, FAKE + 4, 128, FAKE, 1, None) == ALIGN
+    m = lib.fp8_quant_mx32
+    assert m(FAKE, 4, 48, 48, E4M3, FAKE, 48, FAKE, 2, None, None) == SHAPE
+    assert m(FAKE, 4, 64, 64, E4M3, FAKE, 64, FAKE, 2, FAKE + 4, None) == ALIGN
+
+
+def _op(rows=256, k=256, gran=GRAN_1x128, ld=None, lds=4, fmt=E4M3, scale=FAKE):
+    return Operand(FAKE, scale, rows, k, ld if ld is not None else k, lds, fmt, gran)
+
+
+def test_gemm_validation(lib):
+    g = lib.fp8_gemm_scaled
+    C = FAKE
+
+    def call(a, b, op=0, ldc=256, out=0, acc=0, c=C):
+        return g(op, ctypes.byref(a), ctypes.byref(b), c, ldc, out, acc, None)
+
+    blk = dict(gran=GRAN_128x128, lds=4)
+    assert call(_op(rows=200), _op(**blk)) == SHAPE
+    assert call(_op(k=200), _op(k=200, **blk)) == SHAPE
+    assert call(_op(k=256), _op(k=384, **blk)) == SHAPE
+    assert call(_op(ld=264), _op(**blk)) == ALIGN                  # ld % 16
+    assert call(_op(lds=2), _op(**blk)) == ALIGN                   # ld_scale % 4
+    assert call(_op(scale=FAKE + 1), _op(**blk)) == ALIGN          # scale alignment
+    assert call(_op(), _op(gran=GRAN_1x128)) == UNSUP              # fprop needs block B
+    assert call(_op(gran=GRAN_MX32, lds=8), _op(**blk)) == UNSUP   # MX only with MX
+    assert call(_op(gran=GRAN_ROW, lds=1), _op(**blk), op=2) == UNSUP  # wgrad needs 1x128
+    assert call(_op(), _op(**blk), op=5) == INVALID
+    assert call(_op(), _op(**blk), out=3) == INVALID
+    assert call(_op(), _op(**blk), c=None) == INVALID
+    assert call(_op(), _op(**blk), c=FAKE + 8) == ALIGN
+    assert call(_op(), _op(**blk), ldc=100) == INVALID
+    assert call(_op(), _op(**blk), ldc=260) == ALIGN
+    a = _op()
+    a.fmt = 9
+    assert call(a, _op(**blk)) == INVALID
