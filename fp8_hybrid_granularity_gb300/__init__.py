@@ -152,68 +152,93 @@ def _check_bf16(x):
 
 
 def fp8_quant_token(x, group: int = 0, fmt: int = E4M3, transpose: bool = False,
-                    q=None, scale=None, stream=None) -> QTensor:
+                    out: Optional[QTensor] = None, stream=None) -> QTensor:
     """Per-token (group=0) or per-1x128 (group=128) UE8M0 quantization;
-    transpose=True quantizes 128-row groups and writes [cols, rows]."""
-    import torch
+    transpose=True quantizes 128-row groups and writes [cols, rows].
+    out: optional preallocated QTensor (e.g. from alloc_token)."""
     _check_bf16(x)
     rows, cols = x.shape
-    if transpose:
-        ncs = rows // 128
-        q = q if q is not None else torch.empty((cols, rows), dtype=torch.uint8, device=x.device)
-        scale = scale if scale is not None else torch.empty((cols, _round4(ncs)), dtype=torch.uint8,
-                                                            device=x.device)
-    else:
-        ncs = 1 if group == 0 else cols // 128
-        q = q if q is not None else torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
-        if scale is None:
-            scale = torch.empty((rows, 1 if group == 0 else _round4(ncs)), dtype=torch.uint8,
-                                device=x.device)
+    out = out if out is not None else alloc_token(rows, cols, group, fmt, transpose, x.device)
     rc = lib().fp8_quant_token(_ptr(x), rows, cols, x.stride(0), group, 1 if transpose else 0,
-                               fmt, _ptr(q), q.stride(0), _ptr(scale), scale.stride(0),
-                               _stream(stream))
+                               fmt, _ptr(out.codes), out.codes.stride(0), _ptr(out.scale),
+                               out.scale.stride(0), _stream(stream))
     _check(rc, "fp8_quant_token")
-    gran = GRAN_1x128 if (transpose or group == 128) else GRAN_ROW
-    return QTensor(q, scale, fmt, gran, ncs)
-
-
-def fp8_quant_block128(x, fmt: int = E4M3, transposed_copy: bool = False, stream=None):
-    """Per-128x128-block UE8M0 quantization; with transposed_copy=True also
-    returns the codes of x^T and the transposed scale grid."""
-    import torch
-    _check_bf16(x)
-    rows, cols = x.shape
-    dev = x.device
-    q = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
-    s = torch.empty((max(rows // 128, 1), _round4(max(cols // 128, 1))), dtype=torch.uint8, device=dev)
-    qt = st = None
-    if transposed_copy:
-        qt = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
-        st = torch.empty((max(cols // 128, 1), _round4(max(rows // 128, 1))), dtype=torch.uint8,
-                         device=dev)
-    rc = lib().fp8_quant_block128(_ptr(x), rows, cols, x.stride(0), fmt, _ptr(q), q.stride(0),
-                                  _ptr(s), s.stride(0), _ptr(qt), qt.stride(0) if qt is not None else 0,
-                                  _ptr(st), st.stride(0) if st is not None else 0, _stream(stream))
-    _check(rc, "fp8_quant_block128")
-    out = QTensor(q, s, fmt, GRAN_128x128, cols // 128)
-    if transposed_copy:
-        return out, QTensor(qt, st, fmt, GRAN_128x128, rows // 128)
     return out
 
 
-def fp8_quant_mx32(x, fmt: int = E4M3, clamp_count=None, stream=None) -> QTensor:
+def fp8_quant_block128(x, fmt: int = E4M3, transposed_copy: bool = False, out=None,
+                       out_t=None, stream=None):
+    """Per-128x128-block UE8M0 quantization; with transposed_copy=True also
+    returns the codes of x^T and the transposed scale grid.  out / out_t:
+    optional preallocated QTensors (e.g. from alloc_block128)."""
+    _check_bf16(x)
+    rows, cols = x.shape
+    if out is None or (transposed_copy and out_t is None):
+        out, out_t2 = alloc_block128(rows, cols, fmt, transposed_copy, x.device)
+        out_t = out_t if out_t is not None else out_t2
+    qt = out_t.codes if transposed_copy else None
+    st = out_t.scale if transposed_copy else None
+    rc = lib().fp8_quant_block128(_ptr(x), rows, cols, x.stride(0), fmt, _ptr(out.codes),
+                                  out.codes.stride(0), _ptr(out.scale), out.scale.stride(0),
+                                  _ptr(qt), qt.stride(0) if qt is not None else 0,
+                                  _ptr(st), st.stride(0) if st is not None else 0, _stream(stream))
+    _check(rc, "fp8_quant_block128")
+    if transposed_copy:
+        return out, out_t
+    return out
+
+
+def alloc_block128(rows: int, cols: int, fmt: int = E4M3, transposed_copy: bool = False,
+                   device="cuda"):
+    """Output buffers for fp8_quant_block128: (QTensor, QTensor or None)."""
+    import torch
+    q = torch.empty((rows, cols), dtype=torch.uint8, device=device)
+    s = torch.empty((max(rows // 128, 1), _round4(max(cols // 128, 1))), dtype=torch.uint8,
+                    device=device)
+    out = QTensor(q, s, fmt, GRAN_128x128, cols // 128)
+    if not transposed_copy:
+        return out, None
+    qt = torch.empty((cols, rows), dtype=torch.uint8, device=device)
+    st = torch.empty((max(cols // 128, 1), _round4(max(rows // 128, 1))), dtype=torch.uint8,
+                     device=device)
+    return out, QTensor(qt, st, fmt, GRAN_128x128, rows // 128)
+
+
+def alloc_token(rows: int, cols: int, group: int = 0, fmt: int = E4M3, transpose: bool = False,
+                device="cuda") -> QTensor:
+    """Output buffers for fp8_quant_token (shape of the result, padded scales)."""
+    import torch
+    if transpose:
+        q = torch.empty((cols, rows), dtype=torch.uint8, device=device)
+        s = torch.empty((cols, _round4(rows // 128)), dtype=torch.uint8, device=device)
+        return QTensor(q, s, fmt, GRAN_1x128, rows // 128)
+    q = torch.empty((rows, cols), dtype=torch.uint8, device=device)
+    if group == 0:
+        return QTensor(q, torch.empty((rows, 1), dtype=torch.uint8, device=device), fmt,
+                       GRAN_ROW, 1)
+    s = torch.empty((rows, _round4(cols // 128)), dtype=torch.uint8, device=device)
+    return QTensor(q, s, fmt, GRAN_1x128, cols // 128)
+
+
+def alloc_mx32(rows: int, cols: int, fmt: int = E4M3, device="cuda") -> QTensor:
+    import torch
+    q = torch.empty((rows, cols), dtype=torch.uint8, device=device)
+    s = torch.empty((rows, _round4(cols // 32)), dtype=torch.uint8, device=device)
+    return QTensor(q, s, fmt, GRAN_MX32, cols // 32)
+
+
+def fp8_quant_mx32(x, fmt: int = E4M3, clamp_count=None, out=None, stream=None) -> QTensor:
     """MXFP8 quantization (32-element blocks, saturating).  clamp_count: an
     optional int64 CUDA tensor of one element that receives (+=) the number
     of clamped elements."""
-    import torch
     _check_bf16(x)
     rows, cols = x.shape
-    q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
-    s = torch.empty((rows, _round4(cols // 32)), dtype=torch.uint8, device=x.device)
-    rc = lib().fp8_quant_mx32(_ptr(x), rows, cols, x.stride(0), fmt, _ptr(q), q.stride(0), _ptr(s),
-                              s.stride(0), _ptr(clamp_count), _stream(stream))
+    out = out if out is not None else alloc_mx32(rows, cols, fmt, x.device)
+    rc = lib().fp8_quant_mx32(_ptr(x), rows, cols, x.stride(0), fmt, _ptr(out.codes),
+                              out.codes.stride(0), _ptr(out.scale), out.scale.stride(0),
+                              _ptr(clamp_count), _stream(stream))
     _check(rc, "fp8_quant_mx32")
-    return QTensor(q, s, fmt, GRAN_MX32, cols // 32)
+    return out
 
 
 def fp8_gemm_scaled(op: int, a: QTensor, b: QTensor, out=None, out_dtype=None,

@@ -17,10 +17,14 @@
 //      1x128    the group's byte; all four 32-K MMAs of a 128-K stage use it
 //      128x128  the block's byte, the same for the tile's 128 rows
 //      MX32     four distinct bytes per 128-K stage
-//    The kernel reads the caller's compact scale arrays directly: a scale
-//    warp copies one 32-bit word per row and stage (cp.async, 4 bytes) into
-//    the shared-memory layout tcgen05.cp expects, and the MMA's scale-factor
-//    id picks the byte of that word that belongs to the stage.
+//    The kernel reads the caller's compact scale arrays directly.  A scale
+//    warp keeps, per row, four 32-bit scale words in registers and loads the
+//    next group's words while it writes the current ones: for 1x128 and
+//    128x128 a word holds the bytes of four consecutive 128-K blocks, so a
+//    group spans 16 k-blocks of look-ahead; for MX32 a word holds the four
+//    32-K slots of one block (groups of 4 k-blocks).  Per stage it writes the
+//    words into the shared-memory layout tcgen05.cp expects; the MMA's
+//    scale-factor id picks the byte of the word that belongs to the stage.
 //  * Tile 128 x 256 x 128 (one CTA per SM, 4-stage TMA/mbarrier pipeline,
 //    128-byte swizzled operand tiles), persistent over output tiles.
 //  * Warp roles (256 threads): warp 0 TMA producer, warp 1 MMA issuer and
@@ -72,7 +76,7 @@ enum { GRAN_ROW = 0, GRAN_1x128 = 1, GRAN_128x128 = 2, GRAN_MX32 = 3 };
 enum { WHO_PRODUCER = 1, WHO_MMA = 2, WHO_SCALES = 3, WHO_EPILOGUE = 4 };
 
 struct KParams {
-    int M, N, nk, num_nb, num_tiles;
+    int M, N, nk, num_mb, num_nb, num_tiles;
     int gran_a, gran_b;
     int out_fp32, accumulate, inject;
     const uint8_t *sa, *sb;
@@ -83,6 +87,19 @@ struct KParams {
     uint64_t wait_limit_ns;
     unsigned int *err;
 };
+
+// Output tile t -> (m-block, n-block).  Tiles are walked in groups of
+// kGroupM m-blocks, m fastest within a group: the CTAs resident at any moment
+// then share a few A panels and a few B panels, which stay in L2, instead of
+// sweeping every B panel once per m-block.
+constexpr int kGroupM = 16;
+__device__ __forceinline__ void tile_coords(int t, int num_mb, int num_nb, int &mb, int &nb) {
+    const int per_group = kGroupM * num_nb;
+    const int g = t / per_group, w = t - g * per_group;
+    const int rows = min(kGroupM, num_mb - g * kGroupM);
+    mb = g * kGroupM + w % rows;
+    nb = w / rows;
+}
 
 // Shared-memory matrix descriptor for a K-major operand tile stored with the
 // 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
@@ -104,10 +121,6 @@ __device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
     d |= static_cast<uint64_t>(128 >> 4) << 32;
     d |= static_cast<uint64_t>(1) << 46;
     return d;
-}
-
-__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
-    asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 // Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting or
@@ -136,12 +149,76 @@ __device__ bool wait_phase(uint32_t bar, uint32_t parity, uint64_t limit,
     }
 }
 
-// Address of the 32-bit scale word holding row r's scale(s) for 128-K block kb.
-__device__ __forceinline__ const uint8_t *scale_word(const uint8_t *s, int64_t ld, int gran,
-                                                     int64_t r, int kb) {
-    if (gran == GRAN_MX32) return s + r * ld + 4 * kb;
-    if (gran == GRAN_128x128) return s + (r >> 7) * ld + (kb & ~3);
-    return s + r * ld + (kb & ~3);  // 1x128
+// Loads issued where they stand in the program (asm volatile), so that the
+// next group's scale words are in flight while the current group is written.
+__device__ __forceinline__ uint32_t ld_u32_now(const uint8_t *p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_u8_now(const uint8_t *p) {
+    uint16_t v;
+    asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
+// Scale words of one row for one group of G k-blocks (G = 16, or 4 for MX32):
+// four 32-bit words at byte offsets 16*grp + 4t (t < 4) of the row's scales.
+//   1x128 / 128x128 (G = 16): word t holds the bytes of k-blocks
+//     16*grp + 4t .. +3; the MMA of k-block kb picks byte kb & 3.
+//   MX32 (G = 4): word t holds the four 32-K slots of k-block 4*grp + t.
+//   ROW: the row's single byte repeated, in every word.
+// Words whose first k-block lies past K are not read (the row's scale bytes
+// are padded to a multiple of four, not of sixteen).  Rows past the operand
+// (B tail tile) get 2^0.
+template <int G>
+__device__ __forceinline__ void load_row_scales(const uint8_t *__restrict__ s, int64_t ld, int gran,
+                                                int64_t r, int grp, int nk, bool valid,
+                                                uint32_t (&w)[4]) {
+    if (!valid) {
+        w[0] = w[1] = w[2] = w[3] = 0x7F7F7F7Fu;
+        return;
+    }
+    if (gran == GRAN_ROW) {
+        w[0] = w[1] = w[2] = w[3] = ld_u8_now(s + r * ld) * 0x01010101u;
+        return;
+    }
+    const uint8_t *row = (gran == GRAN_128x128) ? s + (r >> 7) * ld : s + r * ld;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const int first_kb = (G == 4) ? 4 * grp + t : 16 * grp + 4 * t;
+        w[t] = first_kb < nk ? ld_u32_now(row + 16 * grp + 4 * t) : 0x7F7F7F7Fu;
+    }
+}
+
+// This lane's rows of a tile: A rows 32a + lane (a < 4), B rows 32h + lane (h < 8).
+struct ScaleGroup {
+    uint32_t a[4][4];
+    uint32_t b[8][4];
+};
+
+template <int G>
+__device__ __forceinline__ void load_group(ScaleGroup &g, const KParams &p, int tile, int grp,
+                                           int lane) {
+    int mb, nb;
+    tile_coords(tile, p.num_mb, p.num_nb, mb, nb);
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        const int64_t m = static_cast<int64_t>(mb) * BM + 32 * a + lane;
+        load_row_scales<G>(p.sa, p.ld_sa, p.gran_a, m, grp, p.nk, true, g.a[a]);
+    }
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+        const int64_t n = static_cast<int64_t>(nb) * BN + 32 * h + lane;
+        load_row_scales<G>(p.sb, p.ld_sb, p.gran_b, n, grp, p.nk, n < p.N, g.b[h]);
+    }
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
 }
 
 __device__ __forceinline__ uint32_t sf_id(int gran, int kb, int j) {
@@ -152,6 +229,8 @@ __device__ __forceinline__ uint32_t sf_id(int gran, int kb, int j) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// G: k-blocks per scale group (16, or 4 when the operands are MX32).
+template <int G>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_mxf8(const __grid_constant__ CUtensorMap tmap_a,
                 const __grid_constant__ CUtensorMap tmap_b, const KParams p) {
@@ -170,7 +249,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(sBAR + 8 * s, 1 + 64);  // TMA expect_tx + 32 cp.async + 32 plain arrivals
+            ptx::mbar_init(sBAR + 8 * s, 1 + 32);  // TMA expect_tx + one arrival per scale-warp lane
             ptx::mbar_init(sBAR + 32 + 8 * s, 1);  // tcgen05.commit
         }
         ptx::mbar_init(tfull, 1);
@@ -195,7 +274,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
-            const int mb = tile / p.num_nb, nb = tile % p.num_nb;
+            int mb, nb;
+            tile_coords(tile, p.num_mb, p.num_nb, mb, nb);
             for (int kb = 0; kb < p.nk; ++kb) {
                 const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
                 ok = wait_phase(sBAR + 32 + 8 * s, ph ^ 1u, limit, abort_flag, p.err, WHO_PRODUCER);
@@ -231,7 +311,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!ok) break;
                 ptx::tc_fence_after();
                 if (lane == 0) {
-                    ptx::fence_proxy_async_smem();  // scale words written by cp.async
                     const uint32_t tsfa = tmem + SFA_COL + 4 * s;
                     const uint32_t tsfb = tmem + SFB_COL + 8 * s;
                     ptx::tc_cp_32x128b_warpx4(tsfa, desc_sf(sSFA + s * SFA_TILE));
@@ -263,24 +342,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         wait_phase(drain, 0u, drain_limit, abort_flag, p.err, WHO_MMA, false);
     } else if (warp == 2) {
         // ------------------------------------------------------ scale loader
+        // Walks the same (tile, k-block) sequence as the producer, one group
+        // of G k-blocks at a time, with the next group's loads in flight.
         uint32_t it = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
-            const int mb = tile / p.num_nb, nb = tile % p.num_nb;
-            // row-constant scales (per-token granularity): one load per tile
-            uint32_t rowA[4], rowB[8];
-#pragma unroll
-            for (int a = 0; a < 4; ++a) {
-                const int64_t m = static_cast<int64_t>(mb) * BM + 32 * a + lane;
-                rowA[a] = (p.gran_a == GRAN_ROW) ? p.sa[m * p.ld_sa] * 0x01010101u : 0u;
+        const int ngrp = (p.nk + G - 1) / G;
+        int tile = blockIdx.x, grp = 0;
+        ScaleGroup cur, nxt;
+        if (tile < p.num_tiles) load_group<G>(cur, p, tile, 0, lane);
+        while (tile < p.num_tiles && ok) {
+            int ntile = tile, ngrp_next = grp + 1;
+            if (ngrp_next == ngrp) {
+                ntile += gridDim.x;
+                ngrp_next = 0;
             }
+            if (ntile < p.num_tiles) load_group<G>(nxt, p, ntile, ngrp_next, lane);
 #pragma unroll
-            for (int h = 0; h < 8; ++h) {
-                const int64_t n = static_cast<int64_t>(nb) * BN + 32 * h + lane;
-                rowB[h] = (p.gran_b == GRAN_ROW && n < p.N) ? p.sb[n * p.ld_sb] * 0x01010101u
-                                                             : 0x7F7F7F7Fu;
-            }
-            for (int kb = 0; kb < p.nk; ++kb) {
+            for (int t = 0; t < G; ++t) {
+                if (G * grp + t >= p.nk || !ok) break;
+                constexpr int kWordStep = G / 4;  // k-blocks per scale word
+                const int wi = t / kWordStep;
                 const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
                 ok = wait_phase(sBAR + 32 + 8 * s, ph ^ 1u, limit, abort_flag, p.err, WHO_SCALES);
                 ok = __all_sync(0xFFFFFFFFu, ok);
@@ -289,45 +370,66 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // lane*16 + a*4: the 32x128-bit layout tcgen05.cp broadcasts.
                 const uint32_t dA = sSFA + s * SFA_TILE + lane * 16;
                 const uint32_t dB = sSFB + s * SFB_TILE + lane * 16;
-#pragma unroll
-                for (int a = 0; a < 4; ++a) {
-                    const int64_t m = static_cast<int64_t>(mb) * BM + 32 * a + lane;
-                    if (p.gran_a == GRAN_ROW) st_shared_u32(dA + 4 * a, rowA[a]);
-                    else ptx::cp_async_4(dA + 4 * a, scale_word(p.sa, p.ld_sa, p.gran_a, m, kb));
-                }
-#pragma unroll
-                for (int h = 0; h < 8; ++h) {
-                    const int64_t n = static_cast<int64_t>(nb) * BN + 32 * h + lane;
-                    const uint32_t dst = dB + (h >> 2) * 512 + (h & 3) * 4;
-                    if (p.gran_b == GRAN_ROW || n >= p.N) st_shared_u32(dst, rowB[h]);
-                    else ptx::cp_async_4(dst, scale_word(p.sb, p.ld_sb, p.gran_b, n, kb));
-                }
+                st_shared_v4(dA, cur.a[0][wi], cur.a[1][wi], cur.a[2][wi], cur.a[3][wi]);
+                st_shared_v4(dB, cur.b[0][wi], cur.b[1][wi], cur.b[2][wi], cur.b[3][wi]);
+                st_shared_v4(dB + 512, cur.b[4][wi], cur.b[5][wi], cur.b[6][wi], cur.b[7][wi]);
                 if (!(p.inject == 1 && it == 0)) {
-                    ptx::fence_proxy_async_smem();
+                    ptx::fence_proxy_async_smem();  // make the words visible to tcgen05.cp
                     ptx::mbar_arrive(sBAR + 8 * s);
-                    ptx::cp_async_mbar_arrive_noinc(sBAR + 8 * s);
                 }
                 ++it;
             }
+            cur = nxt;
+            tile = ntile;
+            grp = ngrp_next;
         }
-        ptx::cp_async_wait_all();
     } else if (warp >= 4) {
         // --------------------------------------------------------- epilogue
         const int q = warp & 3;  // tensor-memory lane quarter this warp may read
         uint32_t tcount = 0;
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
-            const int mb = tile / p.num_nb, nb = tile % p.num_nb;
+            int mb, nb;
+            tile_coords(tile, p.num_mb, p.num_nb, mb, nb);
             bool ok = wait_phase(tfull, tcount & 1u, limit, abort_flag, p.err, WHO_EPILOGUE);
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) break;
             ptx::tc_fence_after();
             const int64_t row = static_cast<int64_t>(mb) * BM + q * 32 + lane;
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + ACC_COL;
+            if (!p.out_fp32 && !p.accumulate) {
+                // BF16 out: pull the whole accumulator row into registers
+                // (packed BF16), release the accumulator to the next tile's
+                // MMAs, then store while they run.
+                uint32_t packed[BN / 2];
+#pragma unroll
+                for (int chunk = 0; chunk < BN / 32; ++chunk) {
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32(taddr + chunk * 32, r);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        packed[chunk * 16 + e] =
+                            ptx::cvt_bf16x2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+                }
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(tempty);
+#pragma unroll
+                for (int chunk = 0; chunk < BN / 32; ++chunk) {
+                    const int64_t n0 = static_cast<int64_t>(nb) * BN + chunk * 32;
+                    if (n0 >= p.N) continue;
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.c) + row * p.ldc + n0);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(packed[chunk * 16 + 4 * v], packed[chunk * 16 + 4 * v + 1],
+                                            packed[chunk * 16 + 4 * v + 2], packed[chunk * 16 + 4 * v + 3]);
+                }
+                ++tcount;
+                continue;
+            }
 #pragma unroll 1
             for (int chunk = 0; chunk < BN / 32; ++chunk) {
                 uint32_t r[32];
-                ptx::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + ACC_COL +
-                                            chunk * 32,
-                                        r);
+                ptx::tmem_ld_32x32b_x32(taddr + chunk * 32, r);
                 ptx::tmem_wait_ld();
                 if (chunk == BN / 32 - 1) {
                     ptx::tc_fence_before();
@@ -349,19 +451,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         dst[v] = o;
                     }
                 } else {
+                    // BF16 with accumulation: add in FP32, round once
                     uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.c) + row * p.ldc + n0);
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
                         float f[8];
 #pragma unroll
                         for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(r[8 * v + e]);
-                        if (p.accumulate) {
-                            const uint4 old = dst[v];
-                            f[0] += bf16_lo(old.x); f[1] += bf16_hi(old.x);
-                            f[2] += bf16_lo(old.y); f[3] += bf16_hi(old.y);
-                            f[4] += bf16_lo(old.z); f[5] += bf16_hi(old.z);
-                            f[6] += bf16_lo(old.w); f[7] += bf16_hi(old.w);
-                        }
+                        const uint4 old = dst[v];
+                        f[0] += bf16_lo(old.x); f[1] += bf16_hi(old.x);
+                        f[2] += bf16_lo(old.y); f[3] += bf16_hi(old.y);
+                        f[4] += bf16_lo(old.z); f[5] += bf16_hi(old.z);
+                        f[6] += bf16_lo(old.w); f[7] += bf16_hi(old.w);
                         dst[v] = make_uint4(ptx::cvt_bf16x2(f[0], f[1]), ptx::cvt_bf16x2(f[2], f[3]),
                                             ptx::cvt_bf16x2(f[4], f[5]), ptx::cvt_bf16x2(f[6], f[7]));
                     }
@@ -437,8 +538,12 @@ int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
     {
         std::lock_guard<std::mutex> lock(g_mu);
         if (!g_attr_set[dev]) {
-            cudaError_t e = cudaFuncSetAttribute(k_gemm_mxf8, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaError_t e = cudaFuncSetAttribute(k_gemm_mxf8<16>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(SMEM_BYTES));
+            if (e != cudaSuccess) return 2 + static_cast<int>(e);
+            e = cudaFuncSetAttribute(k_gemm_mxf8<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(SMEM_BYTES));
             if (e != cudaSuccess) return 2 + static_cast<int>(e);
             int n = 0;
             cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
@@ -452,7 +557,8 @@ int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
     p.N = static_cast<int>(g.N);
     p.nk = static_cast<int>(g.K / BK);
     p.num_nb = static_cast<int>((g.N + BN - 1) / BN);
-    p.num_tiles = static_cast<int>(g.M / BM) * p.num_nb;
+    p.num_mb = static_cast<int>(g.M / BM);
+    p.num_tiles = p.num_mb * p.num_nb;
     p.gran_a = g.gran_a;
     p.gran_b = g.gran_b;
     p.out_fp32 = g.out_fp32;
@@ -476,7 +582,8 @@ int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
 
     int grid = g_sms[dev];
     if (grid > p.num_tiles) grid = p.num_tiles;
-    k_gemm_mxf8<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+    if (g.gran_a == GRAN_MX32) k_gemm_mxf8<4><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+    else k_gemm_mxf8<16><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? 0 : 2 + static_cast<int>(e);
 }

@@ -1,7 +1,7 @@
 // Thin inline-PTX wrappers for the sm_103a features the kernels use:
-// mbarriers, TMA (cp.async.bulk.tensor), Ampere-style cp.async, and the
-// tcgen05 tensor-core / tensor-memory instructions.  Each wrapper is one PTX
-// instruction written from the public PTX ISA description.
+// mbarriers, TMA (cp.async.bulk.tensor) and the tcgen05 tensor-core /
+// tensor-memory instructions.  Each wrapper is one PTX instruction written
+// from the public PTX ISA description.
 #pragma once
 #include <cstdint>
 
@@ -47,19 +47,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // ---------------------------------------------------------------- proxies
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// ---------------------------------------------------------------- cp.async (4 B)
-__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-// The mbarrier receives one arrival once all earlier cp.async of this thread
-// have landed (.noinc: the arrival counts toward the expected count).
-__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- TMA
