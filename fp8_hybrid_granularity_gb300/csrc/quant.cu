@@ -8,8 +8,10 @@
 //
 //  k_quant_row       one scale per token ("A Comprehensive FP8 Training
 //                    Recipe ...", "What carries the argument": token-wise
-//                    activation scales).  One CTA per row, the row kept in
-//                    registers between the amax and the cast.
+//                    activation scales).  Persistent CTAs stage whole rows in
+//                    shared memory with bulk copies several rows ahead;
+//                    rows of up to 8 KB use k_quant_row_regs (one CTA per row,
+//                    row in registers).
 //  k_quant_groups    one scale per 1x128 group (tiled activations) or per
 //                    32-element MX block ("Characterization and Mitigation of
 //                    Training Instabilities in Microscaling Formats", "What
@@ -28,9 +30,106 @@
 namespace fp8hg {
 
 // ------------------------------------------------------------------ per row
+// Persistent, one CTA per SM.  Whole rows are staged in shared memory by 1-D
+// bulk copies issued by one thread, up to nslots rows ahead (each slot's
+// completion on its own mbarrier), so the bytes in flight do not depend on
+// registers.  For each row the CTA reduces the amax from shared memory, then
+// casts from shared memory and stores the codes.
+constexpr int kRowThreads = 512;
+constexpr int kMaxRowSlots = 8;
+constexpr int kRowSmemBudget = 200 * 1024;
+
+constexpr uint64_t kRowWaitNs = 2000000000ull;  // bound on one row's copy (2 s)
+
+// Thread 0 waits (bounded) for a slot's copy; false when the bound ran out.
+__device__ __forceinline__ bool row_wait(uint32_t bar, uint32_t parity, uint64_t limit) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    while (!ptx::mbar_try_wait(bar, parity))
+        if (ptx::globaltimer() - t0 > limit) return false;
+    return true;
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kRowThreads) k_quant_row(const uint16_t *__restrict__ x,
+                                                              int64_t rows, int nvec, int64_t ld_x,
+                                                              uint8_t *__restrict__ q, int64_t ld_q,
+                                                              uint8_t *__restrict__ s, int64_t ld_s,
+                                                              int nslots, unsigned int *err) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t full[kMaxRowSlots];
+    __shared__ uint32_t red[kRowThreads / 32];
+    __shared__ int row_ok;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const uint32_t row_bytes = static_cast<uint32_t>(nvec) * 16u;
+    const uint32_t sbase = ptx::smem_u32(smem);
+    const uint32_t fbase = ptx::smem_u32(full);
+    const int64_t step = gridDim.x;
+    if (tid == 0) {
+        for (int i = 0; i < nslots; ++i) ptx::mbar_init(fbase + 8 * i, 1);
+        ptx::fence_mbar_init();
+        // prologue: the first nslots - 1 rows of this CTA
+        for (int i = 0; i < nslots - 1; ++i) {
+            const int64_t r = blockIdx.x + i * step;
+            if (r >= rows) break;
+            ptx::mbar_arrive_expect_tx(fbase + 8 * i, row_bytes);
+            ptx::bulk_load(sbase + i * row_bytes, x + r * ld_x, row_bytes, fbase + 8 * i);
+        }
+    }
+    __syncthreads();
+    int k = 0;  // rows done by this CTA
+    for (int64_t row = blockIdx.x; row < rows; row += step, ++k) {
+        const int slot = k % nslots;
+        // issue the row nslots - 1 ahead into the slot the previous row freed
+        if (tid == 0) {
+            const int64_t r = row + static_cast<int64_t>(nslots - 1) * step;
+            if (r < rows) {
+                const int sl = (k + nslots - 1) % nslots;
+                ptx::mbar_arrive_expect_tx(fbase + 8 * sl, row_bytes);
+                ptx::bulk_load(sbase + sl * row_bytes, x + r * ld_x, row_bytes, fbase + 8 * sl);
+            }
+        }
+        if (tid == 0) {
+            row_ok = row_wait(fbase + 8 * slot, static_cast<uint32_t>(k / nslots) & 1u, kRowWaitNs);
+            if (!row_ok) {
+                atomicOr(err, 2u);
+                // let this CTA's other copies in flight land before it exits
+                for (int j = 1; j < nslots; ++j) {
+                    const int64_t r = row + static_cast<int64_t>(j) * step;
+                    if (r >= rows) break;
+                    const int sl = (k + j) % nslots;
+                    row_wait(fbase + 8 * sl, static_cast<uint32_t>((k + j) / nslots) & 1u, 2000000ull);
+                }
+            }
+        }
+        __syncthreads();  // also makes the copied row visible to every thread
+        if (!row_ok) return;
+        const uint4 *xs = reinterpret_cast<const uint4 *>(smem + static_cast<size_t>(slot) * row_bytes);
+        uint32_t m = 0;
+        for (int c = tid; c < nvec; c += blockDim.x) m = max(m, bf16_abs_max8(xs[c]));
+        m = __reduce_max_sync(0xFFFFFFFFu, m);
+        if (lane == 0) red[warp] = m;
+        __syncthreads();
+        m = 0;
+        for (int w = 0; w < nwarps; ++w) m = max(m, red[w]);
+        float mul;
+        const uint32_t sbyte = group_scale<FMT, false>(m, mul);
+        uint2 *qr = reinterpret_cast<uint2 *>(q + row * ld_q);
+        uint32_t unused = 0;
+        for (int c = tid; c < nvec; c += blockDim.x)
+            qr[c] = (sbyte == 0xFFu) ? make_uint2(kNanCodes, kNanCodes)
+                                     : quant8<FMT, false>(xs[c], mul, unused);
+        if (tid == 0) s[row * ld_s] = static_cast<uint8_t>(sbyte);
+        __syncthreads();  // the slot and red[] are free for the next row
+    }
+}
+
+// Short rows (up to 8 KB): one CTA per row, the row kept in registers between
+// the amax and the cast; many small CTAs keep the memory system busy.
 template <int FMT, int NV>
-__global__ void __launch_bounds__(512) k_quant_row(const uint16_t *__restrict__ x, int nvec,
-                                                   int64_t ld_x, uint8_t *__restrict__ q,
+__global__ void __launch_bounds__(512) k_quant_row_regs(const uint16_t *__restrict__ x, int nvec,
+                                                        int64_t ld_x, uint8_t *__restrict__ q,
                                                    int64_t ld_q, uint8_t *__restrict__ s,
                                                    int64_t ld_s) {
     __shared__ uint32_t red[16];
@@ -109,45 +208,47 @@ __global__ void __launch_bounds__(512) k_quant_row_2pass(const uint16_t *__restr
 }
 
 // ------------------------------------------------------ groups along a row
-// GV = 16-byte vectors per group: 16 (1x128) or 4 (MX 32).  Lanes
-// [g*GV, g*GV + GV) of a warp hold one group; the loop is warp-uniform so
-// every lane reaches the shuffles.
-template <int FMT, int GV, bool MX, bool COUNT>
+// GV = 16-byte vectors per group: 16 (1x128) or 4 (MX 32).  A CTA covers
+// 256*U consecutive vectors of a row (blockIdx.x) for the rows blockIdx.y,
+// blockIdx.y + gridDim.y, ...; lanes [g*GV, g*GV + GV) of a warp hold one
+// group, and every lane reaches the shuffles.
+template <int FMT, int GV, bool MX, bool COUNT, int U>
 __global__ void __launch_bounds__(256) k_quant_groups(const uint16_t *__restrict__ x, int64_t rows,
-                                                      int64_t vpr, int64_t ld_x,
+                                                      int vpr, int64_t ld_x,
                                                       uint8_t *__restrict__ q, int64_t ld_q,
                                                       uint8_t *__restrict__ s, int64_t ld_s,
                                                       unsigned long long *__restrict__ cnt) {
-    constexpr int U = 4;
     const int lane = threadIdx.x & 31;
-    const int64_t total = rows * vpr;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    const int64_t wbase0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
+    const int cv0 = blockIdx.x * (256 * U) + threadIdx.x;
     uint32_t nsat = 0;
-    for (int64_t wbase = wbase0; wbase < total; wbase += stride * U) {
-        uint4 v[U];
-        int64_t row[U], cv[U];
-        bool ok[U];
+    uint4 v[U], nxt[U];
+    auto load = [&](int64_t r, uint4 (&dst)[U]) {
+        const uint16_t *xr = x + r * ld_x;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int64_t idx = wbase + lane + u * stride;
-            ok[u] = idx < total;
-            row[u] = ok[u] ? idx / vpr : 0;
-            cv[u] = idx - row[u] * vpr;
-            if (ok[u]) v[u] = ptx::ld_stream_v4(x + row[u] * ld_x + cv[u] * 8);
+            const int cv = cv0 + u * 256;
+            if (cv < vpr) dst[u] = ptx::ld_stream_v4(xr + static_cast<int64_t>(cv) * 8);
         }
+    };
+    if (static_cast<int64_t>(blockIdx.y) < rows) load(blockIdx.y, nxt);
+    for (int64_t row = blockIdx.y; row < rows; row += gridDim.y) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) v[u] = nxt[u];
+        if (row + gridDim.y < rows) load(row + gridDim.y, nxt);  // next row in flight
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            uint32_t m = ok[u] ? bf16_abs_max8(v[u]) : 0u;
+            const int cv = cv0 + u * 256;
+            const bool ok = cv < vpr;
+            uint32_t m = ok ? bf16_abs_max8(v[u]) : 0u;
 #pragma unroll
             for (int o = GV / 2; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-            if (ok[u]) {
+            if (ok) {
                 float mul;
                 const uint32_t sbyte = group_scale<FMT, MX>(m, mul);
-                uint2 out = (sbyte == 0xFFu) ? make_uint2(kNanCodes, kNanCodes)
-                                             : quant8<FMT, COUNT>(v[u], mul, nsat);
-                *reinterpret_cast<uint2 *>(q + row[u] * ld_q + cv[u] * 8) = out;
-                if ((lane % GV) == 0) s[row[u] * ld_s + cv[u] / GV] = static_cast<uint8_t>(sbyte);
+                const uint2 out = (sbyte == 0xFFu) ? make_uint2(kNanCodes, kNanCodes)
+                                                   : quant8<FMT, COUNT>(v[u], mul, nsat);
+                *reinterpret_cast<uint2 *>(q + row * ld_q + static_cast<int64_t>(cv) * 8) = out;
+                if ((lane % GV) == 0) s[row * ld_s + cv / GV] = static_cast<uint8_t>(sbyte);
             }
         }
     }
@@ -307,8 +408,16 @@ int num_sms() {
     return g_num_sms[dev];
 }
 
+template <typename K>
+int resident_blocks(K kernel, int threads) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1)
+        n = 1;
+    return n;
+}
+
 template <int FMT>
-cudaError_t launch_row(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, uint8_t *q,
+cudaError_t launch_row_regs(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, uint8_t *q,
                        int64_t ld_q, uint8_t *s, int64_t ld_s, cudaStream_t stream) {
     const int nvec = static_cast<int>(cols / 8);
     // choose NV (vectors per thread) and T (threads) so that T*NV covers the
@@ -335,12 +444,70 @@ cudaError_t launch_row(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld
         return cudaGetLastError();
     }
     switch (best_nv) {
-    case 1: k_quant_row<FMT, 1><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
-    case 2: k_quant_row<FMT, 2><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
-    case 4: k_quant_row<FMT, 4><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
-    case 8: k_quant_row<FMT, 8><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
-    default: k_quant_row<FMT, 16><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
+    case 1: k_quant_row_regs<FMT, 1><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
+    case 2: k_quant_row_regs<FMT, 2><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
+    case 4: k_quant_row_regs<FMT, 4><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
+    case 8: k_quant_row_regs<FMT, 8><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
+    default: k_quant_row_regs<FMT, 16><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
     }
+    return cudaGetLastError();
+}
+
+bool g_row_attr[64][2] = {{false}};
+
+template <int FMT>
+cudaError_t launch_row(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, uint8_t *q,
+                       int64_t ld_q, uint8_t *s, int64_t ld_s, cudaStream_t stream) {
+    const int nvec = static_cast<int>(cols / 8);
+    const int64_t row_bytes = cols * 2;
+    if (row_bytes <= 8192) return launch_row_regs<FMT>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream);
+    // Rows up to ~50 KB: up to 4 CTAs per SM, so that one CTA's per-row
+    // synchronisation overlaps the others' work; each CTA keeps at least 4
+    // (and at most 8) rows in flight, ~200 KB per SM in total.
+    int64_t per_sm = kRowSmemBudget / (4 * row_bytes);
+    const int ctas_per_sm = static_cast<int>(per_sm < 1 ? 1 : (per_sm > 4 ? 4 : per_sm));
+    int nslots = static_cast<int>(kRowSmemBudget / ctas_per_sm / row_bytes);
+    if (nslots > kMaxRowSlots) nslots = kMaxRowSlots;
+    if (nslots < 2) {
+        // rows too long to stage two at a time: amax pass + cast pass
+        k_quant_row_2pass<FMT><<<static_cast<unsigned>(rows), 512, 0, stream>>>(x, nvec, ld_x, q,
+                                                                                ld_q, s, ld_s);
+        return cudaGetLastError();
+    }
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (!g_row_attr[dev][FMT]) {
+        const cudaError_t e = cudaFuncSetAttribute(k_quant_row<FMT>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   kRowSmemBudget);
+        if (e != cudaSuccess) return e;
+        g_row_attr[dev][FMT] = true;
+    }
+    int64_t grid = static_cast<int64_t>(num_sms()) * ctas_per_sm;
+    if (grid > rows) grid = rows;
+    int threads = kRowThreads;
+    if (nvec < threads) threads = ((nvec + 31) / 32) * 32;
+    unsigned int *err = device_error_word();
+    if (!err) return cudaErrorInvalidValue;
+    k_quant_row<FMT><<<static_cast<unsigned>(grid), threads, static_cast<size_t>(nslots) * row_bytes,
+                       stream>>>(x, rows, nvec, ld_x, q, ld_q, s, ld_s, nslots, err);
+    return cudaGetLastError();
+}
+
+template <int FMT, int GV, bool MX, bool COUNT, int U>
+cudaError_t launch_groups_u(const uint16_t *x, int64_t rows, int vpr, int64_t ld_x, uint8_t *q,
+                            int64_t ld_q, uint8_t *s, int64_t ld_s, unsigned long long *cnt,
+                            cudaStream_t stream) {
+    const int gx = (vpr + 256 * U - 1) / (256 * U);
+    const int64_t target = static_cast<int64_t>(num_sms()) *
+                           resident_blocks(k_quant_groups<FMT, GV, MX, COUNT, U>, 256);
+    int64_t gy = (target + gx - 1) / gx;
+    if (gy > rows) gy = rows;
+    if (gy > 65535) gy = 65535;
+    if (gy < 1) gy = 1;
+    k_quant_groups<FMT, GV, MX, COUNT, U><<<dim3(gx, static_cast<unsigned>(gy)), 256, 0, stream>>>(
+        x, rows, vpr, ld_x, q, ld_q, s, ld_s, cnt);
     return cudaGetLastError();
 }
 
@@ -348,16 +515,20 @@ template <int FMT, int GV, bool MX, bool COUNT>
 cudaError_t launch_groups(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, uint8_t *q,
                           int64_t ld_q, uint8_t *s, int64_t ld_s, unsigned long long *cnt,
                           cudaStream_t stream) {
-    const int64_t vpr = cols / 8;
-    const int64_t total = rows * vpr;
-    const int threads = 256;
-    int64_t blocks = (total + threads * 4 - 1) / (threads * 4);
-    const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
-    k_quant_groups<FMT, GV, MX, COUNT><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        x, rows, vpr, ld_x, q, ld_q, s, ld_s, cnt);
-    return cudaGetLastError();
+    const int vpr = static_cast<int>(cols / 8);
+    // vectors per thread: the largest U (up to 4) that leaves no more than
+    // an eighth of the CTA's slots in a row idle
+    int u = 1;
+    for (int cand : {4, 2}) {
+        const int span = 256 * cand, gx = (vpr + span - 1) / span;
+        if (static_cast<int64_t>(gx) * span - vpr <= vpr / 8) {
+            u = cand;
+            break;
+        }
+    }
+    if (u == 4) return launch_groups_u<FMT, GV, MX, COUNT, 4>(x, rows, vpr, ld_x, q, ld_q, s, ld_s, cnt, stream);
+    if (u == 2) return launch_groups_u<FMT, GV, MX, COUNT, 2>(x, rows, vpr, ld_x, q, ld_q, s, ld_s, cnt, stream);
+    return launch_groups_u<FMT, GV, MX, COUNT, 1>(x, rows, vpr, ld_x, q, ld_q, s, ld_s, cnt, stream);
 }
 }  // namespace
 

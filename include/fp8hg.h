@@ -235,8 +235,9 @@ int fp8_gemm_scaled_ex(int op, const fp8hg_operand *a, const fp8hg_operand *b, v
 /*
  * fp8hg_get_device_error — synchronizes `stream`, then reads and clears the
  * device error word of the current device.  Returns FP8HG_OK,
- * FP8HG_ERR_TIMEOUT (a kernel's bounded wait expired since the last call) or
- * FP8HG_ERR_CUDA (the synchronization itself failed).
+ * FP8HG_ERR_TIMEOUT (a bounded wait in a GEMM or per-token quantizer kernel
+ * expired since the last call) or FP8HG_ERR_CUDA (the synchronization itself
+ * failed).
  */
 int fp8hg_get_device_error(void *stream);
 
