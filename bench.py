@@ -40,6 +40,8 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+from fp8_hybrid_granularity_gb300 import replicas  # noqa: E402
+
 METRIC = "scaled-FP8 GEMM TFLOP/s incl. quant (% FP8 peak); quantizer GB/s (% HBM) at 7B shapes"
 M_TOK, HID, MLP = 16384, 3584, 18944
 WORKLOAD = (f"linear_step_7b: Qwen2.5-7B MLP block (gate/up/down) fprop+dgrad+wgrad, "
@@ -149,7 +151,8 @@ class Step:
 
     def __init__(self, torch, fp8hg, workloads, device, seed_offset=0):
         self.torch, self.f = torch, fp8hg
-        T = lambda kind, r, c, name: workloads.make_tensor(kind, r, c, 2 + seed_offset, name,
+        seed = replicas.replica_seed(2, seed_offset)
+        T = lambda kind, r, c, name: workloads.make_tensor(kind, r, c, seed, name,
                                                            device=device)
         self.inp = {
             "X": T("act", M_TOK, HID, "X"), "H": T("act", M_TOK, MLP, "H"),
@@ -288,8 +291,7 @@ SAMPLE_DESC = ("oracle (plain C, fp64, 1 thread) on a 32x32 block of outputs of 
 
 
 def run_reference(args):
-    rank = int(os.environ.get("RANK", "0"))
-    if rank != 0:
+    if not replicas.rank_info().is_root:
         return
     for _ in range(args.warmup):
         oracle_sample_step()
@@ -322,9 +324,8 @@ def main():
     import fp8_hybrid_granularity_gb300 as fp8hg
     from fp8_hybrid_granularity_gb300 import workloads
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    ri = replicas.rank_info()
+    world, rank, local = ri.world, ri.rank, ri.local
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl")
@@ -362,10 +363,7 @@ def main():
     status = fp8hg.fp8hg_get_device_error()
     if status != 0:
         raise RuntimeError(f"device error: {fp8hg.fp8hg_status_str(status)}")
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = replicas.max_over_ranks(ms, dist, dev)
 
     gemm_ms = [a.elapsed_time(b) for k, a, b in events if k == "gemm"]
     per_gemm = [sum(gemm_ms[j::N_GEMM]) / args.steps for j in range(N_GEMM)]
@@ -375,7 +373,7 @@ def main():
     quant_ms = [a.elapsed_time(b) for k, a, b in events if k == "quant"]
     gemm_avg = sum(gemm_ms) / len(gemm_ms)
     quant_step_ms = sum(quant_ms) / args.steps
-    value = world * N_GEMM * GEMM_FLOP / (ms * 1e-3) / 1e12
+    value = replicas.job_throughput(world, N_GEMM * GEMM_FLOP, ms)
     gemm_tf = GEMM_FLOP / (gemm_avg * 1e-3) / 1e12
     quant_gbs = step.quant_bytes / (quant_step_ms * 1e-3) / 1e9
     fp8_peak = 2.0 * peaks["bf16_sus"]   # fp8 dense = 2x bf16 dense (nominal ratio)
@@ -432,11 +430,8 @@ def main():
         b.record()
         barrier()
         e_ms = a.elapsed_time(b) / ke
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * N_GEMM * GEMM_FLOP / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e_ms = replicas.max_over_ranks(e_ms, dist, dev)
+        e2e = {"value": replicas.job_throughput(world, N_GEMM * GEMM_FLOP, e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": step.in_bytes, "d2h_bytes_per_step": step.out_bytes,
                "ms_per_step": e_ms, "steps": ke,
                "note": "pinned host buffers; two device buffer sets, copies overlapped with compute"}
