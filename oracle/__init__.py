@@ -70,6 +70,8 @@ def _load():
         lib.orc_quant_block128.argtypes = [P, I64, I64, I64, I, P, I64, P, I64, P, I64, P, I64]
         lib.orc_quant_mx32.restype = I
         lib.orc_quant_mx32.argtypes = [P, I64, I64, I64, I, P, I64, P, I64, P]
+        lib.orc_mx32_monitor.restype = I
+        lib.orc_mx32_monitor.argtypes = [P, I64, I64, I64, I, P, I64, P, I64, P, P]
         lib.orc_dequant.restype = I
         lib.orc_dequant.argtypes = [P, I64, P, I64, I, I, I64, I64, P]
         lib.orc_gemm_ref_pairs.restype = I
@@ -178,6 +180,24 @@ def quant_mx32(x, fmt: int):
                                 _ptr(s), s.shape[1], _ptr(cnt))
     _check(rc, "quant_mx32")
     return q, s, int(cnt[0])
+
+
+MX_STAT_NAMES = ("saturated", "top_code", "blocks_saturated", "blocks_collapsed")
+
+
+def mx32_monitor(x, fmt: int):
+    """MX quantization with the clamp monitor's counts.  Returns
+    (q, scale, stats dict, per-row saturated counts)."""
+    x = _u16(x)
+    rows, cols = x.shape
+    q = np.empty((rows, cols), np.uint8)
+    s = np.empty((rows, cols // 32), np.uint8)
+    st = np.zeros(4, np.uint64)
+    rs = np.zeros(rows, np.uint64)
+    rc = _load().orc_mx32_monitor(_ptr(x), rows, cols, cols, int(fmt), _ptr(q), cols,
+                                  _ptr(s), s.shape[1], _ptr(st), _ptr(rs))
+    _check(rc, "mx32_monitor")
+    return q, s, dict(zip(MX_STAT_NAMES, (int(v) for v in st))), rs
 
 
 # --- dequantization and GEMM ------------------------------------------------

@@ -23,7 +23,7 @@
  *    power-of-two scale; a scaled magnitude beyond the element format's
  *    largest value is clamped to the largest code.
  *
- * Readings taken where the pages are silent (each is listed in the design doc):
+ * Readings taken where the pages are silent:
  *  - block sizes: 128x128 weight blocks, 1x128 activation groups in the tiled
  *    variant, 32-element MX blocks (the recipe page says the block size is not
  *    reported);
@@ -303,6 +303,52 @@ int orc_quant_mx32(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, 
             scale[r * ld_s + c0 / 32] = orc_quant_group(x + r * ld_x + c0, 1, 32, fmt, 1,
                                                         q + r * ld_q + c0, 1, &nsat);
     if (clamp_count) *clamp_count = nsat;
+    return 0;
+}
+
+/* MX clamp monitor.  "Characterization and Mitigation of Training
+ * Instabilities in Microscaling Formats" proposes watching how many values
+ * are clamped into the last quantization bin, and how many blocks are, as an
+ * early warning of divergence ("What would settle it", "If this is right"),
+ * and names the collapse of a tightly clustered block onto one bin as the
+ * mechanism ("What carries the argument").  This quantizes exactly as
+ * orc_quant_mx32 (same q and scale) and counts, over the whole tensor:
+ *   stats[0]  elements whose scaled magnitude exceeded the format's largest
+ *             value (saturated: written as the largest code)
+ *   stats[1]  elements whose code has the largest finite magnitude (the last
+ *             bin), saturated or rounded there
+ *   stats[2]  blocks holding at least one saturated element
+ *   stats[3]  blocks whose 32 codes are all the same byte (same-bin collapse);
+ *             blocks of zeros and blocks holding a non-finite value excluded
+ * row_sat[r] (if non-null) = saturated elements in row r. */
+int orc_mx32_monitor(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
+                     uint8_t *q, int64_t ld_q, uint8_t *scale, int64_t ld_s, uint64_t *stats,
+                     uint64_t *row_sat)
+{
+    if (cols % 32 || !stats) return -1;
+    const uint8_t top = orc_fp8_encode(orc_fp8_max(fmt), fmt, 1);
+    for (int i = 0; i < 4; i++) stats[i] = 0;
+    for (int64_t r = 0; r < rows; r++) {
+        uint64_t rs = 0;
+        for (int64_t c0 = 0; c0 < cols; c0 += 32) {
+            const uint16_t *xb = x + r * ld_x + c0;
+            uint8_t *qb = q + r * ld_q + c0;
+            uint64_t nsat = 0;
+            uint8_t sb = orc_quant_group(xb, 1, 32, fmt, 1, qb, 1, &nsat);
+            scale[r * ld_s + c0 / 32] = sb;
+            int allzero = 1, same = 1;
+            for (int i = 0; i < 32; i++) {
+                if (orc_bf16_to_double(xb[i]) != 0.0) allzero = 0;
+                if (qb[i] != qb[0]) same = 0;
+                if ((qb[i] & 0x7F) == top) stats[1]++;
+            }
+            stats[0] += nsat;
+            rs += nsat;
+            if (nsat) stats[2]++;
+            if (same && !allzero && sb != 0xFF) stats[3]++;
+        }
+        if (row_sat) row_sat[r] = rs;
+    }
     return 0;
 }
 

@@ -36,8 +36,11 @@ def load_quant_examples(name: str = "quant_examples.txt"):
                 cur[key] = np.array(_hex_list(val), np.uint8)
             elif key == "scale":
                 cur[key] = int(val, 16)
-            elif key == "clamped":
+            elif key in ("clamped", "rows", "saturated", "top_code", "blocks_saturated",
+                         "blocks_collapsed"):
                 cur[key] = int(val)
+            elif key == "row_sat":
+                cur[key] = [int(t) for t in val.split()]
             else:
                 cur[key] = val
     return cases
