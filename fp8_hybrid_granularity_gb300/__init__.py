@@ -11,6 +11,7 @@ Tensor-level API (same names as the C entry points):
   fp8_quant_token(x, group=0|128, fmt, transpose=False) -> QTensor
   fp8_quant_block128(x, fmt, transposed_copy=False)     -> QTensor[, QTensor]
   fp8_quant_mx32(x, fmt, clamp_count=None)              -> QTensor
+  fp8_quant_mx32_monitor(x, fmt, stats=None, row_saturated=None) -> QTensor, stats
   fp8_gemm_scaled(op, a, b, out=None, out_dtype=bf16, accumulate=False)
   fp8hg_get_device_error(stream=None)
 
@@ -84,6 +85,7 @@ def load_library(build_if_stale: bool = True):
         lib.fp8_quant_token.argtypes = [P, I64, I64, I64, I, I, I, P, I64, P, I64, P]
         lib.fp8_quant_block128.argtypes = [P, I64, I64, I64, I, P, I64, P, I64, P, I64, P, I64, P]
         lib.fp8_quant_mx32.argtypes = [P, I64, I64, I64, I, P, I64, P, I64, P, P]
+        lib.fp8_quant_mx32_monitor.argtypes = [P, I64, I64, I64, I, P, I64, P, I64, P, P, P]
         lib.fp8_gemm_scaled.argtypes = [I, ctypes.POINTER(Operand), ctypes.POINTER(Operand), P,
                                         I64, I, I, P]
         lib.fp8_gemm_scaled_ex.argtypes = [I, ctypes.POINTER(Operand), ctypes.POINTER(Operand), P,
@@ -239,6 +241,36 @@ def fp8_quant_mx32(x, fmt: int = E4M3, clamp_count=None, out=None, stream=None) 
                               _ptr(clamp_count), _stream(stream))
     _check(rc, "fp8_quant_mx32")
     return out
+
+
+MX_STAT_NAMES = ("saturated", "top_code", "blocks_saturated", "blocks_collapsed")
+
+
+def fp8_quant_mx32_monitor(x, fmt: int = E4M3, stats=None, row_saturated=None, out=None,
+                           stream=None):
+    """MXFP8 quantization that also counts the last-bin population.
+
+    stats: int64 CUDA tensor of 4 (saturated, top_code, blocks_saturated,
+    blocks_collapsed); allocated zeroed if None.  row_saturated: optional
+    int32 CUDA tensor [rows] of per-row saturated counts.  Both receive +=.
+    Returns (QTensor, stats)."""
+    import torch
+    _check_bf16(x)
+    rows, cols = x.shape
+    if stats is None:
+        stats = torch.zeros(4, dtype=torch.int64, device=x.device)
+    if stats.dtype != torch.int64 or stats.numel() != 4 or not stats.is_contiguous():
+        raise ValueError("stats must be a contiguous int64 tensor of 4 elements")
+    if row_saturated is not None and (row_saturated.dtype != torch.int32 or
+                                      row_saturated.numel() != rows or
+                                      not row_saturated.is_contiguous()):
+        raise ValueError("row_saturated must be a contiguous int32 tensor of `rows` elements")
+    out = out if out is not None else alloc_mx32(rows, cols, fmt, x.device)
+    rc = lib().fp8_quant_mx32_monitor(_ptr(x), rows, cols, x.stride(0), fmt, _ptr(out.codes),
+                                      out.codes.stride(0), _ptr(out.scale), out.scale.stride(0),
+                                      _ptr(stats), _ptr(row_saturated), _stream(stream))
+    _check(rc, "fp8_quant_mx32_monitor")
+    return out, stats
 
 
 def fp8_gemm_scaled(op: int, a: QTensor, b: QTensor, out=None, out_dtype=None,

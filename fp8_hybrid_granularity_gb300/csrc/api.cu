@@ -130,6 +130,23 @@ int fp8_quant_mx32(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, 
                                                      static_cast<cudaStream_t>(stream)));
 }
 
+int fp8_quant_mx32_monitor(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
+                           uint8_t *q, int64_t ld_q, uint8_t *scale, int64_t ld_s,
+                           fp8hg_mx_stats *stats, unsigned int *row_saturated, void *stream) {
+    int st = check_quant_common(x, rows, cols, ld_x, fmt, q, ld_q, scale);
+    if (st != FP8HG_OK) return st;
+    if (stats == nullptr) return FP8HG_ERR_INVALID_ARG;
+    if (!aligned(stats, 8) || (row_saturated && !aligned(row_saturated, 4)))
+        return FP8HG_ERR_ALIGNMENT;
+    if (rows == 0 || cols == 0) return FP8HG_OK;
+    if (cols % 32) return FP8HG_ERR_SHAPE;
+    if (ld_x < cols || ld_q < cols || ld_s < cols / 32) return FP8HG_ERR_INVALID_ARG;
+    return status_from_cuda(fp8hg::launch_quant_mx32_monitor(
+        x, rows, cols, ld_x, fmt, q, ld_q, scale, ld_s,
+        reinterpret_cast<unsigned long long *>(stats), row_saturated,
+        static_cast<cudaStream_t>(stream)));
+}
+
 int fp8_gemm_scaled_ex(int op, const fp8hg_operand *a, const fp8hg_operand *b, void *c, int64_t ldc,
                        int out, int accumulate, const fp8hg_gemm_opts *opts, void *stream) {
     if (op < FP8HG_FPROP || op > FP8HG_WGRAD) return FP8HG_ERR_INVALID_ARG;

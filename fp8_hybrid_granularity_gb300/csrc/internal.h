@@ -15,6 +15,11 @@ cudaError_t launch_quant_mx32(const uint16_t *x, int64_t rows, int64_t cols, int
                               uint8_t *q, int64_t ld_q, uint8_t *s, int64_t ld_s,
                               unsigned long long *cnt, cudaStream_t stream);
 
+cudaError_t launch_quant_mx32_monitor(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
+                                      int fmt, uint8_t *q, int64_t ld_q, uint8_t *s, int64_t ld_s,
+                                      unsigned long long *stats, unsigned int *row_sat,
+                                      cudaStream_t stream);
+
 cudaError_t launch_quant_block128(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
                                   int fmt, uint8_t *q, int64_t ld_q, uint8_t *s, int64_t ld_s,
                                   uint8_t *qt, int64_t ld_qt, uint8_t *st, int64_t ld_st,

@@ -208,19 +208,37 @@ __global__ void __launch_bounds__(512) k_quant_row_2pass(const uint16_t *__restr
 }
 
 // ------------------------------------------------------ groups along a row
+// Optional counters of the MX quantizer.  clamp: elements whose scaled
+// magnitude exceeded the format's maximum.  Monitor (stats non-null): the
+// four counts of fp8hg_mx_stats, and per-row saturated counts.
+struct MxCounters {
+    unsigned long long *clamp;     // COUNT: saturated elements
+    unsigned long long *stats;     // MON: saturated, top code, saturated blocks, collapsed blocks
+    unsigned int *row_sat;         // MON, optional: saturated elements per row
+};
+
+// Number of the eight codes whose magnitude is the format's largest code.
+template <int FMT>
+__device__ __forceinline__ uint32_t top_codes(const uint2 &c) {
+    constexpr uint32_t T = (FMT == FMT_E4M3 ? 0x7Eu : 0x7Bu) * 0x01010101u;
+    const uint32_t a = __vcmpeq4(c.x & 0x7F7F7F7Fu, T), b = __vcmpeq4(c.y & 0x7F7F7F7Fu, T);
+    return (__popc(a) + __popc(b)) >> 3;
+}
+
 // GV = 16-byte vectors per group: 16 (1x128) or 4 (MX 32).  A CTA covers
 // 256*U consecutive vectors of a row (blockIdx.x) for the rows blockIdx.y,
 // blockIdx.y + gridDim.y, ...; lanes [g*GV, g*GV + GV) of a warp hold one
 // group, and every lane reaches the shuffles.
-template <int FMT, int GV, bool MX, bool COUNT, int U>
+template <int FMT, int GV, bool MX, bool COUNT, bool MON, int U>
 __global__ void __launch_bounds__(256) k_quant_groups(const uint16_t *__restrict__ x, int64_t rows,
                                                       int vpr, int64_t ld_x,
                                                       uint8_t *__restrict__ q, int64_t ld_q,
                                                       uint8_t *__restrict__ s, int64_t ld_s,
-                                                      unsigned long long *__restrict__ cnt) {
+                                                      MxCounters cnt) {
+    constexpr bool SAT = COUNT || MON;
     const int lane = threadIdx.x & 31;
     const int cv0 = blockIdx.x * (256 * U) + threadIdx.x;
-    uint32_t nsat = 0;
+    uint32_t nsat = 0, ntop = 0, nbsat = 0, ncoll = 0;
     uint4 v[U], nxt[U];
     auto load = [&](int64_t r, uint4 (&dst)[U]) {
         const uint16_t *xr = x + r * ld_x;
@@ -235,6 +253,7 @@ __global__ void __launch_bounds__(256) k_quant_groups(const uint16_t *__restrict
 #pragma unroll
         for (int u = 0; u < U; ++u) v[u] = nxt[u];
         if (row + gridDim.y < rows) load(row + gridDim.y, nxt);  // next row in flight
+        uint32_t row_nsat = 0;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int cv = cv0 + u * 256;
@@ -242,19 +261,57 @@ __global__ void __launch_bounds__(256) k_quant_groups(const uint16_t *__restrict
             uint32_t m = ok ? bf16_abs_max8(v[u]) : 0u;
 #pragma unroll
             for (int o = GV / 2; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+            uint2 out = make_uint2(0u, 0u);
+            uint32_t sbyte = 0;
+            const uint32_t before = nsat;
             if (ok) {
                 float mul;
-                const uint32_t sbyte = group_scale<FMT, MX>(m, mul);
-                const uint2 out = (sbyte == 0xFFu) ? make_uint2(kNanCodes, kNanCodes)
-                                                   : quant8<FMT, COUNT>(v[u], mul, nsat);
+                sbyte = group_scale<FMT, MX>(m, mul);
+                out = (sbyte == 0xFFu) ? make_uint2(kNanCodes, kNanCodes)
+                                       : quant8<FMT, SAT>(v[u], mul, nsat);
                 *reinterpret_cast<uint2 *>(q + row * ld_q + static_cast<int64_t>(cv) * 8) = out;
                 if ((lane % GV) == 0) s[row * ld_s + cv / GV] = static_cast<uint8_t>(sbyte);
             }
+            if constexpr (MON) {
+                // lanes past the row's end hold out = 0: no top codes, no saturation
+                const uint32_t dsat = nsat - before;
+                ntop += top_codes<FMT>(out);
+                const uint32_t first = __shfl_sync(0xFFFFFFFFu, out.x, lane & ~(GV - 1)) & 0xFFu;
+                const uint32_t rep = first * 0x01010101u;
+                uint32_t same = (out.x == rep && out.y == rep) ? 1u : 0u, gsat = dsat;
+#pragma unroll
+                for (int o = GV / 2; o > 0; o >>= 1) {
+                    same &= __shfl_xor_sync(0xFFFFFFFFu, same, o);
+                    gsat += __shfl_xor_sync(0xFFFFFFFFu, gsat, o);
+                }
+                if (ok && (lane % GV) == 0) {
+                    nbsat += gsat != 0u;
+                    ncoll += (same && m != 0u && sbyte != 0xFFu) ? 1u : 0u;
+                }
+                row_nsat += dsat;
+            }
+        }
+        if constexpr (MON) {
+            if (cnt.row_sat != nullptr) {
+                row_nsat = __reduce_add_sync(0xFFFFFFFFu, row_nsat);
+                if (lane == 0 && row_nsat) atomicAdd(cnt.row_sat + row, row_nsat);
+            }
         }
     }
-    if constexpr (COUNT) {
+    if constexpr (SAT) {
         nsat = __reduce_add_sync(0xFFFFFFFFu, nsat);
-        if (lane == 0 && nsat) atomicAdd(cnt, static_cast<unsigned long long>(nsat));
+        unsigned long long *dst = MON ? cnt.stats : cnt.clamp;
+        if (lane == 0 && nsat) atomicAdd(dst, static_cast<unsigned long long>(nsat));
+    }
+    if constexpr (MON) {
+        ntop = __reduce_add_sync(0xFFFFFFFFu, ntop);
+        nbsat = __reduce_add_sync(0xFFFFFFFFu, nbsat);
+        ncoll = __reduce_add_sync(0xFFFFFFFFu, ncoll);
+        if (lane == 0) {
+            if (ntop) atomicAdd(cnt.stats + 1, static_cast<unsigned long long>(ntop));
+            if (nbsat) atomicAdd(cnt.stats + 2, static_cast<unsigned long long>(nbsat));
+            if (ncoll) atomicAdd(cnt.stats + 3, static_cast<unsigned long long>(ncoll));
+        }
     }
 }
 
@@ -495,25 +552,25 @@ cudaError_t launch_row(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld
     return cudaGetLastError();
 }
 
-template <int FMT, int GV, bool MX, bool COUNT, int U>
+template <int FMT, int GV, bool MX, bool COUNT, bool MON, int U>
 cudaError_t launch_groups_u(const uint16_t *x, int64_t rows, int vpr, int64_t ld_x, uint8_t *q,
-                            int64_t ld_q, uint8_t *s, int64_t ld_s, unsigned long long *cnt,
+                            int64_t ld_q, uint8_t *s, int64_t ld_s, MxCounters cnt,
                             cudaStream_t stream) {
     const int gx = (vpr + 256 * U - 1) / (256 * U);
     const int64_t target = static_cast<int64_t>(num_sms()) *
-                           resident_blocks(k_quant_groups<FMT, GV, MX, COUNT, U>, 256);
+                           resident_blocks(k_quant_groups<FMT, GV, MX, COUNT, MON, U>, 256);
     int64_t gy = (target + gx - 1) / gx;
     if (gy > rows) gy = rows;
     if (gy > 65535) gy = 65535;
     if (gy < 1) gy = 1;
-    k_quant_groups<FMT, GV, MX, COUNT, U><<<dim3(gx, static_cast<unsigned>(gy)), 256, 0, stream>>>(
+    k_quant_groups<FMT, GV, MX, COUNT, MON, U><<<dim3(gx, static_cast<unsigned>(gy)), 256, 0, stream>>>(
         x, rows, vpr, ld_x, q, ld_q, s, ld_s, cnt);
     return cudaGetLastError();
 }
 
-template <int FMT, int GV, bool MX, bool COUNT>
+template <int FMT, int GV, bool MX, bool COUNT, bool MON = false>
 cudaError_t launch_groups(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, uint8_t *q,
-                          int64_t ld_q, uint8_t *s, int64_t ld_s, unsigned long long *cnt,
+                          int64_t ld_q, uint8_t *s, int64_t ld_s, MxCounters cnt,
                           cudaStream_t stream) {
     const int vpr = static_cast<int>(cols / 8);
     // vectors per thread: the largest U (up to 4) that leaves no more than
@@ -526,9 +583,9 @@ cudaError_t launch_groups(const uint16_t *x, int64_t rows, int64_t cols, int64_t
             break;
         }
     }
-    if (u == 4) return launch_groups_u<FMT, GV, MX, COUNT, 4>(x, rows, vpr, ld_x, q, ld_q, s, ld_s, cnt, stream);
-    if (u == 2) return launch_groups_u<FMT, GV, MX, COUNT, 2>(x, rows, vpr, ld_x, q, ld_q, s, ld_s, cnt, stream);
-    return launch_groups_u<FMT, GV, MX, COUNT, 1>(x, rows, vpr, ld_x, q, ld_q, s, ld_s, cnt, stream);
+    if (u == 4) return launch_groups_u<FMT, GV, MX, COUNT, MON, 4>(x, rows, vpr, ld_x, q, ld_q, s, ld_s, cnt, stream);
+    if (u == 2) return launch_groups_u<FMT, GV, MX, COUNT, MON, 2>(x, rows, vpr, ld_x, q, ld_q, s, ld_s, cnt, stream);
+    return launch_groups_u<FMT, GV, MX, COUNT, MON, 1>(x, rows, vpr, ld_x, q, ld_q, s, ld_s, cnt, stream);
 }
 }  // namespace
 
@@ -546,29 +603,44 @@ cudaError_t launch_quant_token(const uint16_t *x, int64_t rows, int64_t cols, in
         return fmt == FMT_E4M3 ? launch_row<FMT_E4M3>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream)
                                : launch_row<FMT_E5M2>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream);
     }
+    const MxCounters none{nullptr, nullptr, nullptr};
     return fmt == FMT_E4M3
                ? launch_groups<FMT_E4M3, 16, false, false>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
-                                                           nullptr, stream)
+                                                           none, stream)
                : launch_groups<FMT_E5M2, 16, false, false>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
-                                                           nullptr, stream);
+                                                           none, stream);
 }
 
 cudaError_t launch_quant_mx32(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
                               uint8_t *q, int64_t ld_q, uint8_t *s, int64_t ld_s,
                               unsigned long long *cnt, cudaStream_t stream) {
     if (rows == 0 || cols == 0) return cudaSuccess;
+    const MxCounters c{cnt, nullptr, nullptr};
     if (cnt) {
         return fmt == FMT_E4M3
                    ? launch_groups<FMT_E4M3, 4, true, true>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
-                                                            cnt, stream)
+                                                            c, stream)
                    : launch_groups<FMT_E5M2, 4, true, true>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
-                                                            cnt, stream);
+                                                            c, stream);
     }
     return fmt == FMT_E4M3
                ? launch_groups<FMT_E4M3, 4, true, false>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
-                                                         nullptr, stream)
+                                                         c, stream)
                : launch_groups<FMT_E5M2, 4, true, false>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
-                                                         nullptr, stream);
+                                                         c, stream);
+}
+
+cudaError_t launch_quant_mx32_monitor(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
+                                      int fmt, uint8_t *q, int64_t ld_q, uint8_t *s, int64_t ld_s,
+                                      unsigned long long *stats, unsigned int *row_sat,
+                                      cudaStream_t stream) {
+    if (rows == 0 || cols == 0) return cudaSuccess;
+    const MxCounters c{nullptr, stats, row_sat};
+    return fmt == FMT_E4M3
+               ? launch_groups<FMT_E4M3, 4, true, false, true>(x, rows, cols, ld_x, q, ld_q, s,
+                                                               ld_s, c, stream)
+               : launch_groups<FMT_E5M2, 4, true, false, true>(x, rows, cols, ld_x, q, ld_q, s,
+                                                               ld_s, c, stream);
 }
 
 cudaError_t launch_quant_block128(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,

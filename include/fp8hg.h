@@ -155,6 +155,50 @@ int fp8_quant_mx32(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, 
                    unsigned long long *clamp_count, void *stream);
 
 /*
+ * Counts of the MX clamp monitor (all over the whole tensor):
+ *   saturated         elements whose scaled magnitude x * 2^-e exceeded the
+ *                     format's largest value (448 or 57344) and were written
+ *                     as the largest code
+ *   top_code          elements whose code has the largest finite magnitude
+ *                     (0x7E / 0x7B, either sign): the last quantization bin,
+ *                     reached by saturation or by rounding
+ *   blocks_saturated  32-element blocks holding at least one saturated element
+ *   blocks_collapsed  blocks whose 32 codes are one and the same byte (all
+ *                     values in one bin); blocks of zeros and blocks holding a
+ *                     NaN or an infinity are not counted
+ * The same layout as four consecutive unsigned 64-bit integers.
+ */
+typedef struct {
+    unsigned long long saturated;
+    unsigned long long top_code;
+    unsigned long long blocks_saturated;
+    unsigned long long blocks_collapsed;
+} fp8hg_mx_stats;
+
+/*
+ * fp8_quant_mx32_monitor — fp8_quant_mx32 (identical codes and scales) that
+ * also counts how much of the tensor lands in the last quantization bin.
+ *
+ * Passage: "Characterization and Mitigation of Training Instabilities in
+ * Microscaling Formats": tightly clustered blocks (layer-norm weights) are
+ * pushed into the format's last bin and collapse onto one code ("What
+ * carries the argument"); the fraction of values and of blocks clamped there
+ * is the proposed early-warning signal of divergence ("What would settle
+ * it", "If this is right").  The four counts above are this library's
+ * reading of that signal.
+ *
+ *   stats          device pointer, required, 8-byte aligned; the counts are
+ *                  ADDED to it (the caller zeroes it)
+ *   row_saturated  optional device array [rows] of unsigned 32-bit counts;
+ *                  each row's saturated elements are ADDED (caller zeroes)
+ * Requirements as fp8_quant_mx32.  Counting uses atomics: concurrent calls
+ * may share the same counters.
+ */
+int fp8_quant_mx32_monitor(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
+                           uint8_t *q, int64_t ld_q, uint8_t *scale, int64_t ld_s,
+                           fp8hg_mx_stats *stats, unsigned int *row_saturated, void *stream);
+
+/*
  * One quantized GEMM operand: `rows` rows of `k` FP8 codes, K-contiguous.
  *   codes     device pointer, 16-byte aligned, row stride ld bytes (ld % 16 == 0)
  *   scale     device pointer to the scale bytes of `gran`:

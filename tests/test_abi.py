@@ -8,7 +8,8 @@ import pytest
 import fp8_hybrid_granularity_gb300 as fp8hg
 from fp8_hybrid_granularity_gb300 import Operand, E4M3, GRAN_ROW, GRAN_1x128, GRAN_128x128, GRAN_MX32
 
-EXPECTED = {"fp8_quant_token", "fp8_quant_block128", "fp8_quant_mx32", "fp8_gemm_scaled",
+EXPECTED = {"fp8_quant_token", "fp8_quant_block128", "fp8_quant_mx32", "fp8_quant_mx32_monitor",
+            "fp8_gemm_scaled",
             "fp8_gemm_scaled_ex", "fp8hg_get_device_error", "fp8hg_status_str", "fp8hg_version"}
 
 OK, INVALID, ALIGN, SHAPE, UNSUP = 0, 1, 2, 3, 4
@@ -58,6 +59,13 @@ def test_block128_and_mx_validation(lib):
     m = lib.fp8_quant_mx32
     assert m(FAKE, 4, 48, 48, E4M3, FAKE, 48, FAKE, 2, None, None) == SHAPE
     assert m(FAKE, 4, 64, 64, E4M3, FAKE, 64, FAKE, 2, FAKE + 4, None) == ALIGN
+    mon = lib.fp8_quant_mx32_monitor
+    assert mon(FAKE, 4, 64, 64, E4M3, FAKE, 64, FAKE, 2, None, None, None) == INVALID  # stats
+    assert mon(FAKE, 4, 48, 48, E4M3, FAKE, 48, FAKE, 2, FAKE, None, None) == SHAPE
+    assert mon(FAKE, 4, 64, 64, E4M3, FAKE, 64, FAKE, 2, FAKE + 4, None, None) == ALIGN
+    assert mon(FAKE, 4, 64, 64, E4M3, FAKE, 64, FAKE, 2, FAKE, FAKE + 2, None) == ALIGN
+    assert mon(FAKE, 4, 64, 64, E4M3, FAKE, 64, FAKE, 1, FAKE, None, None) == INVALID  # ld_s
+    assert mon(FAKE, 0, 64, 64, E4M3, FAKE, 64, FAKE, 2, FAKE, None, None) == OK       # empty
 
 
 def _op(rows=256, k=256, gran=GRAN_1x128, ld=None, lds=4, fmt=E4M3, scale=FAKE):
