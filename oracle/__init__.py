@@ -72,6 +72,8 @@ def _load():
         lib.orc_quant_mx32.argtypes = [P, I64, I64, I64, I, P, I64, P, I64, P]
         lib.orc_mx32_monitor.restype = I
         lib.orc_mx32_monitor.argtypes = [P, I64, I64, I64, I, P, I64, P, I64, P, P]
+        lib.orc_requant_t.restype = I
+        lib.orc_requant_t.argtypes = [P, I64, I64, I64, P, I64, I, I, I, P, I64, P, I64]
         lib.orc_dequant.restype = I
         lib.orc_dequant.argtypes = [P, I64, P, I64, I, I, I64, I64, P]
         lib.orc_gemm_ref_pairs.restype = I
@@ -210,6 +212,21 @@ def dequant(q, scale, gran: int, fmt: int) -> np.ndarray:
     _load().orc_dequant(_ptr(q), k, _ptr(scale), scale.shape[1], int(gran), int(fmt),
                         rows, k, _ptr(out))
     return out
+
+
+def requant_t(q, scale, gran: int, fmt_in: int, fmt_out: int):
+    """Stored FP8 operand q [tokens, cols] (ROW or 1x128-along-K scales) ->
+    1x128 groups along the tokens, transposed: (q_t [cols, tokens],
+    scale_t [cols, tokens/128])."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    scale = np.ascontiguousarray(scale, dtype=np.uint8)
+    rows, cols = q.shape
+    qt = np.empty((cols, rows), np.uint8)
+    st = np.empty((cols, rows // 128), np.uint8)
+    rc = _load().orc_requant_t(_ptr(q), rows, cols, cols, _ptr(scale), scale.shape[1], int(gran),
+                               int(fmt_in), int(fmt_out), _ptr(qt), rows, _ptr(st), rows // 128)
+    _check(rc, "requant_t")
+    return qt, st
 
 
 def gemm_ref_dense(a_hat, b_hat):

@@ -386,6 +386,49 @@ int orc_dequant(const uint8_t *q, int64_t ld_q, const uint8_t *scale, int64_t ld
     return 0;
 }
 
+/* Re-quantization of stored FP8 activations for the weight-gradient GEMM.
+ * The recipe keeps activations in FP8 and quantizes every GEMM operand with
+ * fine-grained power-of-two scales ("A Comprehensive FP8 Training Recipe
+ * ...", "What carries the argument"); the weight gradient contracts over
+ * tokens, so its operands need groups that run along the tokens.  Here the
+ * source is the stored operand itself: q [rows = tokens, cols] K-contiguous
+ * with per-token (ROW) or 1x128-along-K scales.  Every element is
+ * dequantized exactly, x_hat = decode(q) * 2^(byte - 127), and x_hat is
+ * quantized again with 1x128 groups along the tokens (UE8M0 round-up, RNE,
+ * format fmt_out), written transposed:
+ *   q_t [cols, rows] (ld_qt), scale_t [cols, rows/128] (ld_st).
+ * A token whose scale byte is 0xFF, or a NaN / infinite code, makes its
+ * output group non-finite (scale 0xFF, codes 0x7F). */
+int orc_requant_t(const uint8_t *q, int64_t rows, int64_t cols, int64_t ld_q,
+                  const uint8_t *scale, int64_t ld_s, int gran, int fmt_in, int fmt_out,
+                  uint8_t *q_t, int64_t ld_qt, uint8_t *scale_t, int64_t ld_st)
+{
+    if (rows % 128 || (gran != ORC_GRAN_ROW && gran != ORC_GRAN_1x128)) return -1;
+    if (gran == ORC_GRAN_1x128 && cols % 128) return -1;
+    double v[128];
+    for (int64_t c = 0; c < cols; c++) {
+        for (int64_t r0 = 0; r0 < rows; r0 += 128) {
+            double amax = 0.0;
+            int nonfinite = 0;
+            for (int i = 0; i < 128; i++) {
+                v[i] = orc_dequant_at(q, ld_q, scale, ld_s, gran, fmt_in, r0 + i, c);
+                if (!isfinite(v[i])) nonfinite = 1;
+                else if (fabs(v[i]) > amax) amax = fabs(v[i]);
+            }
+            uint8_t *out = q_t + c * ld_qt + r0;
+            if (nonfinite) {
+                for (int i = 0; i < 128; i++) out[i] = 0x7F;
+                scale_t[c * ld_st + r0 / 128] = 0xFF;
+                continue;
+            }
+            int e = orc_ue8m0_exp(amax, fmt_out);
+            for (int i = 0; i < 128; i++) out[i] = orc_fp8_encode(ldexp(v[i], -e), fmt_out, 0);
+            scale_t[c * ld_st + r0 / 128] = (uint8_t)(e + 127);
+        }
+    }
+    return 0;
+}
+
 /* Reference scaled GEMM at chosen output positions:
  *   C_ref[i,j] = sum_k a_hat[i,k] * b_hat[j,k]        (fp64)
  *   S[i,j]     = sum_k |a_hat[i,k] * b_hat[j,k]|      (the tolerance scale)

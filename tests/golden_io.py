@@ -2,13 +2,25 @@
 from __future__ import annotations
 
 import os
+import re
 
 import numpy as np
 
 GOLDEN_DIR = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
 
+def _expand_groups(text: str) -> str:
+    """"(a b)*n" -> the group written n times."""
+    pat = re.compile(r"\(([^()]*)\)\*(\d+)")
+    while True:
+        new = pat.sub(lambda m: " ".join([m.group(1)] * int(m.group(2))), text)
+        if new == text:
+            return text
+        text = new
+
+
 def _hex_list(text: str):
+    text = _expand_groups(text)
     out = []
     for tok in text.split():
         if "*" in tok:
@@ -32,7 +44,7 @@ def load_quant_examples(name: str = "quant_examples.txt"):
                 cases.append(cur)
             elif key in ("x",):
                 cur[key] = np.array(_hex_list(val), np.uint16)
-            elif key in ("q",):
+            elif key in ("q", "q_in", "s_in", "q_out", "s_out"):
                 cur[key] = np.array(_hex_list(val), np.uint8)
             elif key == "scale":
                 cur[key] = int(val, 16)
