@@ -12,6 +12,7 @@ Tensor-level API (same names as the C entry points):
   fp8_quant_block128(x, fmt, transposed_copy=False)     -> QTensor[, QTensor]
   fp8_quant_mx32(x, fmt, clamp_count=None)              -> QTensor
   fp8_quant_mx32_monitor(x, fmt, stats=None, row_saturated=None) -> QTensor, stats
+  fp8_requant_t(src QTensor, fmt)                       -> QTensor (transposed)
   fp8_gemm_scaled(op, a, b, out=None, out_dtype=bf16, accumulate=False)
   fp8hg_get_device_error(stream=None)
 
@@ -86,6 +87,7 @@ def load_library(build_if_stale: bool = True):
         lib.fp8_quant_block128.argtypes = [P, I64, I64, I64, I, P, I64, P, I64, P, I64, P, I64, P]
         lib.fp8_quant_mx32.argtypes = [P, I64, I64, I64, I, P, I64, P, I64, P, P]
         lib.fp8_quant_mx32_monitor.argtypes = [P, I64, I64, I64, I, P, I64, P, I64, P, P, P]
+        lib.fp8_requant_t.argtypes = [P, I64, I64, I64, P, I64, I, I, I, P, I64, P, I64, P]
         lib.fp8_gemm_scaled.argtypes = [I, ctypes.POINTER(Operand), ctypes.POINTER(Operand), P,
                                         I64, I, I, P]
         lib.fp8_gemm_scaled_ex.argtypes = [I, ctypes.POINTER(Operand), ctypes.POINTER(Operand), P,
@@ -240,6 +242,23 @@ def fp8_quant_mx32(x, fmt: int = E4M3, clamp_count=None, out=None, stream=None) 
                               out.codes.stride(0), _ptr(out.scale), out.scale.stride(0),
                               _ptr(clamp_count), _stream(stream))
     _check(rc, "fp8_quant_mx32")
+    return out
+
+
+def fp8_requant_t(src: QTensor, fmt: int = E4M3, out: Optional[QTensor] = None,
+                  stream=None) -> QTensor:
+    """Re-quantize a stored per-token or 1x128 operand [tokens, cols] into
+    1x128 groups along the tokens, transposed ([cols, tokens]): the
+    weight-gradient operand, from the FP8 codes instead of the BF16 source."""
+    if src.gran not in (GRAN_ROW, GRAN_1x128):
+        raise ValueError("source must have per-token or 1x128 scales")
+    rows, cols = src.codes.shape
+    out = out if out is not None else alloc_token(rows, cols, 128, fmt, True, src.codes.device)
+    rc = lib().fp8_requant_t(_ptr(src.codes), rows, cols, src.codes.stride(0), _ptr(src.scale),
+                             src.scale.stride(0), src.gran, src.fmt, fmt, _ptr(out.codes),
+                             out.codes.stride(0), _ptr(out.scale), out.scale.stride(0),
+                             _stream(stream))
+    _check(rc, "fp8_requant_t")
     return out
 
 

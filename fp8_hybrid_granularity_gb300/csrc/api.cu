@@ -147,6 +147,25 @@ int fp8_quant_mx32_monitor(const uint16_t *x, int64_t rows, int64_t cols, int64_
         static_cast<cudaStream_t>(stream)));
 }
 
+int fp8_requant_t(const uint8_t *q, int64_t rows, int64_t cols, int64_t ld_q, const uint8_t *scale,
+                  int64_t ld_s, int gran, int fmt_in, int fmt_out, uint8_t *q_t, int64_t ld_qt,
+                  uint8_t *scale_t, int64_t ld_st, void *stream) {
+    if (!valid_fmt(fmt_in) || !valid_fmt(fmt_out)) return FP8HG_ERR_INVALID_ARG;
+    if (gran != FP8HG_GRAN_ROW && gran != FP8HG_GRAN_1x128) return FP8HG_ERR_UNSUPPORTED;
+    if (rows < 0 || cols < 0) return FP8HG_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return FP8HG_OK;
+    if (!q || !scale || !q_t || !scale_t) return FP8HG_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(q_t, 16) || ld_q % 16 || ld_qt % 16) return FP8HG_ERR_ALIGNMENT;
+    if (rows % 128 || cols % 128) return FP8HG_ERR_SHAPE;
+    if (rows / 128 > 65535) return FP8HG_ERR_SHAPE;
+    if (ld_q < cols || ld_qt < rows || ld_st < rows / 128) return FP8HG_ERR_INVALID_ARG;
+    if (ld_s < (gran == FP8HG_GRAN_ROW ? 1 : cols / 128)) return FP8HG_ERR_INVALID_ARG;
+    return status_from_cuda(fp8hg::launch_requant_t(q, rows, cols, ld_q, scale, ld_s,
+                                                    gran == FP8HG_GRAN_ROW ? 1 : 0, fmt_in,
+                                                    fmt_out, q_t, ld_qt, scale_t, ld_st,
+                                                    static_cast<cudaStream_t>(stream)));
+}
+
 int fp8_gemm_scaled_ex(int op, const fp8hg_operand *a, const fp8hg_operand *b, void *c, int64_t ldc,
                        int out, int accumulate, const fp8hg_gemm_opts *opts, void *stream) {
     if (op < FP8HG_FPROP || op > FP8HG_WGRAD) return FP8HG_ERR_INVALID_ARG;

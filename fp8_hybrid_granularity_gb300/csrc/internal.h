@@ -1,11 +1,21 @@
 // Launchers shared between the C-ABI layer (api.cu) and the kernel files.
 // Arguments are validated by the caller; these only configure and launch.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
 
 namespace fp8hg {
+
+// cuTensorMapEncodeTiled, looked up once through the runtime's driver entry
+// point (no link against libcuda); null if the driver does not provide it.
+using TensorMapEncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                       const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                       const cuuint32_t *, CUtensorMapInterleave,
+                                       CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                       CUtensorMapFloatOOBfill);
+TensorMapEncodeFn tensor_map_encoder();
 
 cudaError_t launch_quant_token(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
                                int group, int transpose, int fmt, uint8_t *q, int64_t ld_q,
@@ -19,6 +29,11 @@ cudaError_t launch_quant_mx32_monitor(const uint16_t *x, int64_t rows, int64_t c
                                       int fmt, uint8_t *q, int64_t ld_q, uint8_t *s, int64_t ld_s,
                                       unsigned long long *stats, unsigned int *row_sat,
                                       cudaStream_t stream);
+
+cudaError_t launch_requant_t(const uint8_t *q, int64_t rows, int64_t cols, int64_t ld_q,
+                             const uint8_t *s, int64_t ld_s, int per_token, int fmt_in,
+                             int fmt_out, uint8_t *qt, int64_t ld_qt, uint8_t *st, int64_t ld_st,
+                             cudaStream_t stream);
 
 cudaError_t launch_quant_block128(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
                                   int fmt, uint8_t *q, int64_t ld_q, uint8_t *s, int64_t ld_s,

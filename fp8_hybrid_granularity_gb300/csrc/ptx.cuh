@@ -149,6 +149,24 @@ __device__ __forceinline__ uint32_t cvt_e5m2x2(float lo, float hi) {
     asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
     return r;
 }
+// Two FP8 codes (the low and high byte of v) -> packed F16x2; exact, since
+// every E4M3 and E5M2 value is an F16 value.  The low byte lands in the low half.
+__device__ __forceinline__ uint32_t cvt_f16x2_e4m3x2(uint16_t v) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+    return r;
+}
+__device__ __forceinline__ uint32_t cvt_f16x2_e5m2x2(uint16_t v) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(r) : "h"(v));
+    return r;
+}
+// The two halves of a packed F16x2 as floats (exact widening).
+__device__ __forceinline__ void f16x2_to_f32(uint32_t h2, float &lo, float &hi) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h2));
+}
 // Two floats -> packed BF16x2, round to nearest even; `lo` in the low half.
 __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
     uint32_t r;

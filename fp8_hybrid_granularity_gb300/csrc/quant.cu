@@ -20,9 +20,12 @@
 //                    transposed: the weight-gradient GEMM's operand layout.
 //  k_quant_block128  one scale per 128x128 block (block-wise weights), with
 //                    an optional transposed copy for the data-gradient GEMM.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstring>
+#include <mutex>
 
 #include "internal.h"
 #include "quant_math.cuh"
@@ -381,6 +384,201 @@ __global__ void __launch_bounds__(256) k_quant_t(const uint16_t *__restrict__ x,
     }
 }
 
+// ------------------------------- stored FP8 codes -> 1x128 along the tokens
+// Re-quantizes a stored operand (codes [tokens, cols], per-token or
+// 1x128-along-K scales) for the weight-gradient GEMM.  Persistent CTAs walk
+// 128-token x 128-column tiles; each tile's codes (16 KB) arrive by one 2-D
+// TMA copy into one of kRqStages shared-memory stages, issued kRqStages tiles
+// ahead, and the 128 tokens' scale bytes are fetched one tile ahead into
+// registers.  Thread (cq, tg) owns columns 4cq..4cq+3 for the 16 tokens
+// 16tg..16tg+15 and reads one 32-bit word (four columns of one token) per
+// token.  Pass 1 decodes each stored value exactly in FP32 (code -> F16 ->
+// F32, times the token's power-of-two scale; no FTZ, so even 2^-136 is exact)
+// and keeps a NaN-propagating max of the magnitudes; the eight token groups
+// of a column are combined in shared memory.  Pass 2 decodes again from the
+// words held in registers and casts with the column's round-up scale.  Each
+// column's 16 codes become one 16-byte chunk of the transposed tile, whose
+// chunks are XOR-swizzled so that neither the chunk writes nor the row reads
+// for the coalesced global stores conflict.
+constexpr int kRQ = 128;          // tokens and columns per tile
+constexpr int kRqStages = 4;
+constexpr uint32_t kRqTileBytes = kRQ * kRQ;
+constexpr uint64_t kRqWaitNs = 2000000000ull;  // bound on one tile's copy (2 s)
+
+struct RqSmem {
+    uint32_t cin[kRqStages][kRQ][kRQ / 4];   // [stage][token][4 columns]
+    uint4 cout[kRQ][kRQ / 16];               // [column][swizzled 16-token chunk]
+    float mul_in[kRQ];
+    float red[8][kRQ];
+    float mul_out[kRQ];
+    uint32_t nan_col[kRQ];
+    uint64_t full[kRqStages];
+    int ok;
+};
+
+template <int FIN>
+__device__ __forceinline__ void decode4(uint32_t w, float (&f)[4]) {
+    uint32_t lo, hi;
+    if constexpr (FIN == FMT_E4M3) {
+        lo = ptx::cvt_f16x2_e4m3x2(static_cast<uint16_t>(w));
+        hi = ptx::cvt_f16x2_e4m3x2(static_cast<uint16_t>(w >> 16));
+    } else {
+        lo = ptx::cvt_f16x2_e5m2x2(static_cast<uint16_t>(w));
+        hi = ptx::cvt_f16x2_e5m2x2(static_cast<uint16_t>(w >> 16));
+    }
+    ptx::f16x2_to_f32(lo, f[0], f[1]);
+    ptx::f16x2_to_f32(hi, f[2], f[3]);
+}
+
+// max(a, |b|), NaN if either is NaN.
+__device__ __forceinline__ float max_abs_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(fabsf(b)));
+    return r;
+}
+
+__device__ __forceinline__ float scale_mul(uint32_t b) {
+    return (b == 0xFFu) ? __uint_as_float(0x7FC00000u) : pow2f(static_cast<int>(b) - 127);
+}
+
+template <int FIN, int FOUT>
+__global__ void __launch_bounds__(256, 2) k_requant_t(const __grid_constant__ CUtensorMap tq,
+                                                      const uint8_t *__restrict__ s, int64_t ld_s,
+                                                      int scale_col_step, int tiles_x, int ntiles,
+                                                      uint8_t *__restrict__ qt, int64_t ld_qt,
+                                                      uint8_t *__restrict__ st, int64_t ld_st,
+                                                      unsigned int *err) {
+    extern __shared__ __align__(128) uint8_t rq_smem[];
+    RqSmem &sm = *reinterpret_cast<RqSmem *>(rq_smem);
+    const int tid = threadIdx.x;
+    const int step = gridDim.x;
+    const uint32_t fbar = ptx::smem_u32(&sm.full[0]);
+    auto issue = [&](int tile, int stage) {
+        const int bx = tile % tiles_x, by = tile / tiles_x;
+        ptx::mbar_arrive_expect_tx(fbar + 8 * stage, kRqTileBytes);
+        ptx::tma_load_2d(ptx::smem_u32(&sm.cin[stage][0][0]), &tq, fbar + 8 * stage, bx * kRQ,
+                         by * kRQ);
+    };
+    auto scale_byte = [&](int tile) -> uint32_t {
+        const int bx = tile % tiles_x, by = tile / tiles_x;
+        return s[(static_cast<int64_t>(by) * kRQ + tid) * ld_s +
+                 static_cast<int64_t>(bx) * scale_col_step];
+    };
+    int issued = 0;  // tiles whose copy thread 0 has issued
+    if (tid == 0) {
+        ptx::prefetch_tmap(&tq);
+        for (int i = 0; i < kRqStages; ++i) ptx::mbar_init(fbar + 8 * i, 1);
+        ptx::fence_mbar_init();
+        for (int i = 0; i < kRqStages; ++i) {
+            const int tile = blockIdx.x + i * step;
+            if (tile >= ntiles) break;
+            issue(tile, i);
+            ++issued;
+        }
+    }
+    uint32_t sb = (tid < kRQ && static_cast<int>(blockIdx.x) < ntiles) ? scale_byte(blockIdx.x) : 0u;
+    __syncthreads();
+    const int cq = tid & 31, tg = tid >> 5;
+    int k = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += step, ++k) {
+        const int stage = k % kRqStages;
+        const int bx = tile % tiles_x, by = tile / tiles_x;
+        if (tid < kRQ) {
+            sm.mul_in[tid] = scale_mul(sb);
+            if (tile + step < ntiles) sb = scale_byte(tile + step);   // one tile ahead
+        }
+        if (tid == 0) {
+            const uint32_t bar = fbar + 8 * stage, parity = static_cast<uint32_t>(k / kRqStages) & 1u;
+            bool ok = ptx::mbar_try_wait(bar, parity);
+            if (!ok) {
+                const uint64_t t0 = ptx::globaltimer();
+                while (!(ok = ptx::mbar_try_wait(bar, parity)))
+                    if (ptx::globaltimer() - t0 > kRqWaitNs) break;
+            }
+            sm.ok = ok;
+        }
+        __syncthreads();                                           // (A)
+        if (!sm.ok) break;
+        uint32_t w[16];
+        float amax[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int t = 16 * tg + i;
+            w[i] = sm.cin[stage][t][cq];
+            const float mi = sm.mul_in[t];
+            float f[4];
+            decode4<FIN>(w[i], f);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) amax[j] = max_abs_nan(amax[j], f[j] * mi);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sm.red[tg][4 * cq + j] = amax[j];
+        __syncthreads();                                           // (B) stage consumed
+        if (tid == 0 && tile + kRqStages * step < ntiles) {
+            issue(tile + kRqStages * step, stage);
+            ++issued;
+        }
+        if (tid < kRQ) {
+            float m = sm.red[0][tid];
+#pragma unroll
+            for (int r = 1; r < 8; ++r) m = max_abs_nan(m, sm.red[r][tid]);
+            const uint32_t mb = __float_as_uint(m);
+            const bool nonfinite = mb >= 0x7F800000u;
+            const int e = nonfinite ? 128 : ue8m0_exponent_f32<FOUT>(mb);
+            sm.mul_out[tid] = nonfinite ? 0.0f : pow2f(-e);
+            sm.nan_col[tid] = nonfinite;
+            st[(static_cast<int64_t>(bx) * kRQ + tid) * ld_st + by] = static_cast<uint8_t>(e + 127);
+        }
+        __syncthreads();                                           // (C)
+        float mo[4];
+        uint32_t out[4][4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mo[j] = sm.mul_out[4 * cq + j];
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {       // token pairs (16tg + 2p, 16tg + 2p + 1)
+            const int t = 16 * tg + 2 * p;
+            const float ma = sm.mul_in[t], mb = sm.mul_in[t + 1];
+            float a[4], b[4];
+            decode4<FIN>(w[2 * p], a);
+            decode4<FIN>(w[2 * p + 1], b);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t pair = cvt2<FOUT>((a[j] * ma) * mo[j], (b[j] * mb) * mo[j]);
+                if (p & 1) out[j][p >> 1] |= pair << 16;
+                else out[j][p >> 1] = pair;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int c = 4 * cq + j;
+            const uint4 v = sm.nan_col[c] ? make_uint4(kNanCodes, kNanCodes, kNanCodes, kNanCodes)
+                                          : make_uint4(out[j][0], out[j][1], out[j][2], out[j][3]);
+            sm.cout[c][tg ^ (cq & 7)] = v;  // row c = 4cq + j, so (c >> 2) & 7 == cq & 7
+        }
+        __syncthreads();                                           // (D)
+        const int64_t r0 = static_cast<int64_t>(by) * kRQ, c0 = static_cast<int64_t>(bx) * kRQ;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int idx = tid + 256 * i;
+            const int row = idx >> 3, ch = idx & 7;
+            *reinterpret_cast<uint4 *>(qt + (c0 + row) * ld_qt + r0 + ch * 16) =
+                sm.cout[row][ch ^ ((row >> 2) & 7)];
+        }
+    }
+    if (tid == 0 && k < issued) {
+        // a copy ran out of time: record it and wait (bounded) for the copies
+        // still in flight before the CTA's shared memory is released
+        atomicOr(err, 4u);
+        for (int j = k; j < issued; ++j) {
+            const uint32_t bar = fbar + 8 * (j % kRqStages);
+            const uint32_t parity = static_cast<uint32_t>(j / kRqStages) & 1u;
+            const uint64_t t0 = ptx::globaltimer();
+            while (!ptx::mbar_try_wait(bar, parity))
+                if (ptx::globaltimer() - t0 > kRqWaitNs) break;
+        }
+    }
+}
+
 // ------------------------------------------------------------ 128x128 blocks
 // 4x4 byte transpose of four 32-bit rows: result word j = byte j of each row.
 __device__ __forceinline__ void transpose4x4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -450,6 +648,20 @@ __global__ void __launch_bounds__(256) k_quant_block128(const uint16_t *__restri
 }
 
 // ------------------------------------------------------------------ launchers
+TensorMapEncodeFn tensor_map_encoder() {
+    static TensorMapEncodeFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult res;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &res) == cudaSuccess &&
+            res == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<TensorMapEncodeFn>(ptr);
+    });
+    return fn;
+}
+
 namespace {
 int g_num_sms[64] = {0};
 
@@ -641,6 +853,51 @@ cudaError_t launch_quant_mx32_monitor(const uint16_t *x, int64_t rows, int64_t c
                                                                ld_s, c, stream)
                : launch_groups<FMT_E5M2, 4, true, false, true>(x, rows, cols, ld_x, q, ld_q, s,
                                                                ld_s, c, stream);
+}
+
+cudaError_t launch_requant_t(const uint8_t *q, int64_t rows, int64_t cols, int64_t ld_q,
+                             const uint8_t *s, int64_t ld_s, int per_token, int fmt_in,
+                             int fmt_out, uint8_t *qt, int64_t ld_qt, uint8_t *st, int64_t ld_st,
+                             cudaStream_t stream) {
+    if (rows == 0 || cols == 0) return cudaSuccess;
+    CUtensorMap tq;
+    std::memset(&tq, 0, sizeof(tq));
+    TensorMapEncodeFn enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld_q)};
+    const cuuint32_t box[2] = {kRQ, kRQ};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(q), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    unsigned int *err = device_error_word();
+    if (!err) return cudaErrorInvalidValue;
+    const int tiles_x = static_cast<int>(cols / kRQ);
+    const int64_t ntiles64 = (rows / kRQ) * static_cast<int64_t>(tiles_x);
+    if (ntiles64 > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    const int ntiles = static_cast<int>(ntiles64);
+    const int step = per_token ? 0 : 1;
+    const size_t smem = sizeof(RqSmem);
+    auto run = [&](auto kern) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem);
+        if (e != cudaSuccess) return e;
+        int64_t grid = static_cast<int64_t>(num_sms()) * (per_sm > 0 ? per_sm : 1);
+        if (grid > ntiles) grid = ntiles;
+        kern<<<static_cast<unsigned>(grid), 256, smem, stream>>>(tq, s, ld_s, step, tiles_x, ntiles,
+                                                                 qt, ld_qt, st, ld_st, err);
+        return cudaGetLastError();
+    };
+    if (fmt_in == FMT_E4M3)
+        return fmt_out == FMT_E4M3 ? run(k_requant_t<FMT_E4M3, FMT_E4M3>)
+                                   : run(k_requant_t<FMT_E4M3, FMT_E5M2>);
+    return fmt_out == FMT_E4M3 ? run(k_requant_t<FMT_E5M2, FMT_E4M3>)
+                               : run(k_requant_t<FMT_E5M2, FMT_E5M2>);
 }
 
 cudaError_t launch_quant_block128(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,

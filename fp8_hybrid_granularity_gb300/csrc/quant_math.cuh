@@ -53,6 +53,18 @@ __device__ __forceinline__ int mx_exponent(uint32_t amax_bits) {
     return clamp_exp((ef - 127) - emax);
 }
 
+// The round-up rule on an FP32 amax pattern (sign cleared, finite): 1.m >
+// 1.75 when the 23-bit mantissa field exceeds 0x600000; zero and subnormal
+// amax give the clamp value -127 (any subnormal is below FMAX * 2^-127).
+template <int FMT>
+__device__ __forceinline__ int ue8m0_exponent_f32(uint32_t amax_bits) {
+    constexpr int emax = (FMT == FMT_E4M3) ? 8 : 15;
+    const int ef = static_cast<int>(amax_bits >> 23);
+    const uint32_t mf = amax_bits & 0x7FFFFFu;
+    if (ef == 0) return -127;
+    return clamp_exp((ef - 127) - emax + (mf > 0x600000u ? 1 : 0));
+}
+
 // 2^n as a float for n in [-127, 127] (2^-127 is an FP32 subnormal).
 __device__ __forceinline__ float pow2f(int n) {
     return (n >= -126) ? __uint_as_float(static_cast<uint32_t>(n + 127) << 23)

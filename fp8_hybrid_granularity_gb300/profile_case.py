@@ -18,6 +18,9 @@ kernel, and prints the mean launch time from CUDA events.  Cases:
   quant_t    1x128-along-tokens transposed quantization of H [M, 18944]
   block128   128x128 quantization (+ transposed copy) of W_down [3584, 18944]
   mx32       MXFP8 quantization of [M, 4096]
+  mx32_mon   the same with the clamp monitor's counts
+  requant    stored per-token FP8 codes of H [M, 18944] -> 1x128 along the
+             tokens, transposed (the weight-gradient operand)
 """
 from __future__ import annotations
 
@@ -35,7 +38,7 @@ HID, MLP = 3584, 18944
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("case", choices=["gemm", "gemm_gate", "wgrad", "quant_row", "quant_1x128", "quant_t", "block128",
-                                     "mx32"])
+                                     "mx32", "mx32_mon", "requant"])
     ap.add_argument("--m", type=int, default=4096)
     ap.add_argument("--warmup", type=int, default=2)
     ap.add_argument("--iters", type=int, default=3)
@@ -81,10 +84,21 @@ def main():
         o, ot = fp8hg.alloc_block128(HID, MLP, E4, True, dev)
         fn = lambda: fp8hg.fp8_quant_block128(w, E4, True, out=o, out_t=ot)
         work, unit = 4.0 * HID * MLP + 2.0 * HID * MLP / 16384, "byte"
+    elif args.case == "requant":
+        h = mk("act", M, MLP, "H")
+        src = fp8hg.fp8_quant_token(h, 0, E4)
+        o = fp8hg.alloc_token(M, MLP, 128, E4, True, dev)
+        fn = lambda: fp8hg.fp8_requant_t(src, E4, out=o)
+        work, unit = 2.0 * M * MLP + M + M * MLP / 128, "byte"
     else:
         x = mk("mx_ln", M, 4096, "A")
         o = fp8hg.alloc_mx32(M, 4096, E4, dev)
-        fn = lambda: fp8hg.fp8_quant_mx32(x, E4, out=o)
+        if args.case == "mx32_mon":
+            st = torch.zeros(4, dtype=torch.int64, device=dev)
+            rs = torch.zeros(M, dtype=torch.int32, device=dev)
+            fn = lambda: fp8hg.fp8_quant_mx32_monitor(x, E4, stats=st, row_saturated=rs, out=o)
+        else:
+            fn = lambda: fp8hg.fp8_quant_mx32(x, E4, out=o)
         work, unit = 3.0 * M * 4096 + M * 4096 / 32, "byte"
     torch.cuda.synchronize()
     for _ in range(args.warmup):

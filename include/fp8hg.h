@@ -155,6 +155,34 @@ int fp8_quant_mx32(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, 
                    unsigned long long *clamp_count, void *stream);
 
 /*
+ * fp8_requant_t — re-quantizes a STORED FP8 activation for the
+ * weight-gradient GEMM: 1x128 groups along the tokens, written transposed,
+ * computed from the FP8 codes and their scales instead of the BF16 original.
+ *
+ * Passage: "A Comprehensive FP8 Training Recipe ...", "What carries the
+ * argument" (activations kept in FP8 with fine-grained power-of-two scales;
+ * the weight gradient contracts over tokens, so its operands need groups
+ * that run along the tokens).  Each stored value x_hat = decode(q) *
+ * 2^(byte - 127) is taken exactly; the output is the UE8M0 round-up
+ * quantization of x_hat in groups of 128 consecutive tokens of one column,
+ * cast to fmt_out by round-to-nearest-even.
+ *
+ *   q        [rows = tokens, cols] codes of format fmt_in (ld_q bytes)
+ *   scale    gran = FP8HG_GRAN_ROW: [rows] (ld_s >= 1); FP8HG_GRAN_1x128:
+ *            [rows, cols/128] (ld_s >= cols/128)
+ *   q_t      [cols, rows] codes of format fmt_out (ld_qt bytes)
+ *   scale_t  [cols, rows/128] (ld_st bytes)
+ * A token whose scale byte is 0xFF, or a NaN / infinite code, makes the
+ * output groups it belongs to non-finite (scale 0xFF, codes 0x7F).
+ * Requirements: rows % 128 == 0, cols % 128 == 0; q, q_t 16-byte aligned;
+ * ld_q % 16 == 0, ld_qt % 16 == 0; every stored value finite in FP32
+ * (|x_hat| < 2^128: true of every operand quantized from BF16).
+ */
+int fp8_requant_t(const uint8_t *q, int64_t rows, int64_t cols, int64_t ld_q, const uint8_t *scale,
+                  int64_t ld_s, int gran, int fmt_in, int fmt_out, uint8_t *q_t, int64_t ld_qt,
+                  uint8_t *scale_t, int64_t ld_st, void *stream);
+
+/*
  * Counts of the MX clamp monitor (all over the whole tensor):
  *   saturated         elements whose scaled magnitude x * 2^-e exceeded the
  *                     format's largest value (448 or 57344) and were written

@@ -9,6 +9,7 @@ import fp8_hybrid_granularity_gb300 as fp8hg
 from fp8_hybrid_granularity_gb300 import Operand, E4M3, GRAN_ROW, GRAN_1x128, GRAN_128x128, GRAN_MX32
 
 EXPECTED = {"fp8_quant_token", "fp8_quant_block128", "fp8_quant_mx32", "fp8_quant_mx32_monitor",
+            "fp8_requant_t",
             "fp8_gemm_scaled",
             "fp8_gemm_scaled_ex", "fp8hg_get_device_error", "fp8hg_status_str", "fp8hg_version"}
 
@@ -66,6 +67,28 @@ def test_block128_and_mx_validation(lib):
     assert mon(FAKE, 4, 64, 64, E4M3, FAKE, 64, FAKE, 2, FAKE, FAKE + 2, None) == ALIGN
     assert mon(FAKE, 4, 64, 64, E4M3, FAKE, 64, FAKE, 1, FAKE, None, None) == INVALID  # ld_s
     assert mon(FAKE, 0, 64, 64, E4M3, FAKE, 64, FAKE, 2, FAKE, None, None) == OK       # empty
+
+
+def test_requant_validation(lib):
+    r = lib.fp8_requant_t
+
+    def call(rows=256, cols=256, ld_q=256, ld_s=2, gran=GRAN_1x128, fi=E4M3, fo=E4M3, q=FAKE,
+             qt=FAKE, ld_qt=256, ld_st=2, s=FAKE, st=FAKE):
+        return r(q, rows, cols, ld_q, s, ld_s, gran, fi, fo, qt, ld_qt, st, ld_st, None)
+
+    assert call(gran=GRAN_128x128) == UNSUP
+    assert call(fi=5) == INVALID
+    assert call(fo=-1) == INVALID
+    assert call(rows=0) == OK                       # empty: nothing read or written
+    assert call(q=None) == INVALID
+    assert call(st=None) == INVALID
+    assert call(q=FAKE + 8) == ALIGN
+    assert call(ld_qt=264) == ALIGN
+    assert call(rows=200, ld_qt=208) == SHAPE
+    assert call(cols=192, ld_q=192) == SHAPE
+    assert call(ld_q=128) == INVALID                # ld_q < cols
+    assert call(ld_s=1) == INVALID                  # 1x128 needs cols/128 scale columns
+    assert call(ld_st=1) == INVALID                 # rows/128 output scale columns
 
 
 def _op(rows=256, k=256, gran=GRAN_1x128, ld=None, lds=4, fmt=E4M3, scale=FAKE):
