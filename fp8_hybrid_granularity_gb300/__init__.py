@@ -14,6 +14,7 @@ Tensor-level API (same names as the C entry points):
   fp8_quant_mx32_monitor(x, fmt, stats=None, row_saturated=None) -> QTensor, stats
   fp8_requant_t(src QTensor, fmt)                       -> QTensor (transposed)
   fp8_gemm_scaled(op, a, b, out=None, out_dtype=bf16, accumulate=False)
+  fp8_gemm_scaled_q(op, a, b, fmt)                      -> QTensor (1x128 along N)
   fp8hg_get_device_error(stream=None)
 
 Scale arrays are allocated with their column count rounded up to a multiple
@@ -88,6 +89,8 @@ def load_library(build_if_stale: bool = True):
         lib.fp8_quant_mx32.argtypes = [P, I64, I64, I64, I, P, I64, P, I64, P, P]
         lib.fp8_quant_mx32_monitor.argtypes = [P, I64, I64, I64, I, P, I64, P, I64, P, P, P]
         lib.fp8_requant_t.argtypes = [P, I64, I64, I64, P, I64, I, I, I, P, I64, P, I64, P]
+        lib.fp8_gemm_scaled_q.argtypes = [I, ctypes.POINTER(Operand), ctypes.POINTER(Operand), P,
+                                          I64, P, I64, I, P]
         lib.fp8_gemm_scaled.argtypes = [I, ctypes.POINTER(Operand), ctypes.POINTER(Operand), P,
                                         I64, I, I, P]
         lib.fp8_gemm_scaled_ex.argtypes = [I, ctypes.POINTER(Operand), ctypes.POINTER(Operand), P,
@@ -290,6 +293,20 @@ def fp8_quant_mx32_monitor(x, fmt: int = E4M3, stats=None, row_saturated=None, o
                                       _ptr(stats), _ptr(row_saturated), _stream(stream))
     _check(rc, "fp8_quant_mx32_monitor")
     return out, stats
+
+
+def fp8_gemm_scaled_q(op: int, a: QTensor, b: QTensor, fmt: int = E4M3,
+                      out: Optional[QTensor] = None, stream=None) -> QTensor:
+    """C = A * B^T with C quantized in the GEMM's epilogue: FP8 codes [M, N]
+    with one UE8M0 scale per 128 columns of a row (a 1x128 operand)."""
+    M, N = a.codes.shape[0], b.codes.shape[0]
+    out = out if out is not None else alloc_token(M, N, 128, fmt, False, a.codes.device)
+    oa, ob = a.operand(), b.operand()
+    rc = lib().fp8_gemm_scaled_q(op, ctypes.byref(oa), ctypes.byref(ob), _ptr(out.codes),
+                                 out.codes.stride(0), _ptr(out.scale), out.scale.stride(0), fmt,
+                                 _stream(stream))
+    _check(rc, "fp8_gemm_scaled_q")
+    return out
 
 
 def fp8_gemm_scaled(op: int, a: QTensor, b: QTensor, out=None, out_dtype=None,

@@ -71,6 +71,49 @@ int check_quant_common(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld
 
 }  // namespace
 
+namespace {
+
+// Checks shared by the GEMM entry points and the common part of GemmArgs.
+int prepare_gemm(int op, const fp8hg_operand *a, const fp8hg_operand *b, fp8hg::GemmArgs &g) {
+    if (op < FP8HG_FPROP || op > FP8HG_WGRAD) return FP8HG_ERR_INVALID_ARG;
+    int st = validate_operand(a);
+    if (st != FP8HG_OK) return st;
+    st = validate_operand(b);
+    if (st != FP8HG_OK) return st;
+    if (a->k != b->k) return FP8HG_ERR_SHAPE;
+    if (!gran_pair_ok(op, a->gran, b->gran)) return FP8HG_ERR_UNSUPPORTED;
+    g = fp8hg::GemmArgs{};
+    g.a_codes = a->codes;
+    g.b_codes = b->codes;
+    g.a_scale = a->scale;
+    g.b_scale = b->scale;
+    g.M = a->rows;
+    g.N = b->rows;
+    g.K = a->k;
+    g.lda = a->ld;
+    g.ldb = b->ld;
+    g.ld_sa = a->ld_scale;
+    g.ld_sb = b->ld_scale;
+    g.fmt_a = a->fmt;
+    g.fmt_b = b->fmt;
+    g.gran_a = a->gran;
+    g.gran_b = b->gran;
+    return FP8HG_OK;
+}
+
+int run_gemm(fp8hg::GemmArgs &g, const fp8hg_gemm_opts *opts, void *stream) {
+    unsigned int *err = fp8hg::device_error_word();
+    if (!err) return FP8HG_ERR_CUDA;
+    g.wait_limit_ns = (opts && opts->wait_limit_ns) ? opts->wait_limit_ns : kDefaultWaitNs;
+    g.inject_fault = opts ? opts->inject_fault : 0;
+    g.err = err;
+    const int rc = fp8hg::launch_gemm_scaled(g, static_cast<cudaStream_t>(stream));
+    if (rc == 1) return FP8HG_ERR_UNSUPPORTED;  // tensor map could not be encoded
+    return rc == 0 ? FP8HG_OK : FP8HG_ERR_CUDA;
+}
+
+}  // namespace
+
 extern "C" {
 
 int fp8_quant_token(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int group,
@@ -168,49 +211,39 @@ int fp8_requant_t(const uint8_t *q, int64_t rows, int64_t cols, int64_t ld_q, co
 
 int fp8_gemm_scaled_ex(int op, const fp8hg_operand *a, const fp8hg_operand *b, void *c, int64_t ldc,
                        int out, int accumulate, const fp8hg_gemm_opts *opts, void *stream) {
-    if (op < FP8HG_FPROP || op > FP8HG_WGRAD) return FP8HG_ERR_INVALID_ARG;
     if (out != FP8HG_OUT_BF16 && out != FP8HG_OUT_FP32) return FP8HG_ERR_INVALID_ARG;
     if (accumulate != 0 && accumulate != 1) return FP8HG_ERR_INVALID_ARG;
-    int st = validate_operand(a);
+    fp8hg::GemmArgs g;
+    int st = prepare_gemm(op, a, b, g);
     if (st != FP8HG_OK) return st;
-    st = validate_operand(b);
-    if (st != FP8HG_OK) return st;
-    if (a->k != b->k) return FP8HG_ERR_SHAPE;
-    if (!gran_pair_ok(op, a->gran, b->gran)) return FP8HG_ERR_UNSUPPORTED;
     if (!c) return FP8HG_ERR_INVALID_ARG;
     if (!aligned(c, 16)) return FP8HG_ERR_ALIGNMENT;
     if (ldc < b->rows) return FP8HG_ERR_INVALID_ARG;
     if (ldc % (out == FP8HG_OUT_BF16 ? 8 : 4)) return FP8HG_ERR_ALIGNMENT;
     if (opts && (opts->inject_fault < 0 || opts->inject_fault > 1)) return FP8HG_ERR_INVALID_ARG;
-
-    unsigned int *err = fp8hg::device_error_word();
-    if (!err) return FP8HG_ERR_CUDA;
-    fp8hg::GemmArgs g;
-    g.a_codes = a->codes;
-    g.b_codes = b->codes;
-    g.a_scale = a->scale;
-    g.b_scale = b->scale;
-    g.M = a->rows;
-    g.N = b->rows;
-    g.K = a->k;
-    g.lda = a->ld;
-    g.ldb = b->ld;
-    g.ld_sa = a->ld_scale;
-    g.ld_sb = b->ld_scale;
-    g.fmt_a = a->fmt;
-    g.fmt_b = b->fmt;
-    g.gran_a = a->gran;
-    g.gran_b = b->gran;
     g.c = c;
     g.ldc = ldc;
     g.out_fp32 = out == FP8HG_OUT_FP32;
     g.accumulate = accumulate;
-    g.wait_limit_ns = (opts && opts->wait_limit_ns) ? opts->wait_limit_ns : kDefaultWaitNs;
-    g.inject_fault = opts ? opts->inject_fault : 0;
-    g.err = err;
-    const int rc = fp8hg::launch_gemm_scaled(g, static_cast<cudaStream_t>(stream));
-    if (rc == 1) return FP8HG_ERR_UNSUPPORTED;  // tensor map could not be encoded
-    return rc == 0 ? FP8HG_OK : FP8HG_ERR_CUDA;
+    return run_gemm(g, opts, stream);
+}
+
+int fp8_gemm_scaled_q(int op, const fp8hg_operand *a, const fp8hg_operand *b, uint8_t *c_codes,
+                      int64_t ld_c, uint8_t *c_scale, int64_t ld_cs, int fmt_c, void *stream) {
+    if (!valid_fmt(fmt_c)) return FP8HG_ERR_INVALID_ARG;
+    fp8hg::GemmArgs g;
+    int st = prepare_gemm(op, a, b, g);
+    if (st != FP8HG_OK) return st;
+    if (!c_codes || !c_scale) return FP8HG_ERR_INVALID_ARG;
+    if (!aligned(c_codes, 16) || ld_c % 16) return FP8HG_ERR_ALIGNMENT;
+    if (ld_c < b->rows || ld_cs < b->rows / 128) return FP8HG_ERR_INVALID_ARG;
+    g.c = c_codes;
+    g.ldc = ld_c;
+    g.out_q = 1;
+    g.fmt_c = fmt_c;
+    g.c_scale = c_scale;
+    g.ld_cs = ld_cs;
+    return run_gemm(g, nullptr, stream);
 }
 
 int fp8_gemm_scaled(int op, const fp8hg_operand *a, const fp8hg_operand *b, void *c, int64_t ldc,

@@ -44,6 +44,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "quant_math.cuh"
 
 namespace fp8hg {
 
@@ -79,6 +80,9 @@ struct KParams {
     int M, N, nk, num_mb, num_nb, num_tiles;
     int gran_a, gran_b;
     int out_fp32, accumulate, inject;
+    int out_q, fmt_c;
+    uint8_t *cs;
+    int64_t ld_cs;
     const uint8_t *sa, *sb;
     int64_t ld_sa, ld_sb;
     void *c;
@@ -230,7 +234,8 @@ __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // G: k-blocks per scale group (16, or 4 when the operands are MX32).
-template <int G>
+// OUTQ: the epilogue quantizes C (FP8, 1x128 along N) instead of storing it.
+template <int G, bool OUTQ>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_mxf8(const __grid_constant__ CUtensorMap tmap_a,
                 const __grid_constant__ CUtensorMap tmap_b, const KParams p) {
@@ -396,7 +401,64 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::tc_fence_after();
             const int64_t row = static_cast<int64_t>(mb) * BM + q * 32 + lane;
             const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + ACC_COL;
-            if (!p.out_fp32 && !p.accumulate) {
+            if constexpr (OUTQ) {
+                // FP8 out, one UE8M0 round-up scale per 128 columns of the row
+                // (the next GEMM's 1x128 operand).  Pass 1 takes each group's
+                // NaN-propagating amax (integer max of |value| patterns) from
+                // tensor memory; pass 2 reads the accumulator again and casts.
+                uint32_t am[BN / 128] = {};
+#pragma unroll
+                for (int chunk = 0; chunk < BN / 32; ++chunk) {
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32(taddr + chunk * 32, r);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) am[chunk / 4] = max(am[chunk / 4], r[e] & 0x7FFFFFFFu);
+                }
+                float mul[BN / 128];
+                uint32_t sbyte[BN / 128];
+#pragma unroll
+                for (int g = 0; g < BN / 128; ++g) {
+                    const bool nonfinite = am[g] >= 0x7F800000u;
+                    const int e = nonfinite ? 128
+                                  : (p.fmt_c == 0 ? ue8m0_exponent_f32<FMT_E4M3>(am[g])
+                                                  : ue8m0_exponent_f32<FMT_E5M2>(am[g]));
+                    mul[g] = nonfinite ? 0.0f : pow2f(-e);
+                    sbyte[g] = static_cast<uint32_t>(e + 127);
+                }
+                uint32_t codes[BN / 4];
+#pragma unroll
+                for (int chunk = 0; chunk < BN / 32; ++chunk) {
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32(taddr + chunk * 32, r);
+                    ptx::tmem_wait_ld();
+                    const float m = mul[chunk / 4];
+                    const bool nan_group = sbyte[chunk / 4] == 0xFFu;
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        const float f0 = __uint_as_float(r[4 * v]) * m, f1 = __uint_as_float(r[4 * v + 1]) * m;
+                        const float f2 = __uint_as_float(r[4 * v + 2]) * m, f3 = __uint_as_float(r[4 * v + 3]) * m;
+                        const uint32_t lo = p.fmt_c == 0 ? ptx::cvt_e4m3x2(f0, f1) : ptx::cvt_e5m2x2(f0, f1);
+                        const uint32_t hi = p.fmt_c == 0 ? ptx::cvt_e4m3x2(f2, f3) : ptx::cvt_e5m2x2(f2, f3);
+                        codes[chunk * 8 + v] = nan_group ? kNanCodes : (lo | (hi << 16));
+                    }
+                }
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(tempty);
+#pragma unroll
+                for (int g = 0; g < BN / 128; ++g) {
+                    const int64_t n0 = static_cast<int64_t>(nb) * BN + g * 128;
+                    if (n0 >= p.N) continue;
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.c) + row * p.ldc + n0);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        dst[v] = make_uint4(codes[32 * g + 4 * v], codes[32 * g + 4 * v + 1],
+                                            codes[32 * g + 4 * v + 2], codes[32 * g + 4 * v + 3]);
+                    p.cs[row * p.ld_cs + n0 / 128] = static_cast<uint8_t>(sbyte[g]);
+                }
+                ++tcount;
+                continue;
+            } else if (!p.out_fp32 && !p.accumulate) {
                 // BF16 out: pull the whole accumulator row into registers
                 // (packed BF16), release the accumulator to the next tile's
                 // MMAs, then store while they run.
@@ -538,13 +600,12 @@ int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
     {
         std::lock_guard<std::mutex> lock(g_mu);
         if (!g_attr_set[dev]) {
-            cudaError_t e = cudaFuncSetAttribute(k_gemm_mxf8<16>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(SMEM_BYTES));
-            if (e != cudaSuccess) return 2 + static_cast<int>(e);
-            e = cudaFuncSetAttribute(k_gemm_mxf8<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(SMEM_BYTES));
-            if (e != cudaSuccess) return 2 + static_cast<int>(e);
+            for (auto kern : {k_gemm_mxf8<16, false>, k_gemm_mxf8<4, false>, k_gemm_mxf8<16, true>,
+                              k_gemm_mxf8<4, true>}) {
+                const cudaError_t e = cudaFuncSetAttribute(
+                    kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_BYTES));
+                if (e != cudaSuccess) return 2 + static_cast<int>(e);
+            }
             int n = 0;
             cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
             g_sms[dev] = n > 0 ? n : 1;
@@ -563,6 +624,10 @@ int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
     p.gran_b = g.gran_b;
     p.out_fp32 = g.out_fp32;
     p.accumulate = g.accumulate;
+    p.out_q = g.out_q;
+    p.fmt_c = g.fmt_c;
+    p.cs = g.c_scale;
+    p.ld_cs = g.ld_cs;
     p.inject = g.inject_fault;
     p.sa = g.a_scale;
     p.sb = g.b_scale;
@@ -582,8 +647,14 @@ int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
 
     int grid = g_sms[dev];
     if (grid > p.num_tiles) grid = p.num_tiles;
-    if (g.gran_a == GRAN_MX32) k_gemm_mxf8<4><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
-    else k_gemm_mxf8<16><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+    const bool mx = g.gran_a == GRAN_MX32;
+    if (g.out_q) {
+        if (mx) k_gemm_mxf8<4, true><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+        else k_gemm_mxf8<16, true><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+    } else {
+        if (mx) k_gemm_mxf8<4, false><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+        else k_gemm_mxf8<16, false><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+    }
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? 0 : 2 + static_cast<int>(e);
 }

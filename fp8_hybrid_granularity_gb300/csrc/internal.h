@@ -49,6 +49,9 @@ struct GemmArgs {
     void *c;
     int64_t ldc;
     int out_fp32, accumulate;
+    int out_q, fmt_c;        // out_q: C quantized in the epilogue (1x128 along N)
+    uint8_t *c_scale;        // out_q: scale bytes [M, N/128]
+    int64_t ld_cs;
     uint64_t wait_limit_ns;
     int inject_fault;
     unsigned int *err;  // device error word

@@ -11,6 +11,8 @@ kernel, and prints the mean launch time from CUDA events.  Cases:
              [3584, 18944] 128x128 blocks, BF16 out
   gemm_gate  fprop gate projection: A = X [M, 3584] per token, B = W_gate
              [18944, 3584] 128x128 blocks, BF16 out
+  gemm_gate_q  the same with the output quantized in the epilogue (E4M3,
+             1x128 along N)
   wgrad      gate weight gradient: A = dY^T [18944, M] 1x128 E5M2, B = X^T
              [3584, M] 1x128 E4M3, FP32 out
   quant_row  per-token quantization of H [M, 18944]
@@ -37,7 +39,7 @@ HID, MLP = 3584, 18944
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["gemm", "gemm_gate", "wgrad", "quant_row", "quant_1x128", "quant_t", "block128",
+    ap.add_argument("case", choices=["gemm", "gemm_gate", "gemm_gate_q", "wgrad", "quant_row", "quant_1x128", "quant_t", "block128",
                                      "mx32", "mx32_mon", "requant"])
     ap.add_argument("--m", type=int, default=4096)
     ap.add_argument("--warmup", type=int, default=2)
@@ -56,13 +58,17 @@ def main():
         out = torch.empty((M, HID), dtype=torch.bfloat16, device=dev)
         fn = lambda: fp8hg.fp8_gemm_scaled(fp8hg.FPROP, a, b, out=out)
         work, unit = 2.0 * M * HID * MLP, "flop"
-    elif args.case == "gemm_gate":
+    elif args.case in ("gemm_gate", "gemm_gate_q"):
         x = mk("act", M, HID, "X")
         w = mk("weight", MLP, HID, "W_gate")
         a = fp8hg.fp8_quant_token(x, 0, E4)
         b = fp8hg.fp8_quant_block128(w, E4)
-        out = torch.empty((M, MLP), dtype=torch.bfloat16, device=dev)
-        fn = lambda: fp8hg.fp8_gemm_scaled(fp8hg.FPROP, a, b, out=out)
+        if args.case == "gemm_gate_q":
+            out = fp8hg.alloc_token(M, MLP, 128, E4, False, dev)
+            fn = lambda: fp8hg.fp8_gemm_scaled_q(fp8hg.FPROP, a, b, E4, out=out)
+        else:
+            out = torch.empty((M, MLP), dtype=torch.bfloat16, device=dev)
+            fn = lambda: fp8hg.fp8_gemm_scaled(fp8hg.FPROP, a, b, out=out)
         work, unit = 2.0 * M * HID * MLP, "flop"
     elif args.case == "wgrad":
         dy = mk("grad", M, MLP, "dY_gate")

@@ -282,6 +282,31 @@ int fp8_gemm_scaled(int op, const fp8hg_operand *a, const fp8hg_operand *b, void
                     int64_t ldc, int out, int accumulate, void *stream);
 
 /*
+ * fp8_gemm_scaled_q — the scaled GEMM with its output quantized in the
+ * epilogue: C = A * B^T (FP32 in tensor memory) leaves the kernel as FP8
+ * codes with one UE8M0 round-up scale per 128 consecutive columns of a row,
+ * i.e. directly as the 1x128 A operand of a following GEMM; no BF16 copy of
+ * C is written and no separate quantization pass reads it back.
+ *
+ * Passage: "A Comprehensive FP8 Training Recipe ...", "What carries the
+ * argument" (activations quantized per token / per 1x128 tile with
+ * power-of-two scales rounded up so the FP8 range is never exceeded); the
+ * fusion into the producing GEMM is this library's design.  The rounding
+ * decisions are taken on the FP32 accumulator: amax over the group, e the
+ * smallest integer with amax <= FMAX * 2^e (clamped to [-127, 127]),
+ * code = RNE(C * 2^-e) in fmt_c; a group holding a NaN or an infinity gets
+ * scale byte 0xFF and codes 0x7F.
+ *
+ *   a, b     as fp8_gemm_scaled (same op / granularity rules)
+ *   c_codes  [M, N] codes (ld_c bytes, ld_c % 16 == 0, 16-byte aligned)
+ *   c_scale  [M, N/128] scale bytes (ld_cs >= N/128; a multiple of four
+ *            keeps it usable as a GEMM operand)
+ *   fmt_c    FP8HG_E4M3 or FP8HG_E5M2
+ */
+int fp8_gemm_scaled_q(int op, const fp8hg_operand *a, const fp8hg_operand *b, uint8_t *c_codes,
+                      int64_t ld_c, uint8_t *c_scale, int64_t ld_cs, int fmt_c, void *stream);
+
+/*
  * Options for fp8_gemm_scaled_ex.
  *   wait_limit_ns  upper bound on any single pipeline wait inside the GEMM
  *                  kernel (0 = the default, 2 s).  When a wait runs out the

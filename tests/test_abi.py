@@ -9,7 +9,7 @@ import fp8_hybrid_granularity_gb300 as fp8hg
 from fp8_hybrid_granularity_gb300 import Operand, E4M3, GRAN_ROW, GRAN_1x128, GRAN_128x128, GRAN_MX32
 
 EXPECTED = {"fp8_quant_token", "fp8_quant_block128", "fp8_quant_mx32", "fp8_quant_mx32_monitor",
-            "fp8_requant_t",
+            "fp8_requant_t", "fp8_gemm_scaled_q",
             "fp8_gemm_scaled",
             "fp8_gemm_scaled_ex", "fp8hg_get_device_error", "fp8hg_status_str", "fp8hg_version"}
 
@@ -93,6 +93,27 @@ def test_requant_validation(lib):
 
 def _op(rows=256, k=256, gran=GRAN_1x128, ld=None, lds=4, fmt=E4M3, scale=FAKE):
     return Operand(FAKE, scale, rows, k, ld if ld is not None else k, lds, fmt, gran)
+
+
+def test_gemm_q_validation(lib):
+    g = lib.fp8_gemm_scaled_q
+    blk = dict(gran=GRAN_128x128, lds=4)
+
+    def call(a=None, b=None, c=FAKE, ldc=256, cs=FAKE, ldcs=4, fmt=E4M3, op=0):
+        a = a or _op()
+        b = b or _op(**blk)
+        return g(op, ctypes.byref(a), ctypes.byref(b), c, ldc, cs, ldcs, fmt, None)
+
+    assert call(fmt=3) == INVALID
+    assert call(c=None) == INVALID
+    assert call(cs=None) == INVALID
+    assert call(c=FAKE + 8) == ALIGN
+    assert call(ldc=264) == ALIGN
+    assert call(ldc=128) == INVALID                 # ldc < N
+    assert call(ldcs=1) == INVALID                  # N/128 = 2 scale columns
+    assert call(b=_op(gran=GRAN_1x128)) == UNSUP    # fprop needs block B
+    assert call(a=_op(rows=200)) == SHAPE
+    assert call(op=7) == INVALID
 
 
 def test_gemm_validation(lib):
