@@ -38,7 +38,7 @@ def build(force: bool = False) -> str:
                  or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
         if force or stale:
             tmp = _LIB_PATH + f".tmp{os.getpid()}"
-            subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared",
+            subprocess.check_call(["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-fPIC", "-shared",
                                    "-fno-fast-math", "-o", tmp, _SRC, "-lm"])
             os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -74,6 +74,12 @@ def _load():
         lib.orc_mx32_monitor.argtypes = [P, I64, I64, I64, I, P, I64, P, I64, P, P]
         lib.orc_requant_t.restype = I
         lib.orc_requant_t.argtypes = [P, I64, I64, I64, P, I64, I, I, I, P, I64, P, I64]
+        lib.orc_quant_token_f32s.restype = I
+        lib.orc_quant_token_f32s.argtypes = [P, I64, I64, I64, I, I, P, I64, P, I64]
+        lib.orc_quant_block128_f32s.restype = I
+        lib.orc_quant_block128_f32s.argtypes = [P, I64, I64, I64, I, P, I64, P, I64, P, I64, P, I64]
+        lib.orc_dequant_f32s.restype = I
+        lib.orc_dequant_f32s.argtypes = [P, I64, P, I64, I, I, I64, I64, P]
         lib.orc_dequant.restype = I
         lib.orc_dequant.argtypes = [P, I64, P, I64, I, I, I64, I64, P]
         lib.orc_gemm_ref_pairs.restype = I
@@ -211,6 +217,47 @@ def dequant(q, scale, gran: int, fmt: int) -> np.ndarray:
     out = np.empty((rows, k), np.float64)
     _load().orc_dequant(_ptr(q), k, _ptr(scale), scale.shape[1], int(gran), int(fmt),
                         rows, k, _ptr(out))
+    return out
+
+
+def quant_token_f32s(x, group: int, fmt: int):
+    """FP32-scale variant: (q [rows, cols], scale float32 [rows, ngroups])."""
+    x = _u16(x)
+    rows, cols = x.shape
+    ng = 1 if group == 0 else cols // 128
+    q = np.empty((rows, cols), np.uint8)
+    s = np.empty((rows, ng), np.float32)
+    rc = _load().orc_quant_token_f32s(_ptr(x), rows, cols, cols, int(group), int(fmt), _ptr(q),
+                                      cols, _ptr(s), ng)
+    _check(rc, "quant_token_f32s")
+    return q, s
+
+
+def quant_block128_f32s(x, fmt: int, transposed_copy: bool = False):
+    """FP32-scale variant: (q, scale float32 [rows/128, cols/128], q_t, scale_t)."""
+    x = _u16(x)
+    rows, cols = x.shape
+    q = np.empty((rows, cols), np.uint8)
+    s = np.empty((rows // 128, cols // 128), np.float32)
+    qt = st = None
+    if transposed_copy:
+        qt = np.empty((cols, rows), np.uint8)
+        st = np.empty((cols // 128, rows // 128), np.float32)
+    rc = _load().orc_quant_block128_f32s(_ptr(x), rows, cols, cols, int(fmt), _ptr(q), cols,
+                                         _ptr(s), s.shape[1], _ptr(qt), rows, _ptr(st),
+                                         rows // 128)
+    _check(rc, "quant_block128_f32s")
+    return q, s, qt, st
+
+
+def dequant_f32s(q, scale, gran: int, fmt: int) -> np.ndarray:
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    scale = np.ascontiguousarray(scale, dtype=np.float32)
+    rows, k = q.shape
+    out = np.empty((rows, k), np.float64)
+    rc = _load().orc_dequant_f32s(_ptr(q), k, _ptr(scale), scale.shape[1], int(gran), int(fmt),
+                                  rows, k, _ptr(out))
+    _check(rc, "dequant_f32s")
     return out
 
 

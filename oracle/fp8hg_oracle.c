@@ -6,8 +6,9 @@
  * CPU-baseline / reference arm do.  It shares no code, header, table or
  * constant generator with the CUDA library.
  *
- * Everything is plain C99 in double precision, written to be checked by eye
- * against the definitions it follows:
+ * Everything is plain C99 in double precision (except the FP32-scale variant,
+ * whose steps are single-precision operations by definition), written to be
+ * checked by eye against the definitions it follows:
  *
  *  - "FP8 Formats for Deep Learning", abstract and core claim: the two FP8
  *    encodings E4M3 (4 exponent bits, 3 mantissa bits, no infinities, a single
@@ -349,6 +350,109 @@ int orc_mx32_monitor(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x
         }
         if (row_sat) row_sat[r] = rs;
     }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* FP32-scale variant                                                        */
+/* ------------------------------------------------------------------------ */
+
+/* "A Comprehensive FP8 Training Recipe ..." compares its UE8M0 recipe with
+ * an "FP8 w. FP32 scale" arm that its setup does not define (referee
+ * comments).  The reading taken here is the ordinary FP32 scaling of FP8
+ * recipes, at the same granularities: per group,
+ *   d = fl32(amax / FMAX)      the stored FP32 scale (x ~ decode(q) * d)
+ *   m = fl32(FMAX / amax)      the multiplier applied before the cast
+ *   q = RNE_sat(fl32(x * m))   saturating nearest-even FP8 encoding
+ * with amax = 0 giving d = m = 1, and a NaN or infinity in the group giving
+ * d = NaN and codes 0x7F.  Every step is one IEEE single-precision operation
+ * (the oracle is built with contraction off), so the CUDA path reaches the
+ * same bits. */
+static float orc_quant_group_f32(const uint16_t *x, ptrdiff_t stride, int n, int fmt,
+                                 uint8_t *q, ptrdiff_t qstride)
+{
+    double amax = 0.0;
+    int nonfinite = 0;
+    for (int i = 0; i < n; i++) {
+        double v = orc_bf16_to_double(x[i * stride]);
+        if (!isfinite(v)) nonfinite = 1;
+        else if (fabs(v) > amax) amax = fabs(v);
+    }
+    if (nonfinite) {
+        for (int i = 0; i < n; i++) q[i * qstride] = 0x7F;
+        return NAN;
+    }
+    const float fmax = (float)orc_fp8_max(fmt);
+    const float a = (float)amax;                 /* exact: BF16 values are FP32 values */
+    const float d = (a == 0.0f) ? 1.0f : a / fmax;
+    const float m = (a == 0.0f) ? 1.0f : fmax / a;
+    for (int i = 0; i < n; i++) {
+        const float xf = (float)orc_bf16_to_double(x[i * stride]);
+        const float y = xf * m;
+        q[i * qstride] = orc_fp8_encode((double)y, fmt, 1);
+    }
+    return d;
+}
+
+/* Per-token (group 0) or 1x128 (group 128) quantization with FP32 scales:
+ * q [rows, cols] (ld_q), scale [rows, ngroups] floats (ld_s floats). */
+int orc_quant_token_f32s(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int group,
+                         int fmt, uint8_t *q, int64_t ld_q, float *scale, int64_t ld_s)
+{
+    if (rows < 0 || cols < 0 || (group != 0 && group != 128)) return -1;
+    int64_t g = group ? group : cols;
+    if (g == 0 || cols % g) return -1;
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t c0 = 0; c0 < cols; c0 += g)
+            scale[r * ld_s + c0 / g] = orc_quant_group_f32(x + r * ld_x + c0, 1, (int)g, fmt,
+                                                           q + r * ld_q + c0, 1);
+    return 0;
+}
+
+/* 128x128-block quantization with FP32 scales (block amax over the whole
+ * block); optional transposed copy of the codes and the scale grid. */
+int orc_quant_block128_f32s(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
+                            uint8_t *q, int64_t ld_q, float *scale, int64_t ld_s,
+                            uint8_t *q_t, int64_t ld_qt, float *scale_t, int64_t ld_st)
+{
+    if (rows % 128 || cols % 128) return -1;
+    uint8_t blk[128 * 128];
+    uint16_t tmp[128 * 128];
+    for (int64_t rb = 0; rb < rows / 128; rb++) {
+        for (int64_t cb = 0; cb < cols / 128; cb++) {
+            /* the block as one group of 16384 elements, row-major */
+            for (int r = 0; r < 128; r++)
+                for (int c = 0; c < 128; c++)
+                    tmp[r * 128 + c] = x[(rb * 128 + r) * ld_x + cb * 128 + c];
+            float d = orc_quant_group_f32(tmp, 1, 128 * 128, fmt, blk, 1);
+            scale[rb * ld_s + cb] = d;
+            for (int r = 0; r < 128; r++)
+                for (int c = 0; c < 128; c++) {
+                    q[(rb * 128 + r) * ld_q + cb * 128 + c] = blk[r * 128 + c];
+                    if (q_t) q_t[(cb * 128 + c) * ld_qt + rb * 128 + r] = blk[r * 128 + c];
+                }
+            if (scale_t) scale_t[cb * ld_st + rb] = d;
+        }
+    }
+    return 0;
+}
+
+/* x_hat = decode(q) * d for an operand with FP32 scales (ROW, 1x128 or
+ * 128x128 layout as in orc_dequant); out [rows, k] dense. */
+int orc_dequant_f32s(const uint8_t *q, int64_t ld_q, const float *scale, int64_t ld_s, int gran,
+                     int fmt, int64_t rows, int64_t k, double *out)
+{
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t c = 0; c < k; c++) {
+            float d;
+            switch (gran) {
+            case ORC_GRAN_ROW: d = scale[r * ld_s]; break;
+            case ORC_GRAN_1x128: d = scale[r * ld_s + c / 128]; break;
+            case ORC_GRAN_128x128: d = scale[(r / 128) * ld_s + c / 128]; break;
+            default: return -1;
+            }
+            out[r * k + c] = orc_fp8_decode(q[r * ld_q + c], fmt) * (double)d;
+        }
     return 0;
 }
 

@@ -46,7 +46,7 @@ def load_quant_examples(name: str = "quant_examples.txt"):
                 cur[key] = np.array(_hex_list(val), np.uint16)
             elif key in ("q", "q_in", "s_in", "q_out", "s_out"):
                 cur[key] = np.array(_hex_list(val), np.uint8)
-            elif key == "scale":
+            elif key in ("scale", "scale_f32"):
                 cur[key] = int(val, 16)
             elif key in ("clamped", "rows", "saturated", "top_code", "blocks_saturated",
                          "blocks_collapsed"):
