@@ -15,6 +15,8 @@ Tensor-level API (same names as the C entry points):
   fp8_requant_t(src QTensor, fmt)                       -> QTensor (transposed)
   fp8_gemm_scaled(op, a, b, out=None, out_dtype=bf16, accumulate=False)
   fp8_gemm_scaled_q(op, a, b, fmt)                      -> QTensor (1x128 along N)
+  fp8_quant_token_f32s / fp8_quant_block128_f32s / fp8_gemm_scaled_f32s
+                                                        the FP32-scale variant
   fp8hg_get_device_error(stream=None)
 
 Scale arrays are allocated with their column count rounded up to a multiple
@@ -91,6 +93,12 @@ def load_library(build_if_stale: bool = True):
         lib.fp8_requant_t.argtypes = [P, I64, I64, I64, P, I64, I, I, I, P, I64, P, I64, P]
         lib.fp8_gemm_scaled_q.argtypes = [I, ctypes.POINTER(Operand), ctypes.POINTER(Operand), P,
                                           I64, P, I64, I, P]
+        lib.fp8_quant_token_f32s.argtypes = [P, I64, I64, I64, I, I, P, I64, P, I64, P]
+        lib.fp8_quant_block128_f32s.argtypes = [P, I64, I64, I64, I, P, I64, P, I64, P, I64, P,
+                                                I64, P]
+        # fp8hg_operand_f32s has the layout of fp8hg_operand (float scale pointer)
+        lib.fp8_gemm_scaled_f32s.argtypes = [I, ctypes.POINTER(Operand), ctypes.POINTER(Operand),
+                                             P, I64, I, P]
         lib.fp8_gemm_scaled.argtypes = [I, ctypes.POINTER(Operand), ctypes.POINTER(Operand), P,
                                         I64, I, I, P]
         lib.fp8_gemm_scaled_ex.argtypes = [I, ctypes.POINTER(Operand), ctypes.POINTER(Operand), P,
@@ -293,6 +301,70 @@ def fp8_quant_mx32_monitor(x, fmt: int = E4M3, stats=None, row_saturated=None, o
                                       _ptr(stats), _ptr(row_saturated), _stream(stream))
     _check(rc, "fp8_quant_mx32_monitor")
     return out, stats
+
+
+# --- FP32-scale variant ("FP8 w. FP32 scale") -------------------------------
+# QTensors of this variant hold float32 scales ([rows, 1], [rows, cols/128]
+# or [rows/128, cols/128]); the GEMM takes them through fp8_gemm_scaled_f32s.
+
+def fp8_quant_token_f32s(x, group: int = 0, fmt: int = E4M3, out: Optional[QTensor] = None,
+                         stream=None) -> QTensor:
+    import torch
+    _check_bf16(x)
+    rows, cols = x.shape
+    if out is None:
+        q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+        ng = 1 if group == 0 else cols // 128
+        out = QTensor(q, torch.empty((rows, ng), dtype=torch.float32, device=x.device), fmt,
+                      GRAN_ROW if group == 0 else GRAN_1x128, ng)
+    rc = lib().fp8_quant_token_f32s(_ptr(x), rows, cols, x.stride(0), group, fmt, _ptr(out.codes),
+                                    out.codes.stride(0), _ptr(out.scale), out.scale.stride(0),
+                                    _stream(stream))
+    _check(rc, "fp8_quant_token_f32s")
+    return out
+
+
+def fp8_quant_block128_f32s(x, fmt: int = E4M3, transposed_copy: bool = False, stream=None):
+    import torch
+    _check_bf16(x)
+    rows, cols = x.shape
+    dev = x.device
+    out = QTensor(torch.empty((rows, cols), dtype=torch.uint8, device=dev),
+                  torch.empty((rows // 128, cols // 128), dtype=torch.float32, device=dev), fmt,
+                  GRAN_128x128, cols // 128)
+    out_t = None
+    if transposed_copy:
+        out_t = QTensor(torch.empty((cols, rows), dtype=torch.uint8, device=dev),
+                        torch.empty((cols // 128, rows // 128), dtype=torch.float32, device=dev),
+                        fmt, GRAN_128x128, rows // 128)
+    rc = lib().fp8_quant_block128_f32s(
+        _ptr(x), rows, cols, x.stride(0), fmt, _ptr(out.codes), out.codes.stride(0),
+        _ptr(out.scale), out.scale.stride(0), _ptr(out_t.codes) if out_t else None,
+        out_t.codes.stride(0) if out_t else 0, _ptr(out_t.scale) if out_t else None,
+        out_t.scale.stride(0) if out_t else 0, _stream(stream))
+    _check(rc, "fp8_quant_block128_f32s")
+    return (out, out_t) if transposed_copy else out
+
+
+def fp8_gemm_scaled_f32s(op: int, a: QTensor, b: QTensor, out=None, out_dtype=None, stream=None):
+    """C = A * B^T on FP8 operands with FP32 scales (promotion GEMM)."""
+    import torch
+    if out is None:
+        dt = out_dtype if out_dtype is not None else torch.bfloat16
+        out = torch.empty((a.codes.shape[0], b.codes.shape[0]), dtype=dt, device=a.codes.device)
+    if out.dtype == torch.bfloat16:
+        kind = OUT_BF16
+    elif out.dtype == torch.float32:
+        kind = OUT_FP32
+    else:
+        raise ValueError("out must be bfloat16 or float32")
+    if a.scale.dtype != torch.float32 or b.scale.dtype != torch.float32:
+        raise ValueError("operands must carry float32 scales")
+    oa, ob = a.operand(), b.operand()
+    rc = lib().fp8_gemm_scaled_f32s(op, ctypes.byref(oa), ctypes.byref(ob), _ptr(out),
+                                    out.stride(0), kind, _stream(stream))
+    _check(rc, "fp8_gemm_scaled_f32s")
+    return out
 
 
 def fp8_gemm_scaled_q(op: int, a: QTensor, b: QTensor, fmt: int = E4M3,

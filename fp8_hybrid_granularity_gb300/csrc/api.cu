@@ -251,6 +251,97 @@ int fp8_gemm_scaled(int op, const fp8hg_operand *a, const fp8hg_operand *b, void
     return fp8_gemm_scaled_ex(op, a, b, c, ldc, out, accumulate, nullptr, stream);
 }
 
+int fp8_quant_token_f32s(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int group,
+                         int fmt, uint8_t *q, int64_t ld_q, float *scale, int64_t ld_s,
+                         void *stream) {
+    int st = check_quant_common(x, rows, cols, ld_x, fmt, q, ld_q,
+                                reinterpret_cast<const uint8_t *>(scale));
+    if (st != FP8HG_OK) return st;
+    if (group != 0 && group != 128) return FP8HG_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return FP8HG_OK;
+    if (!aligned(scale, 4)) return FP8HG_ERR_ALIGNMENT;
+    if (cols % 128) return FP8HG_ERR_SHAPE;
+    if (ld_x < cols || ld_q < cols) return FP8HG_ERR_INVALID_ARG;
+    if (ld_s < (group ? cols / 128 : 1)) return FP8HG_ERR_INVALID_ARG;
+    if (group == 0 && rows > 2147483647LL) return FP8HG_ERR_SHAPE;
+    return status_from_cuda(fp8hg::launch_quant_token_f32s(x, rows, cols, ld_x, group, fmt, q, ld_q,
+                                                           scale, ld_s,
+                                                           static_cast<cudaStream_t>(stream)));
+}
+
+int fp8_quant_block128_f32s(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
+                            uint8_t *q, int64_t ld_q, float *scale, int64_t ld_s, uint8_t *q_t,
+                            int64_t ld_qt, float *scale_t, int64_t ld_st, void *stream) {
+    int st = check_quant_common(x, rows, cols, ld_x, fmt, q, ld_q,
+                                reinterpret_cast<const uint8_t *>(scale));
+    if (st != FP8HG_OK) return st;
+    if (rows == 0 || cols == 0) return FP8HG_OK;
+    if ((q_t == nullptr) != (scale_t == nullptr)) return FP8HG_ERR_INVALID_ARG;
+    if (!aligned(scale, 4) || (scale_t && !aligned(scale_t, 4))) return FP8HG_ERR_ALIGNMENT;
+    if (rows % 128 || cols % 128) return FP8HG_ERR_SHAPE;
+    if (rows / 128 > 65535) return FP8HG_ERR_SHAPE;
+    if (ld_x < cols || ld_q < cols || ld_s < cols / 128) return FP8HG_ERR_INVALID_ARG;
+    if (q_t) {
+        if (!aligned(q_t, 16) || ld_qt % 16) return FP8HG_ERR_ALIGNMENT;
+        if (ld_qt < rows || ld_st < rows / 128) return FP8HG_ERR_INVALID_ARG;
+    }
+    return status_from_cuda(fp8hg::launch_quant_block128_f32s(x, rows, cols, ld_x, fmt, q, ld_q,
+                                                              scale, ld_s, q_t, ld_qt, scale_t,
+                                                              ld_st,
+                                                              static_cast<cudaStream_t>(stream)));
+}
+
+int fp8_gemm_scaled_f32s(int op, const fp8hg_operand_f32s *a, const fp8hg_operand_f32s *b, void *c,
+                         int64_t ldc, int out, void *stream) {
+    if (op < FP8HG_FPROP || op > FP8HG_WGRAD) return FP8HG_ERR_INVALID_ARG;
+    if (out != FP8HG_OUT_BF16 && out != FP8HG_OUT_FP32) return FP8HG_ERR_INVALID_ARG;
+    if (!a || !b) return FP8HG_ERR_INVALID_ARG;
+    for (const fp8hg_operand_f32s *o : {a, b}) {
+        if (!valid_fmt(o->fmt)) return FP8HG_ERR_INVALID_ARG;
+        if (o->rows <= 0 || o->k <= 0 || o->rows % 128 || o->k % 128) return FP8HG_ERR_SHAPE;
+        if (o->rows > 2147483647LL || o->k > 2147483647LL) return FP8HG_ERR_SHAPE;
+        if (!o->codes || !o->scale) return FP8HG_ERR_INVALID_ARG;
+        if (!aligned(o->codes, 16) || o->ld % 16 || !aligned(o->scale, 4))
+            return FP8HG_ERR_ALIGNMENT;
+        if (o->ld < o->k) return FP8HG_ERR_INVALID_ARG;
+    }
+    if (a->k != b->k) return FP8HG_ERR_SHAPE;
+    if (op == FP8HG_WGRAD) return FP8HG_ERR_UNSUPPORTED;
+    if ((a->gran != FP8HG_GRAN_ROW && a->gran != FP8HG_GRAN_1x128) || b->gran != FP8HG_GRAN_128x128)
+        return FP8HG_ERR_UNSUPPORTED;
+    if (a->ld_scale < (a->gran == FP8HG_GRAN_ROW ? 1 : a->k / 128)) return FP8HG_ERR_INVALID_ARG;
+    if (b->ld_scale < b->k / 128) return FP8HG_ERR_INVALID_ARG;
+    if (!c) return FP8HG_ERR_INVALID_ARG;
+    if (!aligned(c, 16)) return FP8HG_ERR_ALIGNMENT;
+    if (ldc < b->rows) return FP8HG_ERR_INVALID_ARG;
+    if (ldc % (out == FP8HG_OUT_BF16 ? 8 : 4)) return FP8HG_ERR_ALIGNMENT;
+    unsigned int *err = fp8hg::device_error_word();
+    if (!err) return FP8HG_ERR_CUDA;
+    fp8hg::GemmF32sArgs g{};
+    g.a_codes = a->codes;
+    g.b_codes = b->codes;
+    g.a_scale = a->scale;
+    g.b_scale = b->scale;
+    g.M = a->rows;
+    g.N = b->rows;
+    g.K = a->k;
+    g.lda = a->ld;
+    g.ldb = b->ld;
+    g.ld_sa = a->ld_scale;
+    g.ld_sb = b->ld_scale;
+    g.fmt_a = a->fmt;
+    g.fmt_b = b->fmt;
+    g.a_per_token = a->gran == FP8HG_GRAN_ROW;
+    g.c = c;
+    g.ldc = ldc;
+    g.out_fp32 = out == FP8HG_OUT_FP32;
+    g.wait_limit_ns = kDefaultWaitNs;
+    g.err = err;
+    const int rc = fp8hg::launch_gemm_f32s(g, static_cast<cudaStream_t>(stream));
+    if (rc == 1) return FP8HG_ERR_UNSUPPORTED;
+    return rc == 0 ? FP8HG_OK : FP8HG_ERR_CUDA;
+}
+
 int fp8hg_get_device_error(void *stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8HG_ERR_CUDA;
     unsigned int *err = fp8hg::device_error_word();

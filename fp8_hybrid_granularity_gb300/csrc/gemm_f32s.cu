@@ -1,0 +1,327 @@
+// FP8 GEMM with FP32 scale factors: the "FP8 w. FP32 scale" arm of "A
+// Comprehensive FP8 Training Recipe for Reasoning-Enhanced Language Models"
+// (its ablation table; the setup leaves the arm undefined, and it is read as
+// ordinary FP32 scaling at the recipe's granularities).
+//
+//   C[M, N] = sum over 128-K blocks kb of  sa(i, kb) * sb(j / 128, kb) * P_kb[i, j],
+//   P_kb = A[:, kb] * B[:, kb]^T on the raw FP8 codes.
+//
+// The tensor core's block scaling only takes power-of-two (UE8M0) factors, so
+// the FP32 factors are applied on the CUDA cores ("promotion"): the MMA
+// writes each 128-K block's partial product P_kb into one of four
+// tensor-memory buffers, and the epilogue warps fold it into FP32
+// accumulators held in registers, acc += (sa * sb) * P_kb, while the MMA
+// fills the others.
+//
+// Tile 128 x 128 x 128, 6-stage TMA pipeline, four partial-product buffers
+// (the MMA runs up to three 128-K blocks ahead of the epilogue), one
+// persistent CTA per SM,
+// 384 threads: warp 0 TMA producer, warp 1 MMA issuer and tensor-memory
+// owner, warps 4-11 epilogue (two warps per 32-lane quarter of tensor
+// memory, 64 columns each).  A: per-token or 1x128 scales; B: 128x128 blocks
+// (fprop and dgrad).  Every wait is bounded (globaltimer); on expiry the
+// kernel records a timeout, drains its copies and MMAs and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "gemm_common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8hg {
+namespace {
+
+using gemm_common::desc_sw128;
+using gemm_common::tile_coords;
+using gemm_common::wait_phase;
+
+constexpr int PM = 128, PN = 128, PK = 128, PSTAGES = 6;
+constexpr uint32_t PA_TILE = PM * PK, PB_TILE = PN * PK;
+constexpr int P_THREADS = 384;
+constexpr int PBUF = 4;                // partial-product buffers in tensor memory
+constexpr uint32_t P_TMEM_COLS = PBUF * PN;
+constexpr uint32_t POFF_A = 0;
+constexpr uint32_t POFF_B = POFF_A + PSTAGES * PA_TILE;
+constexpr uint32_t POFF_BAR = POFF_B + PSTAGES * PB_TILE;
+// barriers (8 bytes each): full[6], empty[6], pfull[4], pempty[4], drain
+constexpr uint32_t PBAR_FULL = 0, PBAR_EMPTY = 48, PBAR_PFULL = 96, PBAR_PEMPTY = 128,
+                   PBAR_DRAIN = 160;
+constexpr uint32_t POFF_TMEM_SLOT = POFF_BAR + 168;
+constexpr uint32_t POFF_ABORT = POFF_BAR + 172;
+constexpr uint32_t P_SMEM_BYTES = POFF_BAR + 192 + 1024;  // + slack for 1024-byte alignment
+constexpr int kEpiWarps = 8;
+constexpr int kScaleGroup = 8;  // k-blocks of scale factors fetched at a time
+
+enum { WHO_PRODUCER = 1, WHO_MMA = 2, WHO_EPILOGUE = 4 };
+
+struct PParams {
+    int M, N, nk, num_mb, num_nb, num_tiles;
+    int a_step;  // 0: one A scale per row, 1: one per (row, 128-K block)
+    const float *sa, *sb;
+    int64_t ld_sa, ld_sb;
+    void *c;
+    int64_t ldc;
+    int out_fp32;
+    uint32_t idesc;
+    uint64_t wait_limit_ns;
+    unsigned int *err;
+};
+
+__device__ __forceinline__ float ld_f32_now(const float *p) {
+    float v;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+__global__ void __launch_bounds__(P_THREADS, 1)
+    k_gemm_f8_promote(const __grid_constant__ CUtensorMap tmap_a,
+                      const __grid_constant__ CUtensorMap tmap_b, const PParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    const uint32_t sA = base + POFF_A, sB = base + POFF_B, sBAR = base + POFF_BAR;
+    const uint32_t full = sBAR + PBAR_FULL, empty = sBAR + PBAR_EMPTY;
+    const uint32_t pfull = sBAR + PBAR_PFULL, pempty = sBAR + PBAR_PEMPTY, drain = sBAR + PBAR_DRAIN;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + POFF_TMEM_SLOT);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + POFF_ABORT);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t limit = p.wait_limit_ns;
+    const uint64_t drain_limit = 2000000ull;  // 2 ms: copies and MMAs finish in microseconds
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < PSTAGES; ++s) {
+            ptx::mbar_init(full + 8 * s, 1);
+            ptx::mbar_init(empty + 8 * s, 1);
+        }
+        for (int b = 0; b < PBUF; ++b) {
+            ptx::mbar_init(pfull + 8 * b, 1);
+            ptx::mbar_init(pempty + 8 * b, kEpiWarps);
+        }
+        ptx::mbar_init(drain, 1);
+        *abort_flag = 0u;
+        ptx::fence_mbar_init();
+        ptx::prefetch_tmap(&tmap_a);
+        ptx::prefetch_tmap(&tmap_b);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), P_TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+            int mb, nb;
+            tile_coords(tile, p.num_mb, p.num_nb, mb, nb);
+            for (int kb = 0; kb < p.nk; ++kb) {
+                const uint32_t s = it % PSTAGES, ph = (it / PSTAGES) & 1u;
+                ok = wait_phase(empty + 8 * s, ph ^ 1u, limit, abort_flag, p.err, WHO_PRODUCER);
+                ok = __all_sync(0xFFFFFFFFu, ok);
+                if (!ok) break;
+                if (lane == 0) {
+                    ptx::mbar_arrive_expect_tx(full + 8 * s, PA_TILE + PB_TILE);
+                    ptx::tma_load_2d(sA + s * PA_TILE, &tmap_a, full + 8 * s, kb * PK, mb * PM);
+                    ptx::tma_load_2d(sB + s * PB_TILE, &tmap_b, full + 8 * s, kb * PK, nb * PN);
+                }
+                __syncwarp();
+                ++it;
+            }
+        }
+        const uint32_t nd = it < static_cast<uint32_t>(PSTAGES) ? it : static_cast<uint32_t>(PSTAGES);
+        for (uint32_t i = it - nd; i < it; ++i)
+            wait_phase(full + 8 * (i % PSTAGES), (i / PSTAGES) & 1u, drain_limit, abort_flag, p.err,
+                       WHO_PRODUCER, false);
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        uint32_t it = 0, g = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+            for (int kb = 0; kb < p.nk; ++kb) {
+                const uint32_t s = it % PSTAGES, ph = (it / PSTAGES) & 1u;
+                const uint32_t b = g % PBUF, pph = (g / PBUF) & 1u;
+                ok = wait_phase(pempty + 8 * b, pph ^ 1u, limit, abort_flag, p.err, WHO_MMA);
+                ok = ok && wait_phase(full + 8 * s, ph, limit, abort_flag, p.err, WHO_MMA);
+                ok = __all_sync(0xFFFFFFFFu, ok);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                if (lane == 0) {
+                    const uint64_t ad = desc_sw128(sA + s * PA_TILE);
+                    const uint64_t bd = desc_sw128(sB + s * PB_TILE);
+#pragma unroll
+                    for (int j = 0; j < PK / 32; ++j)
+                        ptx::tc_mma_f8(tmem + b * PN, ad + 2 * j, bd + 2 * j, p.idesc, j != 0 ? 1u : 0u);
+                    ptx::tc_commit(empty + 8 * s);  // the stage may be refilled
+                    ptx::tc_commit(pfull + 8 * b);  // the partial product is ready
+                }
+                __syncwarp();
+                ++it;
+                ++g;
+            }
+        }
+        if (lane == 0) ptx::tc_commit(drain);
+        __syncwarp();
+        wait_phase(drain, 0u, drain_limit, abort_flag, p.err, WHO_MMA, false);
+    } else if (warp >= 4) {
+        // ------------------------------------------------- promotion epilogue
+        const int q = warp & 3, h = (warp - 4) >> 2;  // lane quarter, column half
+        uint32_t g = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+            int mb, nb;
+            tile_coords(tile, p.num_mb, p.num_nb, mb, nb);
+            const int64_t row = static_cast<int64_t>(mb) * PM + q * 32 + lane;
+            const float *sa_row = p.sa + row * p.ld_sa;
+            const float *sb_blk = p.sb + static_cast<int64_t>(nb) * p.ld_sb;
+            float acc[64];
+#pragma unroll
+            for (int e = 0; e < 64; ++e) acc[e] = 0.0f;
+            // factors sa * sb of the current group of k-blocks; the next
+            // group's scales are in flight while it is consumed
+            float f[kScaleGroup], na[kScaleGroup], nbv[kScaleGroup];
+#pragma unroll
+            for (int t = 0; t < kScaleGroup; ++t) {
+                const bool v = t < p.nk;
+                f[t] = v ? ld_f32_now(sa_row + t * p.a_step) * ld_f32_now(sb_blk + t) : 0.0f;
+            }
+            for (int kg = 0; kg * kScaleGroup < p.nk && ok; ++kg) {
+                const int nk0 = (kg + 1) * kScaleGroup;
+#pragma unroll
+                for (int t = 0; t < kScaleGroup; ++t) {
+                    const bool v = nk0 + t < p.nk;
+                    na[t] = v ? ld_f32_now(sa_row + (nk0 + t) * p.a_step) : 0.0f;
+                    nbv[t] = v ? ld_f32_now(sb_blk + nk0 + t) : 0.0f;
+                }
+#pragma unroll
+                for (int t = 0; t < kScaleGroup; ++t) {
+                    if (kg * kScaleGroup + t >= p.nk) break;
+                    const uint32_t b = g % PBUF, pph = (g / PBUF) & 1u;
+                    ok = wait_phase(pfull + 8 * b, pph, limit, abort_flag, p.err, WHO_EPILOGUE);
+                    ok = __all_sync(0xFFFFFFFFu, ok);
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * PN + h * 64;
+                    uint32_t r0[32], r1[32];
+                    ptx::tmem_ld_32x32b_x32(taddr, r0);
+                    ptx::tmem_ld_32x32b_x32(taddr + 32, r1);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        acc[e] = fmaf(f[t], __uint_as_float(r0[e]), acc[e]);
+                        acc[32 + e] = fmaf(f[t], __uint_as_float(r1[e]), acc[32 + e]);
+                    }
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(pempty + 8 * b);  // the buffer may be rewritten
+                    ++g;
+                }
+#pragma unroll
+                for (int t = 0; t < kScaleGroup; ++t) f[t] = na[t] * nbv[t];
+            }
+            if (!ok) break;
+            const int64_t n0 = static_cast<int64_t>(nb) * PN + h * 64;
+            if (p.out_fp32) {
+                float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.c) + row * p.ldc + n0);
+#pragma unroll
+                for (int v = 0; v < 16; ++v)
+                    dst[v] = make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+            } else {
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.c) + row * p.ldc + n0);
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                    dst[v] = make_uint4(ptx::cvt_bf16x2(acc[8 * v], acc[8 * v + 1]),
+                                        ptx::cvt_bf16x2(acc[8 * v + 2], acc[8 * v + 3]),
+                                        ptx::cvt_bf16x2(acc[8 * v + 4], acc[8 * v + 5]),
+                                        ptx::cvt_bf16x2(acc[8 * v + 6], acc[8 * v + 7]));
+            }
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, P_TMEM_COLS);
+    }
+}
+
+bool make_tmap_128(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t k, uint64_t ld) {
+    TensorMapEncodeFn enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {k, rows};
+    const cuuint64_t strides[1] = {ld};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(PK), 128u};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+std::mutex g_pmu;
+bool g_pattr[64] = {false};
+int g_psms[64] = {0};
+
+}  // namespace
+
+int launch_gemm_f32s(const GemmF32sArgs &g, cudaStream_t stream) {
+    CUtensorMap ta, tb;
+    std::memset(&ta, 0, sizeof(ta));
+    std::memset(&tb, 0, sizeof(tb));
+    if (!make_tmap_128(&ta, g.a_codes, g.M, g.K, g.lda)) return 1;
+    if (!make_tmap_128(&tb, g.b_codes, g.N, g.K, g.ldb)) return 1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_pmu);
+        if (!g_pattr[dev]) {
+            const cudaError_t e = cudaFuncSetAttribute(
+                k_gemm_f8_promote, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                static_cast<int>(P_SMEM_BYTES));
+            if (e != cudaSuccess) return 2 + static_cast<int>(e);
+            int n = 0;
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+            g_psms[dev] = n > 0 ? n : 1;
+            g_pattr[dev] = true;
+        }
+    }
+    PParams p;
+    p.M = static_cast<int>(g.M);
+    p.N = static_cast<int>(g.N);
+    p.nk = static_cast<int>(g.K / PK);
+    p.num_mb = static_cast<int>(g.M / PM);
+    p.num_nb = static_cast<int>(g.N / PN);
+    p.num_tiles = p.num_mb * p.num_nb;
+    p.a_step = g.a_per_token ? 0 : 1;
+    p.sa = g.a_scale;
+    p.sb = g.b_scale;
+    p.ld_sa = g.ld_sa;
+    p.ld_sb = g.ld_sb;
+    p.c = g.c;
+    p.ldc = g.ldc;
+    p.out_fp32 = g.out_fp32;
+    // kind::f8f6f4 instruction descriptor: FP32 accumulator (bits 4-5 = 1),
+    // A / B formats in bits 7-9 / 10-12 (E4M3 = 0, E5M2 = 1), both K-major,
+    // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+    p.idesc = (1u << 4) | (static_cast<uint32_t>(g.fmt_a) << 7) |
+              (static_cast<uint32_t>(g.fmt_b) << 10) | (static_cast<uint32_t>(PN >> 3) << 17) |
+              (static_cast<uint32_t>(PM >> 4) << 24);
+    p.wait_limit_ns = g.wait_limit_ns;
+    p.err = g.err;
+    int grid = g_psms[dev];
+    if (grid > p.num_tiles) grid = p.num_tiles;
+    k_gemm_f8_promote<<<grid, P_THREADS, P_SMEM_BYTES, stream>>>(ta, tb, p);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? 0 : 2 + static_cast<int>(e);
+}
+
+}  // namespace fp8hg

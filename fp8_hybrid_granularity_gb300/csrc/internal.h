@@ -40,6 +40,15 @@ cudaError_t launch_quant_block128(const uint16_t *x, int64_t rows, int64_t cols,
                                   uint8_t *qt, int64_t ld_qt, uint8_t *st, int64_t ld_st,
                                   cudaStream_t stream);
 
+cudaError_t launch_quant_token_f32s(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
+                                    int group, int fmt, uint8_t *q, int64_t ld_q, float *s,
+                                    int64_t ld_s, cudaStream_t stream);
+
+cudaError_t launch_quant_block128_f32s(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
+                                       int fmt, uint8_t *q, int64_t ld_q, float *s, int64_t ld_s,
+                                       uint8_t *qt, int64_t ld_qt, float *st, int64_t ld_st,
+                                       cudaStream_t stream);
+
 struct GemmArgs {
     const uint8_t *a_codes, *b_codes;
     const uint8_t *a_scale, *b_scale;
@@ -60,6 +69,22 @@ struct GemmArgs {
 // Returns 0 on success, 1 if the tensor maps could not be encoded, or a
 // cudaError_t + 2 on a launch failure.
 int launch_gemm_scaled(const GemmArgs &args, cudaStream_t stream);
+
+// FP8 GEMM with FP32 scale factors (promotion on the CUDA cores): A scales
+// per row (a_per_token) or per (row, 128-K block), B scales per 128x128 block.
+struct GemmF32sArgs {
+    const uint8_t *a_codes, *b_codes;
+    const float *a_scale, *b_scale;
+    int64_t M, N, K;
+    int64_t lda, ldb, ld_sa, ld_sb;  // ld_sa / ld_sb in floats
+    int fmt_a, fmt_b, a_per_token;
+    void *c;
+    int64_t ldc;
+    int out_fp32;
+    uint64_t wait_limit_ns;
+    unsigned int *err;
+};
+int launch_gemm_f32s(const GemmF32sArgs &args, cudaStream_t stream);
 
 // Device address of the error word of the current device (null on failure).
 unsigned int *device_error_word();

@@ -53,7 +53,7 @@ __device__ __forceinline__ bool row_wait(uint32_t bar, uint32_t parity, uint64_t
     return true;
 }
 
-template <int FMT>
+template <int FMT, int SM>
 __global__ void __launch_bounds__(kRowThreads) k_quant_row(const uint16_t *__restrict__ x,
                                                               int64_t rows, int nvec, int64_t ld_x,
                                                               uint8_t *__restrict__ q, int64_t ld_q,
@@ -116,21 +116,20 @@ __global__ void __launch_bounds__(kRowThreads) k_quant_row(const uint16_t *__res
         __syncthreads();
         m = 0;
         for (int w = 0; w < nwarps; ++w) m = max(m, red[w]);
-        float mul;
-        const uint32_t sbyte = group_scale<FMT, false>(m, mul);
+        const GroupScale<FMT, SM> gs(m);
         uint2 *qr = reinterpret_cast<uint2 *>(q + row * ld_q);
         uint32_t unused = 0;
         for (int c = tid; c < nvec; c += blockDim.x)
-            qr[c] = (sbyte == 0xFFu) ? make_uint2(kNanCodes, kNanCodes)
-                                     : quant8<FMT, false>(xs[c], mul, unused);
-        if (tid == 0) s[row * ld_s] = static_cast<uint8_t>(sbyte);
+            qr[c] = gs.nan ? make_uint2(kNanCodes, kNanCodes)
+                           : quant8<FMT, false>(xs[c], gs.mul, unused);
+        if (tid == 0) gs.store(s, row * ld_s);
         __syncthreads();  // the slot and red[] are free for the next row
     }
 }
 
 // Short rows (up to 8 KB): one CTA per row, the row kept in registers between
 // the amax and the cast; many small CTAs keep the memory system busy.
-template <int FMT, int NV>
+template <int FMT, int NV, int SM>
 __global__ void __launch_bounds__(512) k_quant_row_regs(const uint16_t *__restrict__ x, int nvec,
                                                         int64_t ld_x, uint8_t *__restrict__ q,
                                                    int64_t ld_q, uint8_t *__restrict__ s,
@@ -160,24 +159,23 @@ __global__ void __launch_bounds__(512) k_quant_row_regs(const uint16_t *__restri
         if (lane == 0) bcast = t;
     }
     __syncthreads();
-    float mul;
-    const uint32_t sbyte = group_scale<FMT, false>(bcast, mul);
+    const GroupScale<FMT, SM> gs(bcast);
     uint2 *qr = reinterpret_cast<uint2 *>(q + row * ld_q);
     uint32_t unused = 0;
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
         const int c = tid + i * blockDim.x;
         if (c < nvec) {
-            qr[c] = (sbyte == 0xFFu) ? make_uint2(kNanCodes, kNanCodes)
-                                     : quant8<FMT, false>(v[i], mul, unused);
+            qr[c] = gs.nan ? make_uint2(kNanCodes, kNanCodes)
+                           : quant8<FMT, false>(v[i], gs.mul, unused);
         }
     }
-    if (tid == 0) s[row * ld_s] = static_cast<uint8_t>(sbyte);
+    if (tid == 0) gs.store(s, row * ld_s);
 }
 
 // Rows too long to keep in registers: the amax pass and the cast pass read the
 // row twice (the second read is served from L2).
-template <int FMT>
+template <int FMT, int SM>
 __global__ void __launch_bounds__(512) k_quant_row_2pass(const uint16_t *__restrict__ x, int nvec,
                                                          int64_t ld_x, uint8_t *__restrict__ q,
                                                          int64_t ld_q, uint8_t *__restrict__ s,
@@ -199,15 +197,14 @@ __global__ void __launch_bounds__(512) k_quant_row_2pass(const uint16_t *__restr
         if (lane == 0) bcast = t;
     }
     __syncthreads();
-    float mul;
-    const uint32_t sbyte = group_scale<FMT, false>(bcast, mul);
+    const GroupScale<FMT, SM> gs(bcast);
     uint2 *qr = reinterpret_cast<uint2 *>(q + row * ld_q);
     uint32_t unused = 0;
     for (int c = tid; c < nvec; c += blockDim.x) {
-        qr[c] = (sbyte == 0xFFu) ? make_uint2(kNanCodes, kNanCodes)
-                                 : quant8<FMT, false>(xr[c], mul, unused);
+        qr[c] = gs.nan ? make_uint2(kNanCodes, kNanCodes)
+                       : quant8<FMT, false>(xr[c], gs.mul, unused);
     }
-    if (tid == 0) s[row * ld_s] = static_cast<uint8_t>(sbyte);
+    if (tid == 0) gs.store(s, row * ld_s);
 }
 
 // ------------------------------------------------------ groups along a row
@@ -232,7 +229,7 @@ __device__ __forceinline__ uint32_t top_codes(const uint2 &c) {
 // 256*U consecutive vectors of a row (blockIdx.x) for the rows blockIdx.y,
 // blockIdx.y + gridDim.y, ...; lanes [g*GV, g*GV + GV) of a warp hold one
 // group, and every lane reaches the shuffles.
-template <int FMT, int GV, bool MX, bool COUNT, bool MON, int U>
+template <int FMT, int GV, int SM, bool COUNT, bool MON, int U>
 __global__ void __launch_bounds__(256) k_quant_groups(const uint16_t *__restrict__ x, int64_t rows,
                                                       int vpr, int64_t ld_x,
                                                       uint8_t *__restrict__ q, int64_t ld_q,
@@ -265,15 +262,15 @@ __global__ void __launch_bounds__(256) k_quant_groups(const uint16_t *__restrict
 #pragma unroll
             for (int o = GV / 2; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
             uint2 out = make_uint2(0u, 0u);
-            uint32_t sbyte = 0;
+            bool group_nan = false;
             const uint32_t before = nsat;
             if (ok) {
-                float mul;
-                sbyte = group_scale<FMT, MX>(m, mul);
-                out = (sbyte == 0xFFu) ? make_uint2(kNanCodes, kNanCodes)
-                                       : quant8<FMT, SAT>(v[u], mul, nsat);
+                const GroupScale<FMT, SM> gs(m);
+                group_nan = gs.nan;
+                out = gs.nan ? make_uint2(kNanCodes, kNanCodes)
+                             : quant8<FMT, SAT>(v[u], gs.mul, nsat);
                 *reinterpret_cast<uint2 *>(q + row * ld_q + static_cast<int64_t>(cv) * 8) = out;
-                if ((lane % GV) == 0) s[row * ld_s + cv / GV] = static_cast<uint8_t>(sbyte);
+                if ((lane % GV) == 0) gs.store(s, row * ld_s + cv / GV);
             }
             if constexpr (MON) {
                 // lanes past the row's end hold out = 0: no top codes, no saturation
@@ -289,7 +286,7 @@ __global__ void __launch_bounds__(256) k_quant_groups(const uint16_t *__restrict
                 }
                 if (ok && (lane % GV) == 0) {
                     nbsat += gsat != 0u;
-                    ncoll += (same && m != 0u && sbyte != 0xFFu) ? 1u : 0u;
+                    ncoll += (same && m != 0u && !group_nan) ? 1u : 0u;
                 }
                 row_nsat += dsat;
             }
@@ -592,7 +589,7 @@ __device__ __forceinline__ void transpose4x4(uint32_t a0, uint32_t a1, uint32_t 
 }
 
 // One CTA per 128x128 block; thread (rsub, csub) owns an 8x8 sub-block.
-template <int FMT, bool TRANS>
+template <int FMT, bool TRANS, int SM>
 __global__ void __launch_bounds__(256) k_quant_block128(const uint16_t *__restrict__ x,
                                                         int64_t ld_x, uint8_t *__restrict__ q,
                                                         int64_t ld_q, uint8_t *__restrict__ s,
@@ -618,19 +615,18 @@ __global__ void __launch_bounds__(256) k_quant_block128(const uint16_t *__restri
     m = red[0];
 #pragma unroll
     for (int i = 1; i < 8; ++i) m = max(m, red[i]);
-    float mul;
-    const uint32_t sbyte = group_scale<FMT, false>(m, mul);
+    const GroupScale<FMT, SM> gs(m);
     uint2 o[8];
     uint32_t unused = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        o[i] = (sbyte == 0xFFu) ? make_uint2(kNanCodes, kNanCodes)
-                                : quant8<FMT, false>(v[i], mul, unused);
+        o[i] = gs.nan ? make_uint2(kNanCodes, kNanCodes)
+                      : quant8<FMT, false>(v[i], gs.mul, unused);
         *reinterpret_cast<uint2 *>(q + (r_first + i) * ld_q + c_first) = o[i];
     }
     if (tid == 0) {
-        s[rb * ld_s + cb] = static_cast<uint8_t>(sbyte);
-        if constexpr (TRANS) st[cb * ld_st + rb] = static_cast<uint8_t>(sbyte);
+        gs.store(s, rb * ld_s + cb);
+        if constexpr (TRANS) gs.store(st, cb * ld_st + rb);
     }
     if constexpr (TRANS) {
         uint32_t lo03[4], lo47[4], hi03[4], hi47[4];
@@ -685,7 +681,7 @@ int resident_blocks(K kernel, int threads) {
     return n;
 }
 
-template <int FMT>
+template <int FMT, int SM>
 cudaError_t launch_row_regs(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, uint8_t *q,
                        int64_t ld_q, uint8_t *s, int64_t ld_s, cudaStream_t stream) {
     const int nvec = static_cast<int>(cols / 8);
@@ -709,27 +705,25 @@ cudaError_t launch_row_regs(const uint16_t *x, int64_t rows, int64_t cols, int64
     }
     const dim3 grid(static_cast<unsigned>(rows));
     if (best_nv < 0) {
-        k_quant_row_2pass<FMT><<<grid, 512, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s);
+        k_quant_row_2pass<FMT, SM><<<grid, 512, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s);
         return cudaGetLastError();
     }
     switch (best_nv) {
-    case 1: k_quant_row_regs<FMT, 1><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
-    case 2: k_quant_row_regs<FMT, 2><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
-    case 4: k_quant_row_regs<FMT, 4><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
-    case 8: k_quant_row_regs<FMT, 8><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
-    default: k_quant_row_regs<FMT, 16><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
+    case 1: k_quant_row_regs<FMT, 1, SM><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
+    case 2: k_quant_row_regs<FMT, 2, SM><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
+    case 4: k_quant_row_regs<FMT, 4, SM><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
+    case 8: k_quant_row_regs<FMT, 8, SM><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
+    default: k_quant_row_regs<FMT, 16, SM><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
     }
     return cudaGetLastError();
 }
 
-bool g_row_attr[64][2] = {{false}};
-
-template <int FMT>
+template <int FMT, int SM>
 cudaError_t launch_row(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, uint8_t *q,
                        int64_t ld_q, uint8_t *s, int64_t ld_s, cudaStream_t stream) {
     const int nvec = static_cast<int>(cols / 8);
     const int64_t row_bytes = cols * 2;
-    if (row_bytes <= 8192) return launch_row_regs<FMT>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream);
+    if (row_bytes <= 8192) return launch_row_regs<FMT, SM>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream);
     // Rows up to ~50 KB: up to 4 CTAs per SM, so that one CTA's per-row
     // synchronisation overlaps the others' work; each CTA keeps at least 4
     // (and at most 8) rows in flight, ~200 KB per SM in total.
@@ -739,19 +733,20 @@ cudaError_t launch_row(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld
     if (nslots > kMaxRowSlots) nslots = kMaxRowSlots;
     if (nslots < 2) {
         // rows too long to stage two at a time: amax pass + cast pass
-        k_quant_row_2pass<FMT><<<static_cast<unsigned>(rows), 512, 0, stream>>>(x, nvec, ld_x, q,
-                                                                                ld_q, s, ld_s);
+        k_quant_row_2pass<FMT, SM><<<static_cast<unsigned>(rows), 512, 0, stream>>>(x, nvec, ld_x, q,
+                                                                                    ld_q, s, ld_s);
         return cudaGetLastError();
     }
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) dev = 0;
-    if (!g_row_attr[dev][FMT]) {
-        const cudaError_t e = cudaFuncSetAttribute(k_quant_row<FMT>,
+    static bool attr_set[64] = {false};   // one flag per device and instantiation
+    if (!attr_set[dev]) {
+        const cudaError_t e = cudaFuncSetAttribute(k_quant_row<FMT, SM>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    kRowSmemBudget);
         if (e != cudaSuccess) return e;
-        g_row_attr[dev][FMT] = true;
+        attr_set[dev] = true;
     }
     int64_t grid = static_cast<int64_t>(num_sms()) * ctas_per_sm;
     if (grid > rows) grid = rows;
@@ -759,28 +754,28 @@ cudaError_t launch_row(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld
     if (nvec < threads) threads = ((nvec + 31) / 32) * 32;
     unsigned int *err = device_error_word();
     if (!err) return cudaErrorInvalidValue;
-    k_quant_row<FMT><<<static_cast<unsigned>(grid), threads, static_cast<size_t>(nslots) * row_bytes,
+    k_quant_row<FMT, SM><<<static_cast<unsigned>(grid), threads, static_cast<size_t>(nslots) * row_bytes,
                        stream>>>(x, rows, nvec, ld_x, q, ld_q, s, ld_s, nslots, err);
     return cudaGetLastError();
 }
 
-template <int FMT, int GV, bool MX, bool COUNT, bool MON, int U>
+template <int FMT, int GV, int SM, bool COUNT, bool MON, int U>
 cudaError_t launch_groups_u(const uint16_t *x, int64_t rows, int vpr, int64_t ld_x, uint8_t *q,
                             int64_t ld_q, uint8_t *s, int64_t ld_s, MxCounters cnt,
                             cudaStream_t stream) {
     const int gx = (vpr + 256 * U - 1) / (256 * U);
     const int64_t target = static_cast<int64_t>(num_sms()) *
-                           resident_blocks(k_quant_groups<FMT, GV, MX, COUNT, MON, U>, 256);
+                           resident_blocks(k_quant_groups<FMT, GV, SM, COUNT, MON, U>, 256);
     int64_t gy = (target + gx - 1) / gx;
     if (gy > rows) gy = rows;
     if (gy > 65535) gy = 65535;
     if (gy < 1) gy = 1;
-    k_quant_groups<FMT, GV, MX, COUNT, MON, U><<<dim3(gx, static_cast<unsigned>(gy)), 256, 0, stream>>>(
+    k_quant_groups<FMT, GV, SM, COUNT, MON, U><<<dim3(gx, static_cast<unsigned>(gy)), 256, 0, stream>>>(
         x, rows, vpr, ld_x, q, ld_q, s, ld_s, cnt);
     return cudaGetLastError();
 }
 
-template <int FMT, int GV, bool MX, bool COUNT, bool MON = false>
+template <int FMT, int GV, int SM, bool COUNT, bool MON = false>
 cudaError_t launch_groups(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, uint8_t *q,
                           int64_t ld_q, uint8_t *s, int64_t ld_s, MxCounters cnt,
                           cudaStream_t stream) {
@@ -795,9 +790,9 @@ cudaError_t launch_groups(const uint16_t *x, int64_t rows, int64_t cols, int64_t
             break;
         }
     }
-    if (u == 4) return launch_groups_u<FMT, GV, MX, COUNT, MON, 4>(x, rows, vpr, ld_x, q, ld_q, s, ld_s, cnt, stream);
-    if (u == 2) return launch_groups_u<FMT, GV, MX, COUNT, MON, 2>(x, rows, vpr, ld_x, q, ld_q, s, ld_s, cnt, stream);
-    return launch_groups_u<FMT, GV, MX, COUNT, MON, 1>(x, rows, vpr, ld_x, q, ld_q, s, ld_s, cnt, stream);
+    if (u == 4) return launch_groups_u<FMT, GV, SM, COUNT, MON, 4>(x, rows, vpr, ld_x, q, ld_q, s, ld_s, cnt, stream);
+    if (u == 2) return launch_groups_u<FMT, GV, SM, COUNT, MON, 2>(x, rows, vpr, ld_x, q, ld_q, s, ld_s, cnt, stream);
+    return launch_groups_u<FMT, GV, SM, COUNT, MON, 1>(x, rows, vpr, ld_x, q, ld_q, s, ld_s, cnt, stream);
 }
 }  // namespace
 
@@ -812,14 +807,15 @@ cudaError_t launch_quant_token(const uint16_t *x, int64_t rows, int64_t cols, in
         return cudaGetLastError();
     }
     if (group == 0) {
-        return fmt == FMT_E4M3 ? launch_row<FMT_E4M3>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream)
-                               : launch_row<FMT_E5M2>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream);
+        return fmt == FMT_E4M3
+                   ? launch_row<FMT_E4M3, SCALE_UE8M0>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream)
+                   : launch_row<FMT_E5M2, SCALE_UE8M0>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream);
     }
     const MxCounters none{nullptr, nullptr, nullptr};
     return fmt == FMT_E4M3
-               ? launch_groups<FMT_E4M3, 16, false, false>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
+               ? launch_groups<FMT_E4M3, 16, SCALE_UE8M0, false>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
                                                            none, stream)
-               : launch_groups<FMT_E5M2, 16, false, false>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
+               : launch_groups<FMT_E5M2, 16, SCALE_UE8M0, false>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
                                                            none, stream);
 }
 
@@ -830,15 +826,15 @@ cudaError_t launch_quant_mx32(const uint16_t *x, int64_t rows, int64_t cols, int
     const MxCounters c{cnt, nullptr, nullptr};
     if (cnt) {
         return fmt == FMT_E4M3
-                   ? launch_groups<FMT_E4M3, 4, true, true>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
+                   ? launch_groups<FMT_E4M3, 4, SCALE_MX, true>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
                                                             c, stream)
-                   : launch_groups<FMT_E5M2, 4, true, true>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
+                   : launch_groups<FMT_E5M2, 4, SCALE_MX, true>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
                                                             c, stream);
     }
     return fmt == FMT_E4M3
-               ? launch_groups<FMT_E4M3, 4, true, false>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
+               ? launch_groups<FMT_E4M3, 4, SCALE_MX, false>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
                                                          c, stream)
-               : launch_groups<FMT_E5M2, 4, true, false>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
+               : launch_groups<FMT_E5M2, 4, SCALE_MX, false>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
                                                          c, stream);
 }
 
@@ -849,9 +845,9 @@ cudaError_t launch_quant_mx32_monitor(const uint16_t *x, int64_t rows, int64_t c
     if (rows == 0 || cols == 0) return cudaSuccess;
     const MxCounters c{nullptr, stats, row_sat};
     return fmt == FMT_E4M3
-               ? launch_groups<FMT_E4M3, 4, true, false, true>(x, rows, cols, ld_x, q, ld_q, s,
+               ? launch_groups<FMT_E4M3, 4, SCALE_MX, false, true>(x, rows, cols, ld_x, q, ld_q, s,
                                                                ld_s, c, stream)
-               : launch_groups<FMT_E5M2, 4, true, false, true>(x, rows, cols, ld_x, q, ld_q, s,
+               : launch_groups<FMT_E5M2, 4, SCALE_MX, false, true>(x, rows, cols, ld_x, q, ld_q, s,
                                                                ld_s, c, stream);
 }
 
@@ -900,27 +896,66 @@ cudaError_t launch_requant_t(const uint8_t *q, int64_t rows, int64_t cols, int64
                                : run(k_requant_t<FMT_E5M2, FMT_E5M2>);
 }
 
+namespace {
+template <int FMT, int SM>
+void launch_block128_t(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, uint8_t *q,
+                       int64_t ld_q, uint8_t *s, int64_t ld_s, uint8_t *qt, int64_t ld_qt,
+                       uint8_t *st, int64_t ld_st, cudaStream_t stream) {
+    const dim3 grid(static_cast<unsigned>(cols / 128), static_cast<unsigned>(rows / 128));
+    if (qt)
+        k_quant_block128<FMT, true, SM><<<grid, 256, 0, stream>>>(x, ld_x, q, ld_q, s, ld_s, qt,
+                                                                  ld_qt, st, ld_st);
+    else
+        k_quant_block128<FMT, false, SM><<<grid, 256, 0, stream>>>(x, ld_x, q, ld_q, s, ld_s,
+                                                                   nullptr, 0, nullptr, 0);
+}
+}  // namespace
+
 cudaError_t launch_quant_block128(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
                                   int fmt, uint8_t *q, int64_t ld_q, uint8_t *s, int64_t ld_s,
                                   uint8_t *qt, int64_t ld_qt, uint8_t *st, int64_t ld_st,
                                   cudaStream_t stream) {
     if (rows == 0 || cols == 0) return cudaSuccess;
-    const dim3 grid(static_cast<unsigned>(cols / 128), static_cast<unsigned>(rows / 128));
-    if (qt) {
-        if (fmt == FMT_E4M3)
-            k_quant_block128<FMT_E4M3, true><<<grid, 256, 0, stream>>>(x, ld_x, q, ld_q, s, ld_s, qt,
-                                                                       ld_qt, st, ld_st);
-        else
-            k_quant_block128<FMT_E5M2, true><<<grid, 256, 0, stream>>>(x, ld_x, q, ld_q, s, ld_s, qt,
-                                                                       ld_qt, st, ld_st);
-    } else {
-        if (fmt == FMT_E4M3)
-            k_quant_block128<FMT_E4M3, false><<<grid, 256, 0, stream>>>(x, ld_x, q, ld_q, s, ld_s,
-                                                                        nullptr, 0, nullptr, 0);
-        else
-            k_quant_block128<FMT_E5M2, false><<<grid, 256, 0, stream>>>(x, ld_x, q, ld_q, s, ld_s,
-                                                                        nullptr, 0, nullptr, 0);
-    }
+    if (fmt == FMT_E4M3)
+        launch_block128_t<FMT_E4M3, SCALE_UE8M0>(x, rows, cols, ld_x, q, ld_q, s, ld_s, qt, ld_qt,
+                                                 st, ld_st, stream);
+    else
+        launch_block128_t<FMT_E5M2, SCALE_UE8M0>(x, rows, cols, ld_x, q, ld_q, s, ld_s, qt, ld_qt,
+                                                 st, ld_st, stream);
+    return cudaGetLastError();
+}
+
+// FP32-scale variant: per token (group 0) or 1x128 (group 128), and
+// 128x128 blocks; scales are floats (ld in floats).
+cudaError_t launch_quant_token_f32s(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
+                                    int group, int fmt, uint8_t *q, int64_t ld_q, float *sf,
+                                    int64_t ld_s, cudaStream_t stream) {
+    if (rows == 0 || cols == 0) return cudaSuccess;
+    uint8_t *s = reinterpret_cast<uint8_t *>(sf);
+    if (group == 0)
+        return fmt == FMT_E4M3
+                   ? launch_row<FMT_E4M3, SCALE_F32>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream)
+                   : launch_row<FMT_E5M2, SCALE_F32>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream);
+    const MxCounters none{nullptr, nullptr, nullptr};
+    return fmt == FMT_E4M3
+               ? launch_groups<FMT_E4M3, 16, SCALE_F32, false>(x, rows, cols, ld_x, q, ld_q, s,
+                                                               ld_s, none, stream)
+               : launch_groups<FMT_E5M2, 16, SCALE_F32, false>(x, rows, cols, ld_x, q, ld_q, s,
+                                                               ld_s, none, stream);
+}
+
+cudaError_t launch_quant_block128_f32s(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
+                                       int fmt, uint8_t *q, int64_t ld_q, float *s, int64_t ld_s,
+                                       uint8_t *qt, int64_t ld_qt, float *st, int64_t ld_st,
+                                       cudaStream_t stream) {
+    if (rows == 0 || cols == 0) return cudaSuccess;
+    uint8_t *sb = reinterpret_cast<uint8_t *>(s), *stb = reinterpret_cast<uint8_t *>(st);
+    if (fmt == FMT_E4M3)
+        launch_block128_t<FMT_E4M3, SCALE_F32>(x, rows, cols, ld_x, q, ld_q, sb, ld_s, qt, ld_qt,
+                                               stb, ld_st, stream);
+    else
+        launch_block128_t<FMT_E5M2, SCALE_F32>(x, rows, cols, ld_x, q, ld_q, sb, ld_s, qt, ld_qt,
+                                               stb, ld_st, stream);
     return cudaGetLastError();
 }
 

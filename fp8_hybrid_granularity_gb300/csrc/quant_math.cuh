@@ -118,4 +118,49 @@ __device__ __forceinline__ uint32_t group_scale(uint32_t amax_bits, float &mul) 
 
 constexpr uint32_t kNanCodes = 0x7F7F7F7Fu;
 
+// How a group's scale is chosen and stored.
+//  SCALE_UE8M0  power of two rounded up (one byte, e + 127)
+//  SCALE_MX     power of two floor(log2 amax) - emax (one byte)
+//  SCALE_F32    the FP32-scale variant: d = fl32(amax / FMAX) is stored and
+//               x is multiplied by m = fl32(FMAX / amax) before the cast
+//               (amax = 0: d = m = 1); both divisions correctly rounded.
+enum { SCALE_UE8M0 = 0, SCALE_MX = 1, SCALE_F32 = 2 };
+
+template <int FMT, int SM>
+struct GroupScale {
+    float mul;      // multiplier applied before the cast
+    uint32_t byte;  // UE8M0 / MX scale byte (0xFF for a non-finite group)
+    float d;        // FP32 scale (NaN for a non-finite group)
+    bool nan;       // the group holds a NaN or an infinity
+    __device__ __forceinline__ explicit GroupScale(uint32_t amax_bits) {
+        nan = amax_bits >= 0x7F80u;
+        if constexpr (SM == SCALE_F32) {
+            const float fmax = fp8_maxf<FMT>();
+            const float a = __uint_as_float(amax_bits << 16);  // BF16 -> FP32, exact
+            byte = 0;
+            if (nan) {
+                d = __uint_as_float(0x7FC00000u);
+                mul = 0.0f;
+            } else if (a == 0.0f) {
+                d = 1.0f;
+                mul = 1.0f;
+            } else {
+                d = __fdiv_rn(a, fmax);
+                mul = __fdiv_rn(fmax, a);
+            }
+        } else {
+            byte = group_scale<FMT, SM == SCALE_MX>(amax_bits, mul);
+            d = 0.0f;
+        }
+    }
+    // The group's scale at element index idx of the caller's scale array
+    // (bytes, or floats for SCALE_F32).
+    __device__ __forceinline__ void store(uint8_t *s, int64_t idx) const {
+        if constexpr (SM == SCALE_F32) reinterpret_cast<float *>(s)[idx] = d;
+        else s[idx] = static_cast<uint8_t>(byte);
+    }
+};
+
+
+
 }  // namespace fp8hg

@@ -13,6 +13,9 @@ kernel, and prints the mean launch time from CUDA events.  Cases:
              [18944, 3584] 128x128 blocks, BF16 out
   gemm_gate_q  the same with the output quantized in the epilogue (E4M3,
              1x128 along N)
+  gemm_gate_f32s  the gate projection with FP32 scales (promotion GEMM)
+  gemm_f32s  the down projection with FP32 scales
+  quant_row_f32s  per-token quantization of H with FP32 scales
   wgrad      gate weight gradient: A = dY^T [18944, M] 1x128 E5M2, B = X^T
              [3584, M] 1x128 E4M3, FP32 out
   quant_row  per-token quantization of H [M, 18944]
@@ -39,7 +42,8 @@ HID, MLP = 3584, 18944
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["gemm", "gemm_gate", "gemm_gate_q", "wgrad", "quant_row", "quant_1x128", "quant_t", "block128",
+    ap.add_argument("case", choices=["gemm", "gemm_gate", "gemm_gate_q", "gemm_gate_f32s", "gemm_f32s",
+                                     "quant_row_f32s", "wgrad", "quant_row", "quant_1x128", "quant_t", "block128",
                                      "mx32", "mx32_mon", "requant"])
     ap.add_argument("--m", type=int, default=4096)
     ap.add_argument("--warmup", type=int, default=2)
@@ -70,6 +74,21 @@ def main():
             out = torch.empty((M, MLP), dtype=torch.bfloat16, device=dev)
             fn = lambda: fp8hg.fp8_gemm_scaled(fp8hg.FPROP, a, b, out=out)
         work, unit = 2.0 * M * HID * MLP, "flop"
+    elif args.case in ("gemm_gate_f32s", "gemm_f32s"):
+        gate = args.case == "gemm_gate_f32s"
+        a_src = mk("act", M, HID if gate else MLP, "X" if gate else "H")
+        w = mk("weight", MLP if gate else HID, HID if gate else MLP, "W_gate" if gate else "W_down")
+        a = fp8hg.fp8_quant_token_f32s(a_src, 0, E4)
+        b = fp8hg.fp8_quant_block128_f32s(w, E4)
+        out = torch.empty((M, w.shape[0]), dtype=torch.bfloat16, device=dev)
+        fn = lambda: fp8hg.fp8_gemm_scaled_f32s(fp8hg.FPROP, a, b, out=out)
+        work, unit = 2.0 * M * HID * MLP, "flop"
+    elif args.case == "quant_row_f32s":
+        h = mk("act", M, MLP, "H")
+        out = fp8hg.QTensor(torch.empty((M, MLP), dtype=torch.uint8, device=dev),
+                            torch.empty((M, 1), dtype=torch.float32, device=dev), E4, 0, 1)
+        fn = lambda: fp8hg.fp8_quant_token_f32s(h, 0, E4, out=out)
+        work, unit = 3.0 * M * MLP + 4 * M, "byte"
     elif args.case == "wgrad":
         dy = mk("grad", M, MLP, "dY_gate")
         x = mk("act", M, HID, "X")

@@ -183,6 +183,52 @@ int fp8_requant_t(const uint8_t *q, int64_t rows, int64_t cols, int64_t ld_q, co
                   uint8_t *scale_t, int64_t ld_st, void *stream);
 
 /*
+ * FP32-scale variant ("FP8 w. FP32 scale").
+ *
+ * Passage: "A Comprehensive FP8 Training Recipe ...", referee comments: the
+ * recipe's ablation compares its UE8M0 scales with an "FP8 w. FP32 scale"
+ * arm that the setup does not define.  This library reads it as ordinary
+ * FP32 scaling at the same granularities: per group
+ *   d = fl32(amax / FMAX)       stored FP32 scale (x ~ decode(q) * d)
+ *   q = RNE_sat(fl32(x * fl32(FMAX / amax)))
+ * (amax = 0: d = 1, codes +-0; a NaN or infinity: d = NaN, codes 0x7F).
+ * Scales are float arrays; their leading dimensions count floats.
+ *
+ * fp8_quant_token_f32s: group 0 (per token, scale [rows]) or 128 (1x128,
+ *   scale [rows, cols/128]); cols % 128 == 0; alignment as fp8_quant_token,
+ *   scale 4-byte aligned.  No transposed form.
+ * fp8_quant_block128_f32s: one scale per 128x128 block, optional transposed
+ *   copy (q_t [cols, rows], scale_t [cols/128, rows/128]); requirements as
+ *   fp8_quant_block128.
+ */
+int fp8_quant_token_f32s(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int group,
+                         int fmt, uint8_t *q, int64_t ld_q, float *scale, int64_t ld_s,
+                         void *stream);
+int fp8_quant_block128_f32s(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
+                            uint8_t *q, int64_t ld_q, float *scale, int64_t ld_s, uint8_t *q_t,
+                            int64_t ld_qt, float *scale_t, int64_t ld_st, void *stream);
+
+/* An operand with FP32 scales: as fp8hg_operand, scale a float array with
+ * ld_scale counted in floats; gran ROW or 1x128 (A) / 128x128 (B). */
+typedef struct {
+    const uint8_t *codes;
+    const float *scale;
+    int64_t rows, k, ld, ld_scale;
+    int32_t fmt, gran;
+} fp8hg_operand_f32s;
+
+/*
+ * fp8_gemm_scaled_f32s — C = A * B^T with FP32 scale factors.  The tensor
+ * cores accumulate each 128-K block's raw FP8 product in FP32; the FP32
+ * factors sa * sb are applied on the CUDA cores between blocks (promotion).
+ * op FPROP or DGRAD: A ROW or 1x128, B 128x128 (WGRAD returns
+ * FP8HG_ERR_UNSUPPORTED).  out BF16 or FP32; M, N, K multiples of 128;
+ * codes 16-byte aligned, ld % 16 == 0; scales 4-byte aligned.
+ */
+int fp8_gemm_scaled_f32s(int op, const fp8hg_operand_f32s *a, const fp8hg_operand_f32s *b, void *c,
+                         int64_t ldc, int out, void *stream);
+
+/*
  * Counts of the MX clamp monitor (all over the whole tensor):
  *   saturated         elements whose scaled magnitude x * 2^-e exceeded the
  *                     format's largest value (448 or 57344) and were written

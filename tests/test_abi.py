@@ -9,7 +9,8 @@ import fp8_hybrid_granularity_gb300 as fp8hg
 from fp8_hybrid_granularity_gb300 import Operand, E4M3, GRAN_ROW, GRAN_1x128, GRAN_128x128, GRAN_MX32
 
 EXPECTED = {"fp8_quant_token", "fp8_quant_block128", "fp8_quant_mx32", "fp8_quant_mx32_monitor",
-            "fp8_requant_t", "fp8_gemm_scaled_q",
+            "fp8_requant_t", "fp8_gemm_scaled_q", "fp8_quant_token_f32s",
+            "fp8_quant_block128_f32s", "fp8_gemm_scaled_f32s",
             "fp8_gemm_scaled",
             "fp8_gemm_scaled_ex", "fp8hg_get_device_error", "fp8hg_status_str", "fp8hg_version"}
 
@@ -114,6 +115,31 @@ def test_gemm_q_validation(lib):
     assert call(b=_op(gran=GRAN_1x128)) == UNSUP    # fprop needs block B
     assert call(a=_op(rows=200)) == SHAPE
     assert call(op=7) == INVALID
+
+
+def test_f32s_validation(lib):
+    qt = lib.fp8_quant_token_f32s
+    assert qt(FAKE, 4, 128, 128, 64, E4M3, FAKE, 128, FAKE, 1, None) == INVALID    # group
+    assert qt(FAKE, 4, 128, 128, 0, E4M3, FAKE, 128, FAKE + 2, 1, None) == ALIGN   # scale align
+    assert qt(FAKE, 4, 96, 96, 0, E4M3, FAKE, 112, FAKE, 1, None) == SHAPE
+    assert qt(FAKE, 4, 256, 256, 128, E4M3, FAKE, 256, FAKE, 1, None) == INVALID   # ld_s
+    qb = lib.fp8_quant_block128_f32s
+    assert qb(FAKE, 100, 128, 128, E4M3, FAKE, 128, FAKE, 1, None, 0, None, 0, None) == SHAPE
+    assert qb(FAKE, 128, 128, 128, E4M3, FAKE, 128, FAKE, 1, FAKE, 128, None, 0, None) == INVALID
+    g = lib.fp8_gemm_scaled_f32s
+
+    def call(a, b, op=0, c=FAKE, ldc=256, out=0):
+        return g(op, ctypes.byref(a), ctypes.byref(b), c, ldc, out, None)
+
+    blk = dict(gran=GRAN_128x128, lds=2)
+    assert call(_op(gran=GRAN_ROW, lds=1), _op(**blk), op=2) == UNSUP     # wgrad
+    assert call(_op(), _op(gran=GRAN_1x128, lds=2)) == UNSUP             # B must be blocks
+    assert call(_op(gran=GRAN_MX32, lds=8), _op(**blk)) == UNSUP
+    assert call(_op(rows=200), _op(**blk)) == SHAPE
+    assert call(_op(lds=1), _op(**blk)) == INVALID                       # 1x128 needs K/128
+    assert call(_op(scale=FAKE + 2), _op(**blk)) == ALIGN
+    assert call(_op(), _op(**blk), out=2) == INVALID
+    assert call(_op(), _op(**blk), ldc=100) == INVALID
 
 
 def test_gemm_validation(lib):
