@@ -380,9 +380,12 @@ def main():
 
     # ---------------- end to end: host buffers in, results back, every step
     # Each step's inputs are copied host -> device from pinned memory and all
-    # of its outputs device -> host, inside the timed region.  Two device
+    # of its outputs device -> host, inside the timed region.  Three device
     # buffer sets let step i+1's inputs arrive and step i-1's outputs leave
-    # while step i computes (copy engines and SMs work concurrently).
+    # while step i computes (copy engines and SMs work concurrently); with
+    # two sets a step's input copy would wait for the output copy of the
+    # step before last, and the chain copy-in -> compute -> copy-out would
+    # set the period instead of the copy bandwidth.
     e2e = None
     if not args.no_e2e:
         host_in = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in step.inp.items()}
@@ -390,30 +393,33 @@ def main():
             host_in[k].copy_(v)
         host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
                     for k, v in step.out.items()}
-        sets = [step, Step(torch, fp8hg, workloads, dev, seed_offset=rank)]
+        n_sets = 3
+        sets = [step] + [Step(torch, fp8hg, workloads, dev, seed_offset=rank)
+                         for _ in range(n_sets - 1)]
         s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-        ke = max(4, min(args.steps, 12))
-        sets[1].run()
+        ke = max(4, min(args.steps, 30))
+        for st_ in sets[1:]:
+            st_.run()
         barrier()
-        freed = [None, None]  # event: buffer set's outputs copied back
+        freed = [None] * n_sets  # event: buffer set's outputs copied back
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.current_stream().wait_stream(s_in)
         a.record()
         for st_ in (s_in, s_cmp, s_out):
             st_.wait_event(a)
         for i in range(ke):
-            cur = sets[i % 2]
+            cur = sets[i % n_sets]
             with torch.cuda.stream(s_in):
-                if freed[i % 2] is not None:
-                    s_in.wait_event(freed[i % 2])
+                if freed[i % n_sets] is not None:
+                    s_in.wait_event(freed[i % n_sets])
                 for k, v in cur.inp.items():
                     v.copy_(host_in[k], non_blocking=True)
                 ev_in = torch.cuda.Event()
                 ev_in.record(s_in)
             with torch.cuda.stream(s_cmp):
                 s_cmp.wait_event(ev_in)
-                if freed[i % 2] is not None:
-                    s_cmp.wait_event(freed[i % 2])
+                if freed[i % n_sets] is not None:
+                    s_cmp.wait_event(freed[i % n_sets])
                 cur.run()
                 ev_done = torch.cuda.Event()
                 ev_done.record(s_cmp)
@@ -423,7 +429,7 @@ def main():
                     host_out[k].copy_(v, non_blocking=True)
                 ev_out = torch.cuda.Event()
                 ev_out.record(s_out)
-                freed[i % 2] = ev_out
+                freed[i % n_sets] = ev_out
         cs = torch.cuda.current_stream()
         for st_ in (s_in, s_cmp, s_out):
             cs.wait_stream(st_)
@@ -434,7 +440,7 @@ def main():
         e2e = {"value": replicas.job_throughput(world, N_GEMM * GEMM_FLOP, e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": step.in_bytes, "d2h_bytes_per_step": step.out_bytes,
                "ms_per_step": e_ms, "steps": ke,
-               "note": "pinned host buffers; two device buffer sets, copies overlapped with compute"}
+               "note": "pinned host buffers; three device buffer sets, copies overlapped with compute"}
         del sets
 
     cpu = None
