@@ -71,7 +71,9 @@ constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_TILE;
 constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_TILE;
 constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + 96;
 constexpr uint32_t OFF_ABORT = OFF_BAR + 100;
-constexpr uint32_t SMEM_USED = OFF_BAR + 128;
+constexpr uint32_t OFF_EPI = OFF_BAR + 128;      // 4 KB per epilogue warp: store staging
+constexpr uint32_t EPI_WARP_BYTES = 32 * 128;
+constexpr uint32_t SMEM_USED = OFF_EPI + 4 * EPI_WARP_BYTES;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
 
 enum { GRAN_ROW = 0, GRAN_1x128 = 1, GRAN_128x128 = 2, GRAN_MX32 = 3 };
@@ -176,6 +178,27 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                  "r"(d)
                  : "memory");
+}
+
+// Coalesced store of a 32-row x 128-byte piece of the output through this
+// warp's shared-memory staging area: lane l holds row l's 128 bytes; each
+// global store instruction then writes four whole 128-byte row segments
+// instead of 32 scattered 16-byte pieces.  The 16-byte chunks are
+// XOR-swizzled by row so that neither the row writes nor the column reads
+// conflict.
+__device__ __forceinline__ void store_piece(uint8_t *stage, const uint4 (&v)[8], int lane,
+                                            uint8_t *g_row0, int64_t ld_bytes) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4 *>(stage + lane * 128 + ((c ^ (lane & 7)) << 4)) = v[c];
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int idx = i * 32 + lane, r = idx >> 3, c = idx & 7;
+        *reinterpret_cast<uint4 *>(g_row0 + r * ld_bytes + c * 16) =
+            *reinterpret_cast<const uint4 *>(stage + r * 128 + ((c ^ (r & 7)) << 4));
+    }
+    __syncwarp();
 }
 
 __device__ __forceinline__ uint32_t sf_id(int gran, int kb, int j) {
@@ -344,6 +367,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp >= 4) {
         // --------------------------------------------------------- epilogue
         const int q = warp & 3;  // tensor-memory lane quarter this warp may read
+        uint8_t *stage = gbase + OFF_EPI + q * EPI_WARP_BYTES;
         uint32_t tcount = 0;
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
             int mb, nb;
@@ -353,6 +377,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!ok) break;
             ptx::tc_fence_after();
             const int64_t row = static_cast<int64_t>(mb) * BM + q * 32 + lane;
+            const int64_t row0 = static_cast<int64_t>(mb) * BM + q * 32;  // this warp's first row
             const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + ACC_COL;
             if constexpr (OUTQ) {
                 // FP8 out, one UE8M0 round-up scale per 128 columns of the row
@@ -402,11 +427,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int g = 0; g < BN / 128; ++g) {
                     const int64_t n0 = static_cast<int64_t>(nb) * BN + g * 128;
                     if (n0 >= p.N) continue;
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.c) + row * p.ldc + n0);
+                    uint4 v[8];
 #pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        dst[v] = make_uint4(codes[32 * g + 4 * v], codes[32 * g + 4 * v + 1],
-                                            codes[32 * g + 4 * v + 2], codes[32 * g + 4 * v + 3]);
+                    for (int c = 0; c < 8; ++c)
+                        v[c] = make_uint4(codes[32 * g + 4 * c], codes[32 * g + 4 * c + 1],
+                                          codes[32 * g + 4 * c + 2], codes[32 * g + 4 * c + 3]);
+                    store_piece(stage, v, lane, static_cast<uint8_t *>(p.c) + row0 * p.ldc + n0, p.ldc);
                     p.cs[row * p.ld_cs + n0 / 128] = static_cast<uint8_t>(sbyte[g]);
                 }
                 ++tcount;
@@ -417,26 +443,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // MMAs, then store while they run.
                 uint32_t packed[BN / 2];
 #pragma unroll
-                for (int chunk = 0; chunk < BN / 32; ++chunk) {
-                    uint32_t r[32];
+                for (int chunk = 0; chunk < BN / 32; chunk += 2) {
+                    // two loads in flight per wait: the drain is latency-bound
+                    uint32_t r[32], r2[32];
                     ptx::tmem_ld_32x32b_x32(taddr + chunk * 32, r);
+                    ptx::tmem_ld_32x32b_x32(taddr + chunk * 32 + 32, r2);
                     ptx::tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
+                    for (int e = 0; e < 16; ++e) {
                         packed[chunk * 16 + e] =
                             ptx::cvt_bf16x2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+                        packed[chunk * 16 + 16 + e] =
+                            ptx::cvt_bf16x2(__uint_as_float(r2[2 * e]), __uint_as_float(r2[2 * e + 1]));
+                    }
                 }
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(tempty);
 #pragma unroll
-                for (int chunk = 0; chunk < BN / 32; ++chunk) {
-                    const int64_t n0 = static_cast<int64_t>(nb) * BN + chunk * 32;
+                for (int pc = 0; pc < BN / 64; ++pc) {       // 64 BF16 columns = 128 bytes
+                    const int64_t n0 = static_cast<int64_t>(nb) * BN + pc * 64;
                     if (n0 >= p.N) continue;
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.c) + row * p.ldc + n0);
+                    uint4 v[8];
 #pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(packed[chunk * 16 + 4 * v], packed[chunk * 16 + 4 * v + 1],
-                                            packed[chunk * 16 + 4 * v + 2], packed[chunk * 16 + 4 * v + 3]);
+                    for (int c = 0; c < 8; ++c)
+                        v[c] = make_uint4(packed[pc * 32 + 4 * c], packed[pc * 32 + 4 * c + 1],
+                                          packed[pc * 32 + 4 * c + 2], packed[pc * 32 + 4 * c + 3]);
+                    store_piece(stage, v, lane,
+                                reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.c) + row0 * p.ldc + n0),
+                                p.ldc * 2);
                 }
                 ++tcount;
                 continue;
@@ -452,7 +486,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 const int64_t n0 = static_cast<int64_t>(nb) * BN + chunk * 32;
                 if (n0 >= p.N) continue;
-                if (p.out_fp32) {
+                if (p.out_fp32 && !p.accumulate) {
+                    uint4 v[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) v[c] = make_uint4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
+                    store_piece(stage, v, lane,
+                                reinterpret_cast<uint8_t *>(static_cast<float *>(p.c) + row0 * p.ldc + n0),
+                                p.ldc * 4);
+                } else if (p.out_fp32) {
                     float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.c) + row * p.ldc + n0);
 #pragma unroll
                     for (int v = 0; v < 8; ++v) {
