@@ -201,6 +201,23 @@ __device__ __forceinline__ void store_piece(uint8_t *stage, const uint4 (&v)[8],
     __syncwarp();
 }
 
+// The reverse: a 32-row x 128-byte piece of C read with whole-segment loads;
+// lane l receives row l's 128 bytes.
+__device__ __forceinline__ void load_piece(uint8_t *stage, uint4 (&v)[8], int lane,
+                                           const uint8_t *g_row0, int64_t ld_bytes) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int idx = i * 32 + lane, r = idx >> 3, c = idx & 7;
+        *reinterpret_cast<uint4 *>(stage + r * 128 + ((c ^ (r & 7)) << 4)) =
+            *reinterpret_cast<const uint4 *>(g_row0 + r * ld_bytes + c * 16);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        v[c] = *reinterpret_cast<const uint4 *>(stage + lane * 128 + ((c ^ (lane & 7)) << 4));
+    __syncwarp();
+}
+
 __device__ __forceinline__ uint32_t sf_id(int gran, int kb, int j) {
     return (gran == GRAN_1x128 || gran == GRAN_128x128) ? static_cast<uint32_t>(kb & 3)
                                                         : static_cast<uint32_t>(j);
@@ -475,53 +492,61 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ++tcount;
                 continue;
             }
+            // FP32 out, or accumulation into C: 64 columns at a time, the old
+            // values read and the new ones written as whole 128-byte row
+            // segments through the staging area; the accumulator is
+            // released after its last columns are read.
 #pragma unroll 1
-            for (int chunk = 0; chunk < BN / 32; ++chunk) {
-                uint32_t r[32];
-                ptx::tmem_ld_32x32b_x32(taddr + chunk * 32, r);
+            for (int pc = 0; pc < BN / 64; ++pc) {
+                uint32_t r0[32], r1[32];
+                ptx::tmem_ld_32x32b_x32(taddr + pc * 64, r0);
+                ptx::tmem_ld_32x32b_x32(taddr + pc * 64 + 32, r1);
                 ptx::tmem_wait_ld();
-                if (chunk == BN / 32 - 1) {
+                if (pc == BN / 64 - 1) {
                     ptx::tc_fence_before();
                     ptx::mbar_arrive(tempty);  // accumulator may be overwritten now
                 }
-                const int64_t n0 = static_cast<int64_t>(nb) * BN + chunk * 32;
+                const int64_t n0 = static_cast<int64_t>(nb) * BN + pc * 64;
                 if (n0 >= p.N) continue;
-                if (p.out_fp32 && !p.accumulate) {
-                    uint4 v[8];
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) v[c] = make_uint4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
-                    store_piece(stage, v, lane,
-                                reinterpret_cast<uint8_t *>(static_cast<float *>(p.c) + row0 * p.ldc + n0),
-                                p.ldc * 4);
-                } else if (p.out_fp32) {
-                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.c) + row * p.ldc + n0);
-#pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        float4 o = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                               __uint_as_float(r[4 * v + 2]),
-                                               __uint_as_float(r[4 * v + 3]));
+                if (p.out_fp32) {
+                    auto piece = [&](const uint32_t(&rr)[32], int64_t col) {
+                        uint8_t *g = reinterpret_cast<uint8_t *>(static_cast<float *>(p.c) + row0 * p.ldc + col);
+                        uint4 v[8];
                         if (p.accumulate) {
-                            const float4 old = dst[v];
-                            o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
+                            load_piece(stage, v, lane, g, p.ldc * 4);
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                v[c] = make_uint4(__float_as_uint(__uint_as_float(rr[4 * c]) + __uint_as_float(v[c].x)),
+                                                  __float_as_uint(__uint_as_float(rr[4 * c + 1]) + __uint_as_float(v[c].y)),
+                                                  __float_as_uint(__uint_as_float(rr[4 * c + 2]) + __uint_as_float(v[c].z)),
+                                                  __float_as_uint(__uint_as_float(rr[4 * c + 3]) + __uint_as_float(v[c].w)));
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                v[c] = make_uint4(rr[4 * c], rr[4 * c + 1], rr[4 * c + 2], rr[4 * c + 3]);
                         }
-                        dst[v] = o;
-                    }
+                        store_piece(stage, v, lane, g, p.ldc * 4);
+                    };
+                    piece(r0, n0);
+                    piece(r1, n0 + 32);
                 } else {
                     // BF16 with accumulation: add in FP32, round once
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.c) + row * p.ldc + n0);
+                    uint8_t *g = reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.c) + row0 * p.ldc + n0);
+                    uint4 v[8];
+                    load_piece(stage, v, lane, g, p.ldc * 2);
+                    auto add8 = [](const uint32_t *f32, const uint4 &old) {
+                        return make_uint4(
+                            ptx::cvt_bf16x2(__uint_as_float(f32[0]) + bf16_lo(old.x), __uint_as_float(f32[1]) + bf16_hi(old.x)),
+                            ptx::cvt_bf16x2(__uint_as_float(f32[2]) + bf16_lo(old.y), __uint_as_float(f32[3]) + bf16_hi(old.y)),
+                            ptx::cvt_bf16x2(__uint_as_float(f32[4]) + bf16_lo(old.z), __uint_as_float(f32[5]) + bf16_hi(old.z)),
+                            ptx::cvt_bf16x2(__uint_as_float(f32[6]) + bf16_lo(old.w), __uint_as_float(f32[7]) + bf16_hi(old.w)));
+                    };
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        float f[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(r[8 * v + e]);
-                        const uint4 old = dst[v];
-                        f[0] += bf16_lo(old.x); f[1] += bf16_hi(old.x);
-                        f[2] += bf16_lo(old.y); f[3] += bf16_hi(old.y);
-                        f[4] += bf16_lo(old.z); f[5] += bf16_hi(old.z);
-                        f[6] += bf16_lo(old.w); f[7] += bf16_hi(old.w);
-                        dst[v] = make_uint4(ptx::cvt_bf16x2(f[0], f[1]), ptx::cvt_bf16x2(f[2], f[3]),
-                                            ptx::cvt_bf16x2(f[4], f[5]), ptx::cvt_bf16x2(f[6], f[7]));
+                    for (int c = 0; c < 4; ++c) {
+                        v[c] = add8(r0 + 8 * c, v[c]);
+                        v[c + 4] = add8(r1 + 8 * c, v[c + 4]);
                     }
+                    store_piece(stage, v, lane, g, p.ldc * 2);
                 }
             }
             ++tcount;
