@@ -629,16 +629,31 @@ __global__ void __launch_bounds__(256) k_quant_block128(const uint16_t *__restri
         if constexpr (TRANS) gs.store(st, cb * ld_st + rb);
     }
     if constexpr (TRANS) {
+        // The transposed block is assembled in shared memory (8-byte units
+        // XOR-swizzled by row group) and written as whole 128-byte rows; each
+        // thread's own transposed 8x8 would otherwise go out as 8-byte pieces
+        // scattered over 8 rows.
+        __shared__ __align__(16) uint8_t tile_t[128 * 128];
         uint32_t lo03[4], lo47[4], hi03[4], hi47[4];
         transpose4x4(o[0].x, o[1].x, o[2].x, o[3].x, lo03);
         transpose4x4(o[4].x, o[5].x, o[6].x, o[7].x, lo47);
         transpose4x4(o[0].y, o[1].y, o[2].y, o[3].y, hi03);
         transpose4x4(o[4].y, o[5].y, o[6].y, o[7].y, hi47);
-        uint8_t *qtb = qt + c_first * ld_qt + r_first;
+        // output row csub*8 + j of the tile, 8-byte unit rsub (tokens rsub*8..+7)
+        const int unit = rsub ^ csub;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            *reinterpret_cast<uint2 *>(qtb + j * ld_qt) = make_uint2(lo03[j], lo47[j]);
-            *reinterpret_cast<uint2 *>(qtb + (j + 4) * ld_qt) = make_uint2(hi03[j], hi47[j]);
+            *reinterpret_cast<uint2 *>(tile_t + (csub * 8 + j) * 128 + unit * 8) = make_uint2(lo03[j], lo47[j]);
+            *reinterpret_cast<uint2 *>(tile_t + (csub * 8 + j + 4) * 128 + unit * 8) = make_uint2(hi03[j], hi47[j]);
+        }
+        __syncthreads();
+        const int64_t r0 = rb * 128, c0 = cb * 128;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int idx = tid + 256 * i, row = idx >> 3, c16 = idx & 7, g = row >> 3;
+            const uint2 a = *reinterpret_cast<const uint2 *>(tile_t + row * 128 + ((2 * c16) ^ g) * 8);
+            const uint2 b = *reinterpret_cast<const uint2 *>(tile_t + row * 128 + ((2 * c16 + 1) ^ g) * 8);
+            *reinterpret_cast<uint4 *>(qt + (c0 + row) * ld_qt + r0 + c16 * 16) = make_uint4(a.x, a.y, b.x, b.y);
         }
     }
 }
@@ -685,22 +700,38 @@ template <int FMT, int SM>
 cudaError_t launch_row_regs(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, uint8_t *q,
                        int64_t ld_q, uint8_t *s, int64_t ld_s, cudaStream_t stream) {
     const int nvec = static_cast<int>(cols / 8);
-    // choose NV (vectors per thread) and T (threads) so that T*NV covers the
-    // row with the least idle slots, T <= 512
-    const int nvs[5] = {1, 2, 4, 8, 16};
+    // Vectors per thread NV and threads T (T * NV covers the row, T <= 512):
+    // the largest NV that keeps at least 96 threads per row and wastes at
+    // most an eighth of the CTA's slots (fewer threads per row: more rows
+    // resident per SM, more bytes in flight); failing that, the least waste.
+    const int nvs[5] = {16, 8, 4, 2, 1};
     int best_nv = -1, best_t = 0;
-    int64_t best_waste = -1;
     for (int k = 0; k < 5; ++k) {
         const int nv = nvs[k];
         int t = (nvec + nv - 1) / nv;
         t = ((t + 31) / 32) * 32;
         if (t > 512) continue;
-        if (t < 64 && nv > 1) continue;
+        if (t < 96 && nv > 1) continue;
         const int64_t waste = static_cast<int64_t>(t) * nv - nvec;
-        if (best_nv < 0 || waste < best_waste) {
+        if (waste <= nvec / 8) {
             best_nv = nv;
             best_t = t;
-            best_waste = waste;
+            break;
+        }
+    }
+    if (best_nv < 0) {
+        int64_t best_waste = -1;
+        for (int k = 0; k < 5; ++k) {
+            const int nv = nvs[k];
+            int t = (nvec + nv - 1) / nv;
+            t = ((t + 31) / 32) * 32;
+            if (t > 512) continue;
+            const int64_t waste = static_cast<int64_t>(t) * nv - nvec;
+            if (best_nv < 0 || waste < best_waste) {
+                best_nv = nv;
+                best_t = t;
+                best_waste = waste;
+            }
         }
     }
     const dim3 grid(static_cast<unsigned>(rows));
