@@ -755,10 +755,11 @@ cudaError_t launch_row(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld
     const int nvec = static_cast<int>(cols / 8);
     const int64_t row_bytes = cols * 2;
     if (row_bytes <= 8192) return launch_row_regs<FMT, SM>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream);
-    // Rows up to ~50 KB: up to 4 CTAs per SM, so that one CTA's per-row
-    // synchronisation overlaps the others' work; each CTA keeps at least 4
-    // (and at most 8) rows in flight, ~200 KB per SM in total.
-    int64_t per_sm = kRowSmemBudget / (4 * row_bytes);
+    // Several CTAs per SM (up to 4, at least 2 row slots each, at most 8),
+    // ~200 KB of rows per SM in total: one CTA's per-row synchronisation then
+    // overlaps the others' work.  For 37 KB rows two CTAs with two slots
+    // each beat one CTA with five (6.2 vs 5.5 TB/s).
+    int64_t per_sm = kRowSmemBudget / (2 * row_bytes);
     const int ctas_per_sm = static_cast<int>(per_sm < 1 ? 1 : (per_sm > 4 ? 4 : per_sm));
     int nslots = static_cast<int>(kRowSmemBudget / ctas_per_sm / row_bytes);
     if (nslots > kMaxRowSlots) nslots = kMaxRowSlots;

@@ -26,6 +26,11 @@ kernel, and prints the mean launch time from CUDA events.  Cases:
   mx32_mon   the same with the clamp monitor's counts
   requant    stored per-token FP8 codes of H [M, 18944] -> 1x128 along the
              tokens, transposed (the weight-gradient operand)
+  sweep      quantizer bandwidth for BF16 [R, 4096] tensors, R = 128 * 4^i
+             (1 MB to 4 GB), per token, 1x128 and 128x128, with L2 flushed
+             before every timed launch (and L2-warm for tensors <= 64 MB);
+             then the down-projection GEMM at M = 4096, 16384, 65536.  One
+             JSON line per point (--m is ignored).
 """
 from __future__ import annotations
 
@@ -44,13 +49,15 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("case", choices=["gemm", "gemm_gate", "gemm_gate_q", "gemm_gate_f32s", "gemm_f32s",
                                      "quant_row_f32s", "wgrad", "quant_row", "quant_1x128", "quant_t", "block128",
-                                     "mx32", "mx32_mon", "requant"])
+                                     "mx32", "mx32_mon", "requant", "sweep"])
     ap.add_argument("--m", type=int, default=4096)
     ap.add_argument("--warmup", type=int, default=2)
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
     fp8hg.load_library()
     dev = torch.device("cuda", 0)
+    if args.case == "sweep":
+        return sweep(dev, max(args.iters, 3))
     M = args.m
     mk = lambda kind, r, c, n: workloads.make_tensor(kind, r, c, 4, n, device=dev)
     E4 = fp8hg.E4M3
@@ -144,6 +151,72 @@ def main():
     rate = work / (ms * 1e-3) / (1e12 if unit == "flop" else 1e9)
     print(json.dumps({"case": args.case, "m": M, "ms": ms,
                       ("tflops" if unit == "flop" else "gbs"): rate}))
+
+
+def _time(fn, iters, flush=None):
+    """Mean CUDA-event time of fn over iters launches (ms); flush() runs
+    untimed before each launch when given."""
+    total = 0.0
+    for _ in range(iters):
+        if flush is not None:
+            flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        total += a.elapsed_time(b)
+    return total / iters
+
+
+def sweep(dev, iters):
+    E4 = fp8hg.E4M3
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    scratch = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    flush = lambda: scratch.fill_(1)
+    for i in range(7):
+        R, C = 128 * 4 ** i, 4096
+        x = workloads.make_tensor("act", R, C, 4, "sweep", device=dev)
+        outs = {"token": fp8hg.alloc_token(R, C, 0, E4, False, dev),
+                "1x128": fp8hg.alloc_token(R, C, 128, E4, False, dev),
+                "128x128": fp8hg.alloc_block128(R, C, E4, False, dev)[0]}
+        fns = {"token": lambda: fp8hg.fp8_quant_token(x, 0, E4, out=outs["token"]),
+               "1x128": lambda: fp8hg.fp8_quant_token(x, 128, E4, out=outs["1x128"]),
+               "128x128": lambda: fp8hg.fp8_quant_block128(x, E4, out=outs["128x128"])}
+        groups = {"token": R, "1x128": R * C / 128, "128x128": R * C / 16384}
+        for g, fn in fns.items():
+            fn()
+            torch.cuda.synchronize()
+            nbytes = 3.0 * R * C + groups[g]
+            line = {"case": "sweep_quant", "gran": g, "rows": R, "cols": C,
+                    "tensor_mb": 2.0 * R * C / 2 ** 20, "bytes": nbytes}
+            ms = _time(fn, iters, flush)
+            line.update(ms_flushed=ms, gbs_flushed=nbytes / ms / 1e6)
+            if 2 * R * C <= 64 * 2 ** 20:
+                ms_w = _time(fn, iters)
+                line.update(ms_l2warm=ms_w, gbs_l2warm=nbytes / ms_w / 1e6)
+            print(json.dumps(line), flush=True)
+        del x, outs, fns
+        torch.cuda.empty_cache()
+    assert fp8hg.fp8hg_get_device_error() == 0
+    w = workloads.make_tensor("weight", HID, MLP, 4, "W_down", device=dev)
+    b = fp8hg.fp8_quant_block128(w, E4)
+    for M in (4096, 16384, 65536):
+        h = workloads.make_tensor("act", M, MLP, 4, "H", device=dev)
+        a = fp8hg.fp8_quant_token(h, 0, E4)
+        del h
+        out = torch.empty((M, HID), dtype=torch.bfloat16, device=dev)
+        fn = lambda: fp8hg.fp8_gemm_scaled(fp8hg.FPROP, a, b, out=out)
+        fn()
+        torch.cuda.synchronize()
+        ms = _time(fn, iters, flush)
+        print(json.dumps({"case": "sweep_gemm_down", "m": M, "k": MLP, "n": HID, "ms": ms,
+                          "tflops": 2.0 * M * HID * MLP / ms / 1e9}), flush=True)
+        del a, out
+        torch.cuda.empty_cache()
+    status = fp8hg.fp8hg_get_device_error()
+    if status != 0:
+        raise SystemExit(f"device error {fp8hg.fp8hg_status_str(status)}")
 
 
 if __name__ == "__main__":
