@@ -129,17 +129,22 @@ __global__ void __launch_bounds__(kRowThreads) k_quant_row(const uint16_t *__res
 
 // Short rows (up to 8 KB): one CTA per row, the row kept in registers between
 // the amax and the cast; many small CTAs keep the memory system busy.
-template <int FMT, int NV, int SM>
+// GV = 0: one scale for the whole row (per token).  GV = 16 (1x128) or 4
+// (MX 32): one scale per group of GV consecutive 16-byte vectors; thread tid
+// holds vectors tid + i * blockDim.x, so a group is GV consecutive lanes
+// (blockDim.x is a multiple of 32) and is reduced with lane shuffles.
+template <int FMT, int NV, int SM, int GV>
 __global__ void __launch_bounds__(512) k_quant_row_regs(const uint16_t *__restrict__ x, int nvec,
                                                         int64_t ld_x, uint8_t *__restrict__ q,
-                                                   int64_t ld_q, uint8_t *__restrict__ s,
-                                                   int64_t ld_s) {
+                                                        int64_t ld_q, uint8_t *__restrict__ s,
+                                                        int64_t ld_s) {
     __shared__ uint32_t red[16];
     __shared__ uint32_t bcast;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nwarps = blockDim.x >> 5;
     const int64_t row = blockIdx.x;
     const uint4 *xr = reinterpret_cast<const uint4 *>(x + row * ld_x);
+    uint2 *qr = reinterpret_cast<uint2 *>(q + row * ld_q);
     uint4 v[NV];
     uint32_t m = 0;
 #pragma unroll
@@ -149,6 +154,26 @@ __global__ void __launch_bounds__(512) k_quant_row_regs(const uint16_t *__restri
             v[i] = ptx::ld_stream_v4(xr + c);
             m = max(m, bf16_abs_max8(v[i]));
         }
+    }
+    uint32_t unused = 0;
+    if constexpr (GV > 0) {
+        // nvec is a multiple of GV, so a group is either wholly inside the
+        // row or wholly past it; every lane reaches the shuffles
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int c = tid + i * blockDim.x;
+            const bool ok = c < nvec;
+            uint32_t g = ok ? bf16_abs_max8(v[i]) : 0u;
+#pragma unroll
+            for (int o = GV / 2; o > 0; o >>= 1) g = max(g, __shfl_xor_sync(0xFFFFFFFFu, g, o));
+            if (ok) {
+                const GroupScale<FMT, SM> gs(g);
+                qr[c] = gs.nan ? make_uint2(kNanCodes, kNanCodes)
+                               : quant8<FMT, false>(v[i], gs.mul, unused);
+                if ((tid % GV) == 0) gs.store(s, row * ld_s + c / GV);
+            }
+        }
+        return;
     }
     m = __reduce_max_sync(0xFFFFFFFFu, m);
     if (lane == 0) red[warp] = m;
@@ -160,8 +185,6 @@ __global__ void __launch_bounds__(512) k_quant_row_regs(const uint16_t *__restri
     }
     __syncthreads();
     const GroupScale<FMT, SM> gs(bcast);
-    uint2 *qr = reinterpret_cast<uint2 *>(q + row * ld_q);
-    uint32_t unused = 0;
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
         const int c = tid + i * blockDim.x;
@@ -696,7 +719,7 @@ int resident_blocks(K kernel, int threads) {
     return n;
 }
 
-template <int FMT, int SM>
+template <int FMT, int SM, int GV = 0>
 cudaError_t launch_row_regs(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, uint8_t *q,
                        int64_t ld_q, uint8_t *s, int64_t ld_s, cudaStream_t stream) {
     const int nvec = static_cast<int>(cols / 8);
@@ -736,15 +759,16 @@ cudaError_t launch_row_regs(const uint16_t *x, int64_t rows, int64_t cols, int64
     }
     const dim3 grid(static_cast<unsigned>(rows));
     if (best_nv < 0) {
+        if (GV != 0) return cudaErrorInvalidValue;   // callers send only rows of at most 8 KB
         k_quant_row_2pass<FMT, SM><<<grid, 512, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s);
         return cudaGetLastError();
     }
     switch (best_nv) {
-    case 1: k_quant_row_regs<FMT, 1, SM><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
-    case 2: k_quant_row_regs<FMT, 2, SM><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
-    case 4: k_quant_row_regs<FMT, 4, SM><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
-    case 8: k_quant_row_regs<FMT, 8, SM><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
-    default: k_quant_row_regs<FMT, 16, SM><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
+    case 1: k_quant_row_regs<FMT, 1, SM, GV><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
+    case 2: k_quant_row_regs<FMT, 2, SM, GV><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
+    case 4: k_quant_row_regs<FMT, 4, SM, GV><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
+    case 8: k_quant_row_regs<FMT, 8, SM, GV><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
+    default: k_quant_row_regs<FMT, 16, SM, GV><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
     }
     return cudaGetLastError();
 }
@@ -843,6 +867,10 @@ cudaError_t launch_quant_token(const uint16_t *x, int64_t rows, int64_t cols, in
                    ? launch_row<FMT_E4M3, SCALE_UE8M0>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream)
                    : launch_row<FMT_E5M2, SCALE_UE8M0>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream);
     }
+    if (cols * 2 <= 8192)   // short rows: one row per CTA, held in registers
+        return fmt == FMT_E4M3
+                   ? launch_row_regs<FMT_E4M3, SCALE_UE8M0, 16>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream)
+                   : launch_row_regs<FMT_E5M2, SCALE_UE8M0, 16>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream);
     const MxCounters none{nullptr, nullptr, nullptr};
     return fmt == FMT_E4M3
                ? launch_groups<FMT_E4M3, 16, SCALE_UE8M0, false>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
@@ -863,6 +891,10 @@ cudaError_t launch_quant_mx32(const uint16_t *x, int64_t rows, int64_t cols, int
                    : launch_groups<FMT_E5M2, 4, SCALE_MX, true>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
                                                             c, stream);
     }
+    if (cols * 2 <= 8192)   // short rows: one row per CTA, held in registers
+        return fmt == FMT_E4M3
+                   ? launch_row_regs<FMT_E4M3, SCALE_MX, 4>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream)
+                   : launch_row_regs<FMT_E5M2, SCALE_MX, 4>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream);
     return fmt == FMT_E4M3
                ? launch_groups<FMT_E4M3, 4, SCALE_MX, false>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
                                                          c, stream)
@@ -968,6 +1000,10 @@ cudaError_t launch_quant_token_f32s(const uint16_t *x, int64_t rows, int64_t col
         return fmt == FMT_E4M3
                    ? launch_row<FMT_E4M3, SCALE_F32>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream)
                    : launch_row<FMT_E5M2, SCALE_F32>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream);
+    if (cols * 2 <= 8192)
+        return fmt == FMT_E4M3
+                   ? launch_row_regs<FMT_E4M3, SCALE_F32, 16>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream)
+                   : launch_row_regs<FMT_E5M2, SCALE_F32, 16>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream);
     const MxCounters none{nullptr, nullptr, nullptr};
     return fmt == FMT_E4M3
                ? launch_groups<FMT_E4M3, 16, SCALE_F32, false>(x, rows, cols, ld_x, q, ld_q, s,
