@@ -23,6 +23,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -697,18 +698,21 @@ TensorMapEncodeFn tensor_map_encoder() {
 }
 
 namespace {
-int g_num_sms[64] = {0};
+// Per-device caches, filled on first use; concurrent first uses write the
+// same values.
+std::atomic<int> g_num_sms[64];
 
 int num_sms() {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) dev = 0;
-    if (g_num_sms[dev] == 0) {
-        int n = 0;
+    int n = g_num_sms[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        g_num_sms[dev] = n > 0 ? n : 1;
+        if (n <= 0) n = 1;
+        g_num_sms[dev].store(n, std::memory_order_relaxed);
     }
-    return g_num_sms[dev];
+    return n;
 }
 
 template <typename K>
@@ -796,13 +800,13 @@ cudaError_t launch_row(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) dev = 0;
-    static bool attr_set[64] = {false};   // one flag per device and instantiation
-    if (!attr_set[dev]) {
+    static std::atomic<bool> attr_set[64];   // one flag per device and instantiation
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
         const cudaError_t e = cudaFuncSetAttribute(k_quant_row<FMT, SM>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    kRowSmemBudget);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
     int64_t grid = static_cast<int64_t>(num_sms()) * ctas_per_sm;
     if (grid > rows) grid = rows;
