@@ -403,12 +403,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // tensor memory; pass 2 reads the accumulator again and casts.
                 uint32_t am[BN / 128] = {};
 #pragma unroll
-                for (int chunk = 0; chunk < BN / 32; ++chunk) {
-                    uint32_t r[32];
-                    ptx::tmem_ld_32x32b_x32(taddr + chunk * 32, r);
+                for (int g = 0; g < BN / 128; ++g) {
+                    // a whole group's four loads in flight per wait
+                    uint32_t r[4][32];
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) ptx::tmem_ld_32x32b_x32(taddr + g * 128 + c4 * 32, r[c4]);
                     ptx::tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) am[chunk / 4] = max(am[chunk / 4], r[e] & 0x7FFFFFFFu);
+                    for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) am[g] = max(am[g], r[c4][e] & 0x7FFFFFFFu);
                 }
                 float mul[BN / 128];
                 uint32_t sbyte[BN / 128];
@@ -423,20 +427,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 uint32_t codes[BN / 4];
 #pragma unroll
-                for (int chunk = 0; chunk < BN / 32; ++chunk) {
-                    uint32_t r[32];
-                    ptx::tmem_ld_32x32b_x32(taddr + chunk * 32, r);
+                for (int chunk = 0; chunk < BN / 32; chunk += 2) {
+                    uint32_t r[2][32];
+                    ptx::tmem_ld_32x32b_x32(taddr + chunk * 32, r[0]);
+                    ptx::tmem_ld_32x32b_x32(taddr + chunk * 32 + 32, r[1]);
                     ptx::tmem_wait_ld();
                     const float m = mul[chunk / 4];
                     const bool nan_group = sbyte[chunk / 4] == 0xFFu;
 #pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        const float f0 = __uint_as_float(r[4 * v]) * m, f1 = __uint_as_float(r[4 * v + 1]) * m;
-                        const float f2 = __uint_as_float(r[4 * v + 2]) * m, f3 = __uint_as_float(r[4 * v + 3]) * m;
-                        const uint32_t lo = p.fmt_c == 0 ? ptx::cvt_e4m3x2(f0, f1) : ptx::cvt_e5m2x2(f0, f1);
-                        const uint32_t hi = p.fmt_c == 0 ? ptx::cvt_e4m3x2(f2, f3) : ptx::cvt_e5m2x2(f2, f3);
-                        codes[chunk * 8 + v] = nan_group ? kNanCodes : (lo | (hi << 16));
-                    }
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            const float f0 = __uint_as_float(r[h][4 * v]) * m, f1 = __uint_as_float(r[h][4 * v + 1]) * m;
+                            const float f2 = __uint_as_float(r[h][4 * v + 2]) * m, f3 = __uint_as_float(r[h][4 * v + 3]) * m;
+                            const uint32_t lo = p.fmt_c == 0 ? ptx::cvt_e4m3x2(f0, f1) : ptx::cvt_e5m2x2(f0, f1);
+                            const uint32_t hi = p.fmt_c == 0 ? ptx::cvt_e4m3x2(f2, f3) : ptx::cvt_e5m2x2(f2, f3);
+                            codes[(chunk + h) * 8 + v] = nan_group ? kNanCodes : (lo | (hi << 16));
+                        }
                 }
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(tempty);
