@@ -567,6 +567,379 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
+// ---------------------------------------------------------- wide variant
+// Tile 256 x 224: two M = 128 MMAs per k-step share each B tile, so every
+// stage (A 32 KB + B 28 KB) feeds twice the flops of a 128 x 256 stage with
+// 1.25x the bytes: 67 instead of 96 bytes per MMA cycle, for an operand feed
+// that is bound by the latency of what it has in flight.  Both accumulators
+// (2 x 224 columns) and the scale factors (3 stages x 16 columns) fill the
+// 512 tensor-memory columns.  384 threads: warp 0 TMA producer, warp 1 MMA
+// issuer, warp 2 scale loader, warps 4-11 epilogue (two per 32-lane quarter,
+// one per accumulator).  BF16 or FP32 output, with or without accumulation.
+constexpr int WBM = 256, WBN = 224, WSTAGES = 3;
+constexpr uint32_t WA_TILE = WBM * BK, WB_TILE = WBN * BK;
+constexpr uint32_t WSF_TILE = 1024;  // 256 rows x 4 scale bytes (A, and B padded to 256)
+constexpr uint32_t WACC1 = WBN;      // second accumulator's first column
+constexpr uint32_t WSFA_COL = 2 * WBN;                 // + 8 * stage
+constexpr uint32_t WSFB_COL = 2 * WBN + 8 * WSTAGES;   // + 8 * stage
+constexpr int W_THREADS = 384;
+constexpr uint32_t WOFF_A = 0;
+constexpr uint32_t WOFF_B = WOFF_A + WSTAGES * WA_TILE;
+constexpr uint32_t WOFF_SFA = WOFF_B + WSTAGES * WB_TILE;
+constexpr uint32_t WOFF_SFB = WOFF_SFA + WSTAGES * WSF_TILE;
+constexpr uint32_t WOFF_BAR = WOFF_SFB + WSTAGES * WSF_TILE;
+constexpr uint32_t WOFF_TMEM_SLOT = WOFF_BAR + 96;
+constexpr uint32_t WOFF_ABORT = WOFF_BAR + 100;
+constexpr uint32_t WOFF_EPI = WOFF_BAR + 128;
+constexpr uint32_t W_SMEM_BYTES = WOFF_EPI + 8 * EPI_WARP_BYTES + 1024;
+static_assert(WSFB_COL + 8 * WSTAGES <= TMEM_COLS, "tensor memory overflow");
+static_assert(W_SMEM_BYTES <= 232448, "shared memory overflow");
+
+struct WScaleGroup {
+    uint32_t a[8][4];
+    uint32_t b[7][4];
+};
+
+template <int G>
+__device__ __forceinline__ void load_group_wide(WScaleGroup &g, const KParams &p, int tile, int grp,
+                                                int lane) {
+    int mb, nb;
+    tile_coords(tile, p.num_mb, p.num_nb, mb, nb);
+#pragma unroll
+    for (int a = 0; a < 8; ++a) {
+        const int64_t m = static_cast<int64_t>(mb) * WBM + 32 * a + lane;
+        load_row_scales<G>(p.sa, p.ld_sa, p.gran_a, m, grp, p.nk, true, g.a[a]);
+    }
+#pragma unroll
+    for (int h = 0; h < 7; ++h) {
+        const int64_t n = static_cast<int64_t>(nb) * WBN + 32 * h + lane;
+        load_row_scales<G>(p.sb, p.ld_sb, p.gran_b, n, grp, p.nk, n < p.N, g.b[h]);
+    }
+}
+
+// Half piece: 32 rows x 64 bytes through the staging area (lane l holds row
+// l's four 16-byte chunks).
+__device__ __forceinline__ void store_piece64(uint8_t *stage, const uint4 (&v)[4], int lane,
+                                              uint8_t *g_row0, int64_t ld_bytes) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4 *>(stage + lane * 128 + ((c ^ (lane & 7)) << 4)) = v[c];
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int idx = i * 32 + lane, r = idx >> 2, c = idx & 3;
+        *reinterpret_cast<uint4 *>(g_row0 + r * ld_bytes + c * 16) =
+            *reinterpret_cast<const uint4 *>(stage + r * 128 + ((c ^ (r & 7)) << 4));
+    }
+    __syncwarp();
+}
+
+__device__ __forceinline__ void load_piece64(uint8_t *stage, uint4 (&v)[4], int lane,
+                                             const uint8_t *g_row0, int64_t ld_bytes) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int idx = i * 32 + lane, r = idx >> 2, c = idx & 3;
+        *reinterpret_cast<uint4 *>(stage + r * 128 + ((c ^ (r & 7)) << 4)) =
+            *reinterpret_cast<const uint4 *>(g_row0 + r * ld_bytes + c * 16);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        v[c] = *reinterpret_cast<const uint4 *>(stage + lane * 128 + ((c ^ (lane & 7)) << 4));
+    __syncwarp();
+}
+
+template <int G>
+__global__ void __launch_bounds__(W_THREADS, 1)
+    k_gemm_wide(const __grid_constant__ CUtensorMap tmap_a,
+                const __grid_constant__ CUtensorMap tmap_b, const KParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    const uint32_t sA = base + WOFF_A, sB = base + WOFF_B;
+    const uint32_t sSFA = base + WOFF_SFA, sSFB = base + WOFF_SFB, sBAR = base + WOFF_BAR;
+    const uint32_t tfull = sBAR + 64, tempty = sBAR + 72, drain = sBAR + 80;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + WOFF_TMEM_SLOT);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + WOFF_ABORT);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t limit = p.wait_limit_ns;
+    const uint64_t drain_limit = 2000000ull;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < WSTAGES; ++s) {
+            ptx::mbar_init(sBAR + 8 * s, 1 + 32);  // TMA expect_tx + the scale warp's lanes
+            ptx::mbar_init(sBAR + 32 + 8 * s, 1);  // tcgen05.commit
+        }
+        ptx::mbar_init(tfull, 1);
+        ptx::mbar_init(tempty, 256);
+        ptx::mbar_init(drain, 1);
+        *abort_flag = 0u;
+        ptx::fence_mbar_init();
+        ptx::prefetch_tmap(&tmap_a);
+        ptx::prefetch_tmap(&tmap_b);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+            int mb, nb;
+            tile_coords(tile, p.num_mb, p.num_nb, mb, nb);
+            for (int kb = 0; kb < p.nk; ++kb) {
+                const uint32_t s = it % WSTAGES, ph = (it / WSTAGES) & 1u;
+                ok = wait_phase(sBAR + 32 + 8 * s, ph ^ 1u, limit, abort_flag, p.err, WHO_PRODUCER);
+                ok = __all_sync(0xFFFFFFFFu, ok);
+                if (!ok) break;
+                if (lane == 0) {
+                    ptx::mbar_arrive_expect_tx(sBAR + 8 * s, WA_TILE + WB_TILE);
+                    ptx::tma_load_2d(sA + s * WA_TILE, &tmap_a, sBAR + 8 * s, kb * BK, mb * WBM);
+                    ptx::tma_load_2d(sB + s * WB_TILE, &tmap_b, sBAR + 8 * s, kb * BK, nb * WBN);
+                }
+                __syncwarp();
+                ++it;
+            }
+        }
+        const uint32_t nd = it < static_cast<uint32_t>(WSTAGES) ? it : static_cast<uint32_t>(WSTAGES);
+        for (uint32_t i = it - nd; i < it; ++i)
+            wait_phase(sBAR + 8 * (i % WSTAGES), (i / WSTAGES) & 1u, drain_limit, abort_flag, p.err,
+                       WHO_PRODUCER, false);
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        uint32_t it = 0, tcount = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+            ok = wait_phase(tempty, (tcount & 1u) ^ 1u, limit, abort_flag, p.err, WHO_MMA);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            for (int kb = 0; kb < p.nk; ++kb) {
+                const uint32_t s = it % WSTAGES, ph = (it / WSTAGES) & 1u;
+                ok = wait_phase(sBAR + 8 * s, ph, limit, abort_flag, p.err, WHO_MMA);
+                ok = __all_sync(0xFFFFFFFFu, ok);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t tsfa = tmem + WSFA_COL + 8 * s;
+                    const uint32_t tsfb = tmem + WSFB_COL + 8 * s;
+                    ptx::tc_cp_32x128b_warpx4(tsfa, desc_sf(sSFA + s * WSF_TILE));
+                    ptx::tc_cp_32x128b_warpx4(tsfa + 4, desc_sf(sSFA + s * WSF_TILE + 512));
+                    ptx::tc_cp_32x128b_warpx4(tsfb, desc_sf(sSFB + s * WSF_TILE));
+                    ptx::tc_cp_32x128b_warpx4(tsfb + 4, desc_sf(sSFB + s * WSF_TILE + 512));
+                    const uint64_t ad0 = desc_sw128(sA + s * WA_TILE);
+                    const uint64_t ad1 = desc_sw128(sA + s * WA_TILE + WA_TILE / 2);
+                    const uint64_t bd = desc_sw128(sB + s * WB_TILE);
+#pragma unroll
+                    for (int j = 0; j < BK / 32; ++j) {
+                        const uint32_t idesc = p.idesc | (sf_id(p.gran_a, kb, j) << 29) |
+                                               (sf_id(p.gran_b, kb, j) << 4);
+                        const uint32_t acc = (kb | j) != 0 ? 1u : 0u;
+                        ptx::tc_mma_mxf8(tmem, ad0 + 2 * j, bd + 2 * j, idesc, tsfa, tsfb, acc);
+                        ptx::tc_mma_mxf8(tmem + WACC1, ad1 + 2 * j, bd + 2 * j, idesc, tsfa + 4, tsfb, acc);
+                    }
+                    ptx::tc_commit(sBAR + 32 + 8 * s);
+                }
+                __syncwarp();
+                ++it;
+            }
+            if (!ok) break;
+            if (lane == 0) ptx::tc_commit(tfull);
+            __syncwarp();
+            ++tcount;
+        }
+        if (lane == 0) ptx::tc_commit(drain);
+        __syncwarp();
+        wait_phase(drain, 0u, drain_limit, abort_flag, p.err, WHO_MMA, false);
+    } else if (warp == 2) {
+        // ------------------------------------------------------ scale loader
+        uint32_t it = 0;
+        bool ok = true;
+        const int ngrp = (p.nk + G - 1) / G;
+        int tile = blockIdx.x, grp = 0;
+        WScaleGroup cur, nxt;
+        if (tile < p.num_tiles) load_group_wide<G>(cur, p, tile, 0, lane);
+        while (tile < p.num_tiles && ok) {
+            int ntile = tile, ngrp_next = grp + 1;
+            if (ngrp_next == ngrp) {
+                ntile += gridDim.x;
+                ngrp_next = 0;
+            }
+            if (ntile < p.num_tiles) load_group_wide<G>(nxt, p, ntile, ngrp_next, lane);
+#pragma unroll
+            for (int t = 0; t < G; ++t) {
+                if (G * grp + t >= p.nk || !ok) break;
+                constexpr int kWordStep = G / 4;
+                const int wi = t / kWordStep;
+                const uint32_t s = it % WSTAGES, ph = (it / WSTAGES) & 1u;
+                ok = wait_phase(sBAR + 32 + 8 * s, ph ^ 1u, limit, abort_flag, p.err, WHO_SCALES);
+                ok = __all_sync(0xFFFFFFFFu, ok);
+                if (!ok) break;
+                const uint32_t dA = sSFA + s * WSF_TILE + lane * 16;
+                const uint32_t dB = sSFB + s * WSF_TILE + lane * 16;
+                st_shared_v4(dA, cur.a[0][wi], cur.a[1][wi], cur.a[2][wi], cur.a[3][wi]);
+                st_shared_v4(dA + 512, cur.a[4][wi], cur.a[5][wi], cur.a[6][wi], cur.a[7][wi]);
+                st_shared_v4(dB, cur.b[0][wi], cur.b[1][wi], cur.b[2][wi], cur.b[3][wi]);
+                st_shared_v4(dB + 512, cur.b[4][wi], cur.b[5][wi], cur.b[6][wi], 0x7F7F7F7Fu);
+                if (!(p.inject == 1 && it == 0)) {
+                    ptx::fence_proxy_async_smem();
+                    ptx::mbar_arrive(sBAR + 8 * s);
+                }
+                ++it;
+            }
+            cur = nxt;
+            tile = ntile;
+            grp = ngrp_next;
+        }
+    } else if (warp >= 4) {
+        // --------------------------------------------------------- epilogue
+        const int q = warp & 3, half = (warp - 4) >> 2;
+        uint8_t *stage = gbase + WOFF_EPI + (warp - 4) * EPI_WARP_BYTES;
+        uint32_t tcount = 0;
+        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+            int mb, nb;
+            tile_coords(tile, p.num_mb, p.num_nb, mb, nb);
+            bool ok = wait_phase(tfull, tcount & 1u, limit, abort_flag, p.err, WHO_EPILOGUE);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const int64_t row0 = static_cast<int64_t>(mb) * WBM + half * 128 + q * 32;
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + half * WACC1;
+            if (p.out_fp32 || p.accumulate) {
+                // FP32 out or accumulation into C: 32 columns at a time, old
+                // values read and new ones written as row
+                // segments through the staging area; the accumulator is
+                // released after its last columns are read.
+#pragma unroll 1
+                for (int chunk = 0; chunk < WBN / 32; ++chunk) {
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32(taddr + chunk * 32, r);
+                    ptx::tmem_wait_ld();
+                    if (chunk == WBN / 32 - 1) {
+                        ptx::tc_fence_before();
+                        ptx::mbar_arrive(tempty);
+                    }
+                    auto emit = [&](const uint32_t(&rr)[32], int cc) {
+                        const int64_t n0 = static_cast<int64_t>(nb) * WBN + cc * 32;
+                        if (n0 >= p.N) return;
+                        if (p.out_fp32) {
+                            uint8_t *g = reinterpret_cast<uint8_t *>(static_cast<float *>(p.c) + row0 * p.ldc + n0);
+                            uint4 v[8];
+                            if (p.accumulate) {
+                                load_piece(stage, v, lane, g, p.ldc * 4);
+#pragma unroll
+                                for (int c = 0; c < 8; ++c)
+                                    v[c] = make_uint4(__float_as_uint(__uint_as_float(rr[4 * c]) + __uint_as_float(v[c].x)),
+                                                      __float_as_uint(__uint_as_float(rr[4 * c + 1]) + __uint_as_float(v[c].y)),
+                                                      __float_as_uint(__uint_as_float(rr[4 * c + 2]) + __uint_as_float(v[c].z)),
+                                                      __float_as_uint(__uint_as_float(rr[4 * c + 3]) + __uint_as_float(v[c].w)));
+                            } else {
+#pragma unroll
+                                for (int c = 0; c < 8; ++c)
+                                    v[c] = make_uint4(rr[4 * c], rr[4 * c + 1], rr[4 * c + 2], rr[4 * c + 3]);
+                            }
+                            store_piece(stage, v, lane, g, p.ldc * 4);
+                        } else {
+                            // BF16 with accumulation: add in FP32, round once
+                            uint8_t *g = reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.c) + row0 * p.ldc + n0);
+                            uint4 v[4];
+                            load_piece64(stage, v, lane, g, p.ldc * 2);
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                v[c] = make_uint4(
+                                    ptx::cvt_bf16x2(__uint_as_float(rr[8 * c]) + bf16_lo(v[c].x),
+                                                    __uint_as_float(rr[8 * c + 1]) + bf16_hi(v[c].x)),
+                                    ptx::cvt_bf16x2(__uint_as_float(rr[8 * c + 2]) + bf16_lo(v[c].y),
+                                                    __uint_as_float(rr[8 * c + 3]) + bf16_hi(v[c].y)),
+                                    ptx::cvt_bf16x2(__uint_as_float(rr[8 * c + 4]) + bf16_lo(v[c].z),
+                                                    __uint_as_float(rr[8 * c + 5]) + bf16_hi(v[c].z)),
+                                    ptx::cvt_bf16x2(__uint_as_float(rr[8 * c + 6]) + bf16_lo(v[c].w),
+                                                    __uint_as_float(rr[8 * c + 7]) + bf16_hi(v[c].w)));
+                            }
+                            store_piece64(stage, v, lane, g, p.ldc * 2);
+                        }
+                    };
+                    emit(r, chunk);
+                }
+                ++tcount;
+                continue;
+            }
+            uint32_t packed[WBN / 2];
+#pragma unroll
+            for (int chunk = 0; chunk < WBN / 32; chunk += 2) {
+                uint32_t r[32], r2[32];
+                ptx::tmem_ld_32x32b_x32(taddr + chunk * 32, r);
+                if (chunk + 1 < WBN / 32) ptx::tmem_ld_32x32b_x32(taddr + chunk * 32 + 32, r2);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    packed[chunk * 16 + e] =
+                        ptx::cvt_bf16x2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+                if (chunk + 1 < WBN / 32) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        packed[chunk * 16 + 16 + e] =
+                            ptx::cvt_bf16x2(__uint_as_float(r2[2 * e]), __uint_as_float(r2[2 * e + 1]));
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(tempty);
+            // N is a multiple of 128 and the tile starts at a multiple of 224,
+            // so a 64-column piece can straddle N by exactly 32 columns: it is
+            // then written as a 32-column half piece.
+#pragma unroll
+            for (int pc = 0; pc < WBN / 64; ++pc) {        // three 64-column pieces
+                const int64_t n0 = static_cast<int64_t>(nb) * WBN + pc * 64;
+                if (n0 >= p.N) continue;
+                uint8_t *g = reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.c) + row0 * p.ldc + n0);
+                if (n0 + 64 <= p.N) {
+                    uint4 v[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        v[c] = make_uint4(packed[pc * 32 + 4 * c], packed[pc * 32 + 4 * c + 1],
+                                          packed[pc * 32 + 4 * c + 2], packed[pc * 32 + 4 * c + 3]);
+                    store_piece(stage, v, lane, g, p.ldc * 2);
+                } else {
+                    uint4 v[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        v[c] = make_uint4(packed[pc * 32 + 4 * c], packed[pc * 32 + 4 * c + 1],
+                                          packed[pc * 32 + 4 * c + 2], packed[pc * 32 + 4 * c + 3]);
+                    store_piece64(stage, v, lane, g, p.ldc * 2);
+                }
+            }
+            {                                               // the last 32 columns
+                const int64_t n0 = static_cast<int64_t>(nb) * WBN + 192;
+                if (n0 < p.N) {
+                    uint4 v[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        v[c] = make_uint4(packed[96 + 4 * c], packed[96 + 4 * c + 1],
+                                          packed[96 + 4 * c + 2], packed[96 + 4 * c + 3]);
+                    store_piece64(stage, v, lane,
+                                  reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.c) + row0 * p.ldc + n0),
+                                  p.ldc * 2);
+                }
+            }
+            ++tcount;
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -614,11 +987,14 @@ unsigned int *device_error_word() {
 }
 
 int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
+    // the 256 x 224 variant where M is a multiple of 256 (not for MX32 operands
+    // or the quantized epilogue)
+    const bool wide = !g.out_q && g.M % WBM == 0 && g.gran_a != GRAN_MX32;
     CUtensorMap ta, tb;
     std::memset(&ta, 0, sizeof(ta));
     std::memset(&tb, 0, sizeof(tb));
-    if (!make_tmap(&ta, g.a_codes, g.M, g.K, g.lda, BM)) return 1;
-    if (!make_tmap(&tb, g.b_codes, g.N, g.K, g.ldb, BN)) return 1;
+    if (!make_tmap(&ta, g.a_codes, g.M, g.K, g.lda, wide ? WBM : BM)) return 1;
+    if (!make_tmap(&tb, g.b_codes, g.N, g.K, g.ldb, wide ? WBN : BN)) return 1;
 
     int dev = 0;
     cudaGetDevice(&dev);
@@ -632,6 +1008,10 @@ int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
                     kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_BYTES));
                 if (e != cudaSuccess) return 2 + static_cast<int>(e);
             }
+            const cudaError_t e = cudaFuncSetAttribute(
+                k_gemm_wide<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                static_cast<int>(W_SMEM_BYTES));
+            if (e != cudaSuccess) return 2 + static_cast<int>(e);
             int n = 0;
             cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
             g_sms[dev] = n > 0 ? n : 1;
@@ -643,8 +1023,9 @@ int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
     p.M = static_cast<int>(g.M);
     p.N = static_cast<int>(g.N);
     p.nk = static_cast<int>(g.K / BK);
-    p.num_nb = static_cast<int>((g.N + BN - 1) / BN);
-    p.num_mb = static_cast<int>(g.M / BM);
+    const int tbn = wide ? WBN : BN, tbm = wide ? WBM : BM;
+    p.num_nb = static_cast<int>((g.N + tbn - 1) / tbn);
+    p.num_mb = static_cast<int>(g.M / tbm);
     p.num_tiles = p.num_mb * p.num_nb;
     p.gran_a = g.gran_a;
     p.gran_b = g.gran_b;
@@ -665,7 +1046,7 @@ int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
     // (E4M3 = 0, E5M2 = 1) in bits 7-9 / 10-12, K-major A and B, N >> 3 in
     // bits 17-22, UE8M0 scale type in bit 23, M >> 4 in bits 24-28; the
     // scale-factor byte ids (bits 4-5 for B, 29-30 for A) are set per MMA.
-    p.idesc = (1u << 23) | (static_cast<uint32_t>(BN >> 3) << 17) |
+    p.idesc = (1u << 23) | (static_cast<uint32_t>(tbn >> 3) << 17) |
               (static_cast<uint32_t>(BM >> 4) << 24) | (static_cast<uint32_t>(g.fmt_a) << 7) |
               (static_cast<uint32_t>(g.fmt_b) << 10);
     p.wait_limit_ns = g.wait_limit_ns;
@@ -674,7 +1055,9 @@ int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
     int grid = g_sms[dev];
     if (grid > p.num_tiles) grid = p.num_tiles;
     const bool mx = g.gran_a == GRAN_MX32;
-    if (g.out_q) {
+    if (wide) {
+        k_gemm_wide<16><<<grid, W_THREADS, W_SMEM_BYTES, stream>>>(ta, tb, p);
+    } else if (g.out_q) {
         if (mx) k_gemm_mxf8<4, true><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
         else k_gemm_mxf8<16, true><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
     } else {
