@@ -574,8 +574,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // that is bound by the latency of what it has in flight.  Both accumulators
 // (2 x 224 columns) and the scale factors (3 stages x 16 columns) fill the
 // 512 tensor-memory columns.  384 threads: warp 0 TMA producer, warp 1 MMA
-// issuer, warp 2 scale loader, warps 4-11 epilogue (two per 32-lane quarter,
-// one per accumulator).  BF16 or FP32 output, with or without accumulation.
+// issuer, warps 2 and 3 scale loaders (A, B), warps 4-11 epilogue (two per
+// 32-lane quarter, one per accumulator).  BF16 or FP32 output, with or without accumulation.
 constexpr int WBM = 256, WBN = 224, WSTAGES = 3;
 constexpr uint32_t WA_TILE = WBM * BK, WB_TILE = WBN * BK;
 constexpr uint32_t WSF_TILE = 1024;  // 256 rows x 4 scale bytes (A, and B padded to 256)
@@ -595,25 +595,26 @@ constexpr uint32_t W_SMEM_BYTES = WOFF_EPI + 8 * EPI_WARP_BYTES + 1024;
 static_assert(WSFB_COL + 8 * WSTAGES <= TMEM_COLS, "tensor memory overflow");
 static_assert(W_SMEM_BYTES <= 232448, "shared memory overflow");
 
-struct WScaleGroup {
-    uint32_t a[8][4];
-    uint32_t b[7][4];
+// One lane's scale words for one operand of a tile: A rows 32a + lane
+// (a < 8, 256 rows) or B rows 32h + lane (h < 7, 224 rows; row 8 padding).
+struct WScaleRows {
+    uint32_t w[8][4];
 };
 
-template <int G>
-__device__ __forceinline__ void load_group_wide(WScaleGroup &g, const KParams &p, int tile, int grp,
-                                                int lane) {
+template <int G, bool IS_A>
+__device__ __forceinline__ void load_rows_wide(WScaleRows &g, const KParams &p, int tile, int grp,
+                                               int lane) {
     int mb, nb;
     tile_coords(tile, p.num_mb, p.num_nb, mb, nb);
 #pragma unroll
-    for (int a = 0; a < 8; ++a) {
-        const int64_t m = static_cast<int64_t>(mb) * WBM + 32 * a + lane;
-        load_row_scales<G>(p.sa, p.ld_sa, p.gran_a, m, grp, p.nk, true, g.a[a]);
-    }
-#pragma unroll
-    for (int h = 0; h < 7; ++h) {
-        const int64_t n = static_cast<int64_t>(nb) * WBN + 32 * h + lane;
-        load_row_scales<G>(p.sb, p.ld_sb, p.gran_b, n, grp, p.nk, n < p.N, g.b[h]);
+    for (int h = 0; h < 8; ++h) {
+        if constexpr (IS_A) {
+            const int64_t m = static_cast<int64_t>(mb) * WBM + 32 * h + lane;
+            load_row_scales<G>(p.sa, p.ld_sa, p.gran_a, m, grp, p.nk, true, g.w[h]);
+        } else {
+            const int64_t n = static_cast<int64_t>(nb) * WBN + 32 * h + lane;
+            load_row_scales<G>(p.sb, p.ld_sb, p.gran_b, n, grp, p.nk, h < 7 && n < p.N, g.w[h]);
+        }
     }
 }
 
@@ -668,7 +669,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < WSTAGES; ++s) {
-            ptx::mbar_init(sBAR + 8 * s, 1 + 32);  // TMA expect_tx + the scale warp's lanes
+            ptx::mbar_init(sBAR + 8 * s, 1 + 64);  // TMA expect_tx + both scale warps' lanes
             ptx::mbar_init(sBAR + 32 + 8 * s, 1);  // tcgen05.commit
         }
         ptx::mbar_init(tfull, 1);
@@ -759,21 +760,30 @@ __global__ void __launch_bounds__(W_THREADS, 1)
         if (lane == 0) ptx::tc_commit(drain);
         __syncwarp();
         wait_phase(drain, 0u, drain_limit, abort_flag, p.err, WHO_MMA, false);
-    } else if (warp == 2) {
-        // ------------------------------------------------------ scale loader
+    } else if (warp == 2 || warp == 3) {
+        // ------------------------------------------------- scale loaders
+        // warp 2: A's 256 rows, warp 3: B's 224 rows (padded to 256); each
+        // keeps its rows' words for one group of G k-blocks in registers with
+        // the next group's loads in flight, and arrives on the stage.
+        const bool is_a = warp == 2;
         uint32_t it = 0;
         bool ok = true;
         const int ngrp = (p.nk + G - 1) / G;
         int tile = blockIdx.x, grp = 0;
-        WScaleGroup cur, nxt;
-        if (tile < p.num_tiles) load_group_wide<G>(cur, p, tile, 0, lane);
+        WScaleRows cur, nxt;
+        auto load = [&](WScaleRows &dst, int t, int gr) {
+            if (is_a) load_rows_wide<G, true>(dst, p, t, gr, lane);
+            else load_rows_wide<G, false>(dst, p, t, gr, lane);
+        };
+        if (tile < p.num_tiles) load(cur, tile, 0);
+        const uint32_t sbase = is_a ? sSFA : sSFB;
         while (tile < p.num_tiles && ok) {
             int ntile = tile, ngrp_next = grp + 1;
             if (ngrp_next == ngrp) {
                 ntile += gridDim.x;
                 ngrp_next = 0;
             }
-            if (ntile < p.num_tiles) load_group_wide<G>(nxt, p, ntile, ngrp_next, lane);
+            if (ntile < p.num_tiles) load(nxt, ntile, ngrp_next);
 #pragma unroll
             for (int t = 0; t < G; ++t) {
                 if (G * grp + t >= p.nk || !ok) break;
@@ -783,12 +793,9 @@ __global__ void __launch_bounds__(W_THREADS, 1)
                 ok = wait_phase(sBAR + 32 + 8 * s, ph ^ 1u, limit, abort_flag, p.err, WHO_SCALES);
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) break;
-                const uint32_t dA = sSFA + s * WSF_TILE + lane * 16;
-                const uint32_t dB = sSFB + s * WSF_TILE + lane * 16;
-                st_shared_v4(dA, cur.a[0][wi], cur.a[1][wi], cur.a[2][wi], cur.a[3][wi]);
-                st_shared_v4(dA + 512, cur.a[4][wi], cur.a[5][wi], cur.a[6][wi], cur.a[7][wi]);
-                st_shared_v4(dB, cur.b[0][wi], cur.b[1][wi], cur.b[2][wi], cur.b[3][wi]);
-                st_shared_v4(dB + 512, cur.b[4][wi], cur.b[5][wi], cur.b[6][wi], 0x7F7F7F7Fu);
+                const uint32_t d = sbase + s * WSF_TILE + lane * 16;
+                st_shared_v4(d, cur.w[0][wi], cur.w[1][wi], cur.w[2][wi], cur.w[3][wi]);
+                st_shared_v4(d + 512, cur.w[4][wi], cur.w[5][wi], cur.w[6][wi], cur.w[7][wi]);
                 if (!(p.inject == 1 && it == 0)) {
                     ptx::fence_proxy_async_smem();
                     ptx::mbar_arrive(sBAR + 8 * s);
@@ -874,21 +881,14 @@ __global__ void __launch_bounds__(W_THREADS, 1)
             }
             uint32_t packed[WBN / 2];
 #pragma unroll
-            for (int chunk = 0; chunk < WBN / 32; chunk += 2) {
-                uint32_t r[32], r2[32];
+            for (int chunk = 0; chunk < WBN / 32; ++chunk) {
+                uint32_t r[32];
                 ptx::tmem_ld_32x32b_x32(taddr + chunk * 32, r);
-                if (chunk + 1 < WBN / 32) ptx::tmem_ld_32x32b_x32(taddr + chunk * 32 + 32, r2);
                 ptx::tmem_wait_ld();
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
                     packed[chunk * 16 + e] =
                         ptx::cvt_bf16x2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
-                if (chunk + 1 < WBN / 32) {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        packed[chunk * 16 + 16 + e] =
-                            ptx::cvt_bf16x2(__uint_as_float(r2[2 * e]), __uint_as_float(r2[2 * e + 1]));
-                }
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(tempty);
