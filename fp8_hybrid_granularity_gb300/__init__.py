@@ -60,7 +60,7 @@ class Operand(ctypes.Structure):
 
 class GemmOpts(ctypes.Structure):
     _fields_ = [("wait_limit_ns", ctypes.c_uint64), ("inject_fault", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("tile", ctypes.c_int32)]
 
 
 _lib = None
@@ -383,8 +383,9 @@ def fp8_gemm_scaled_q(op: int, a: QTensor, b: QTensor, fmt: int = E4M3,
 
 def fp8_gemm_scaled(op: int, a: QTensor, b: QTensor, out=None, out_dtype=None,
                     accumulate: bool = False, wait_limit_ns: int = 0, inject_fault: int = 0,
-                    stream=None):
-    """C = A * B^T (or C += A * B^T) on block-scaled FP8 operands."""
+                    tile: int = 0, stream=None):
+    """C = A * B^T (or C += A * B^T) on block-scaled FP8 operands.  tile: 0 =
+    library's choice, 1 = 128 x 256 tiles, 2 = 256 x 224 tiles (M % 256 == 0)."""
     import torch
     if out is None:
         dt = out_dtype if out_dtype is not None else torch.bfloat16
@@ -396,8 +397,8 @@ def fp8_gemm_scaled(op: int, a: QTensor, b: QTensor, out=None, out_dtype=None,
     else:
         raise ValueError("out must be bfloat16 or float32")
     oa, ob = a.operand(), b.operand()
-    if wait_limit_ns or inject_fault:
-        opts = GemmOpts(wait_limit_ns, inject_fault, 0)
+    if wait_limit_ns or inject_fault or tile:
+        opts = GemmOpts(wait_limit_ns, inject_fault, tile)
         rc = lib().fp8_gemm_scaled_ex(op, ctypes.byref(oa), ctypes.byref(ob), _ptr(out),
                                       out.stride(0), kind, 1 if accumulate else 0,
                                       ctypes.byref(opts), _stream(stream))

@@ -106,6 +106,7 @@ int run_gemm(fp8hg::GemmArgs &g, const fp8hg_gemm_opts *opts, void *stream) {
     if (!err) return FP8HG_ERR_CUDA;
     g.wait_limit_ns = (opts && opts->wait_limit_ns) ? opts->wait_limit_ns : kDefaultWaitNs;
     g.inject_fault = opts ? opts->inject_fault : 0;
+    g.tile = opts ? opts->tile : 0;
     g.err = err;
     const int rc = fp8hg::launch_gemm_scaled(g, static_cast<cudaStream_t>(stream));
     if (rc == 1) return FP8HG_ERR_UNSUPPORTED;  // tensor map could not be encoded
@@ -221,6 +222,8 @@ int fp8_gemm_scaled_ex(int op, const fp8hg_operand *a, const fp8hg_operand *b, v
     if (ldc < b->rows) return FP8HG_ERR_INVALID_ARG;
     if (ldc % (out == FP8HG_OUT_BF16 ? 8 : 4)) return FP8HG_ERR_ALIGNMENT;
     if (opts && (opts->inject_fault < 0 || opts->inject_fault > 1)) return FP8HG_ERR_INVALID_ARG;
+    if (opts && (opts->tile < 0 || opts->tile > 2)) return FP8HG_ERR_INVALID_ARG;
+    if (opts && opts->tile == 2 && a->rows % 256) return FP8HG_ERR_UNSUPPORTED;
     g.c = c;
     g.ldc = ldc;
     g.out_fp32 = out == FP8HG_OUT_FP32;

@@ -987,15 +987,6 @@ unsigned int *device_error_word() {
 }
 
 int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
-    // the 256 x 224 variant where M is a multiple of 256 (not for MX32 operands
-    // or the quantized epilogue)
-    const bool wide = !g.out_q && g.M % WBM == 0 && g.gran_a != GRAN_MX32;
-    CUtensorMap ta, tb;
-    std::memset(&ta, 0, sizeof(ta));
-    std::memset(&tb, 0, sizeof(tb));
-    if (!make_tmap(&ta, g.a_codes, g.M, g.K, g.lda, wide ? WBM : BM)) return 1;
-    if (!make_tmap(&tb, g.b_codes, g.N, g.K, g.ldb, wide ? WBN : BN)) return 1;
-
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) dev = 0;
@@ -1008,16 +999,38 @@ int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
                     kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_BYTES));
                 if (e != cudaSuccess) return 2 + static_cast<int>(e);
             }
-            const cudaError_t e = cudaFuncSetAttribute(
-                k_gemm_wide<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                static_cast<int>(W_SMEM_BYTES));
-            if (e != cudaSuccess) return 2 + static_cast<int>(e);
+            for (auto kern : {k_gemm_wide<16>, k_gemm_wide<4>}) {
+                const cudaError_t e = cudaFuncSetAttribute(
+                    kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(W_SMEM_BYTES));
+                if (e != cudaSuccess) return 2 + static_cast<int>(e);
+            }
             int n = 0;
             cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
             g_sms[dev] = n > 0 ? n : 1;
             g_attr_set[dev] = true;
         }
     }
+    const int sms = g_sms[dev];
+
+    // The 256 x 224 variant where M is a multiple of 256 (not for the
+    // quantized epilogue, whose 1x128 groups must not straddle tiles), unless
+    // its coarser tiles fill the last wave of SMs so much worse that its
+    // ~8 % faster tiles do not make up for it.
+    bool wide = !g.out_q && g.M % WBM == 0 && g.tile != 1;
+    if (wide && g.tile != 2) {
+        auto wave_eff = [&](int64_t tiles) {
+            const int64_t waves = (tiles + sms - 1) / sms;
+            return static_cast<double>(tiles) / static_cast<double>(waves * sms);
+        };
+        const int64_t t_wide = (g.M / WBM) * ((g.N + WBN - 1) / WBN);
+        const int64_t t_std = (g.M / BM) * ((g.N + BN - 1) / BN);
+        wide = 1.08 * wave_eff(t_wide) >= wave_eff(t_std);
+    }
+    CUtensorMap ta, tb;
+    std::memset(&ta, 0, sizeof(ta));
+    std::memset(&tb, 0, sizeof(tb));
+    if (!make_tmap(&ta, g.a_codes, g.M, g.K, g.lda, wide ? WBM : BM)) return 1;
+    if (!make_tmap(&tb, g.b_codes, g.N, g.K, g.ldb, wide ? WBN : BN)) return 1;
 
     KParams p;
     p.M = static_cast<int>(g.M);
@@ -1052,11 +1065,12 @@ int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
     p.wait_limit_ns = g.wait_limit_ns;
     p.err = g.err;
 
-    int grid = g_sms[dev];
+    int grid = sms;
     if (grid > p.num_tiles) grid = p.num_tiles;
     const bool mx = g.gran_a == GRAN_MX32;
     if (wide) {
-        k_gemm_wide<16><<<grid, W_THREADS, W_SMEM_BYTES, stream>>>(ta, tb, p);
+        if (mx) k_gemm_wide<4><<<grid, W_THREADS, W_SMEM_BYTES, stream>>>(ta, tb, p);
+        else k_gemm_wide<16><<<grid, W_THREADS, W_SMEM_BYTES, stream>>>(ta, tb, p);
     } else if (g.out_q) {
         if (mx) k_gemm_mxf8<4, true><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
         else k_gemm_mxf8<16, true><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, p);

@@ -63,6 +63,7 @@ struct GemmArgs {
     int64_t ld_cs;
     uint64_t wait_limit_ns;
     int inject_fault;
+    int tile;           // 0 = choose, 1 = 128 x 256, 2 = 256 x 224
     unsigned int *err;  // device error word
 };
 

@@ -363,11 +363,15 @@ int fp8_gemm_scaled_q(int op, const fp8hg_operand *a, const fp8hg_operand *b, ui
  *                  arrival, so the first wait of the MMA warp can never
  *                  complete: a host-chosen, GPU-safe way to exercise the
  *                  timeout path in tests.
+ *   tile           0 = the library's choice.  1 = 128 x 256 tiles.  2 = 256 x 224
+ *                  tiles (two accumulators per B stage); honoured when M is a
+ *                  multiple of 256, else FP8HG_ERR_UNSUPPORTED.  The result
+ *                  does not depend on the tile beyond FP32 accumulation order.
  */
 typedef struct {
     uint64_t wait_limit_ns;
     int32_t inject_fault;
-    int32_t reserved;
+    int32_t tile;
 } fp8hg_gemm_opts;
 
 /* fp8_gemm_scaled with options (opts may be NULL = defaults). */

@@ -142,6 +142,19 @@ def test_f32s_validation(lib):
     assert call(_op(), _op(**blk), ldc=100) == INVALID
 
 
+def test_gemm_options_validation(lib):
+    g = lib.fp8_gemm_scaled_ex
+    blk = dict(gran=GRAN_128x128, lds=4)
+
+    def call(a, opts):
+        return g(0, ctypes.byref(a), ctypes.byref(_op(**blk)), FAKE, 256, 0, 0,
+                 ctypes.byref(opts), None)
+
+    assert call(_op(), fp8hg.GemmOpts(0, 0, 3)) == INVALID        # tile selector
+    assert call(_op(), fp8hg.GemmOpts(0, 2, 0)) == INVALID        # inject_fault
+    assert call(_op(rows=128), fp8hg.GemmOpts(0, 0, 2)) == UNSUP  # 256-row tiles, M = 128
+
+
 def test_gemm_validation(lib):
     g = lib.fp8_gemm_scaled
     C = FAKE

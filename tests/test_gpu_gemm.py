@@ -42,77 +42,95 @@ CASES = [
 ]
 
 
+TILES = [1, 2]   # 128 x 256 tiles; 256 x 224 tiles with two accumulators
+
+
 @pytest.mark.parametrize("case", CASES, ids=lambda c: f"op{c[0]}-{c[1][0]}{c[1][1]}-{c[2][0]}{c[2][1]}-{c[3]}x{c[4]}x{c[5]}")
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
-def test_gemm_matches_oracle(cuda_lib, case, out_dtype):
+@pytest.mark.parametrize("tile", TILES)
+def test_gemm_matches_oracle(cuda_lib, case, out_dtype, tile):
     op, (ga, fa, ka), (gb, fb, kb), M, N, K = case
+    if tile == 2 and M % 256:
+        pytest.skip("256-row tiles need M % 256 == 0")
     qa, sa = _operand(ka, M, K, ga, fa, M + K)
     qb, sb = _operand(kb, N, K, gb, fb, N + 3 * K)
     c = fp8hg.fp8_gemm_scaled(op, to_qtensor(qa, sa, fa, ga), to_qtensor(qb, sb, fb, gb),
-                              out_dtype=out_dtype)
+                              out_dtype=out_dtype, tile=tile)
     assert fp8hg.fp8hg_get_device_error() == 0
     c_ref, s_abs = _ref(qa, sa, ga, fa, qb, sb, gb, fb)
     check_gemm(c.float().cpu().numpy(), c_ref, s_abs, "gemm")
 
 
-def test_gemm_accumulate(cuda_lib):
-    M, N, K = 256, 256, 512
+@pytest.mark.parametrize("tile", TILES)
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_gemm_accumulate(cuda_lib, tile, out_dtype):
+    """C = A1 B^T, then C += A2 B^T; N = 384 leaves a ragged last tile for
+    both tile shapes (384 = 256 + 128 = 224 + 160)."""
+    M, N, K = 256, 384, 512
     qa, sa = _operand("act", M, K, GRAN_1x128, E4M3, 1)
     qb, sb = _operand("weight", N, K, GRAN_128x128, E4M3, 2)
     qa2, sa2 = _operand("act", M, K, GRAN_1x128, E4M3, 3)
     a, b, a2 = to_qtensor(qa, sa, E4M3, GRAN_1x128), to_qtensor(qb, sb, E4M3, GRAN_128x128), \
         to_qtensor(qa2, sa2, E4M3, GRAN_1x128)
-    c = fp8hg.fp8_gemm_scaled(FPROP, a, b, out_dtype=torch.float32)
-    fp8hg.fp8_gemm_scaled(FPROP, a2, b, out=c, accumulate=True)
+    c = fp8hg.fp8_gemm_scaled(FPROP, a, b, out_dtype=out_dtype, tile=tile)
+    c1 = c.float().cpu().numpy()                   # the first product as stored
+    fp8hg.fp8_gemm_scaled(FPROP, a2, b, out=c, accumulate=True, tile=tile)
     r1, s1 = _ref(qa, sa, GRAN_1x128, E4M3, qb, sb, GRAN_128x128, E4M3)
     r2, s2 = _ref(qa2, sa2, GRAN_1x128, E4M3, qb, sb, GRAN_128x128, E4M3)
-    check_gemm(c.cpu().numpy(), r1 + r2, s1 + s2, "accumulate fp32")
+    check_gemm(c1, r1, s1, "first product")
+    # the sum is rounded once more to the output type (BF16: one more ulp)
+    check_gemm(c.float().cpu().numpy(), r1 + r2, s1 + s2 + np.abs(r1), "accumulate")
 
 
-def test_gemm_unit_scales_exact(cuda_lib):
+@pytest.mark.parametrize("tile", TILES)
+def test_gemm_unit_scales_exact(cuda_lib, tile):
     """Small-integer codes with unit scales: the product is an exact integer
     matrix that FP32 accumulation represents exactly."""
     rng = np.random.default_rng(0)
     ints = np.arange(-8, 9)
     codes = torch.tensor(ints, dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
-    M, N, K = 128, 256, 256
+    M, N, K = 256, 256, 256
     ia, ib = rng.integers(0, 17, (M, K)), rng.integers(0, 17, (N, K))
     qa, qb = codes[ia], codes[ib]
     sa = np.full((M, K // 128), 127, np.uint8)
     sb = np.full((N // 128, K // 128), 127, np.uint8)
     c = fp8hg.fp8_gemm_scaled(FPROP, to_qtensor(qa, sa, E4M3, GRAN_1x128),
-                              to_qtensor(qb, sb, E4M3, GRAN_128x128), out_dtype=torch.float32)
+                              to_qtensor(qb, sb, E4M3, GRAN_128x128), out_dtype=torch.float32,
+                              tile=tile)
     exact = ints[ia].astype(np.int64) @ ints[ib].astype(np.int64).T
     assert np.array_equal(c.cpu().numpy().astype(np.int64), exact)
 
 
-def test_gemm_distinct_row_scales(cuda_lib):
+@pytest.mark.parametrize("tile", TILES)
+def test_gemm_distinct_row_scales(cuda_lib, tile):
     """Unit codes, a distinct power-of-two scale per A row and per 128-row B
     block, and per-32-K MX scales: any mix-up of scale rows, blocks or K slots
     changes the product by a power of two."""
     rng = np.random.default_rng(1)
-    M, N, K = 128, 256, 256
+    M, N, K = 256, 256, 256
     one = 0x38  # E4M3 code of 1.0
     qa = np.full((M, K), one, np.uint8)
     qb = np.full((N, K), one, np.uint8)
     sa = (100 + rng.integers(0, 40, (M, K // 32))).astype(np.uint8)
     sb = (100 + rng.integers(0, 40, (N, K // 32))).astype(np.uint8)
     c = fp8hg.fp8_gemm_scaled(FPROP, to_qtensor(qa, sa, E4M3, GRAN_MX32),
-                              to_qtensor(qb, sb, E4M3, GRAN_MX32), out_dtype=torch.float32)
+                              to_qtensor(qb, sb, E4M3, GRAN_MX32), out_dtype=torch.float32,
+                              tile=tile)
     c_ref, s_abs = _ref(qa, sa, GRAN_MX32, E4M3, qb, sb, GRAN_MX32, E4M3)
     check_gemm(c.cpu().numpy(), c_ref, s_abs, "distinct scales")
 
 
-def test_gemm_timeout_path(cuda_lib):
+@pytest.mark.parametrize("tile", TILES)
+def test_gemm_timeout_path(cuda_lib, tile):
     """A host-injected missing arrival makes the first pipeline wait run out:
     the kernel returns, the status reads TIMEOUT, and the next call works."""
-    M, N, K = 128, 256, 256
+    M, N, K = 256, 256, 256
     qa, sa = _operand("act", M, K, GRAN_1x128, E4M3, 5)
     qb, sb = _operand("weight", N, K, GRAN_128x128, E4M3, 6)
     a, b = to_qtensor(qa, sa, E4M3, GRAN_1x128), to_qtensor(qb, sb, E4M3, GRAN_128x128)
-    fp8hg.fp8_gemm_scaled(FPROP, a, b, wait_limit_ns=20_000_000, inject_fault=1)
+    fp8hg.fp8_gemm_scaled(FPROP, a, b, wait_limit_ns=20_000_000, inject_fault=1, tile=tile)
     assert fp8hg.fp8hg_get_device_error() == 6  # FP8HG_ERR_TIMEOUT
-    c = fp8hg.fp8_gemm_scaled(FPROP, a, b, out_dtype=torch.float32)
+    c = fp8hg.fp8_gemm_scaled(FPROP, a, b, out_dtype=torch.float32, tile=tile)
     assert fp8hg.fp8hg_get_device_error() == 0
     c_ref, s_abs = _ref(qa, sa, GRAN_1x128, E4M3, qb, sb, GRAN_128x128, E4M3)
     check_gemm(c.cpu().numpy(), c_ref, s_abs, "after timeout")
