@@ -467,7 +467,7 @@ def main():
                        "gemms_per_step": N_GEMM, "quant_launches_per_step": N_QUANT,
                        "l2": "inputs larger than L2 (each step streams ~15 GB); no flush",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
-            "roofline": {"bound": "tensor", "kernel": "k_gemm_mxf8", "achieved": gemm_tf,
+            "roofline": {"bound": "tensor", "kernel": "k_gemm_wide", "achieved": gemm_tf,
                          "peak": fp8_peak, "unit": "TFLOP/s", "frac": gemm_tf / fp8_peak,
                          "traffic": traffic,
                          "peak_source": f"{peaks['src']} bf16 sustained x2 (nominal fp8/bf16 ratio)",
