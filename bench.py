@@ -235,10 +235,12 @@ class Step:
 
 
 # ---------------------------------------------------------- oracle sample
-def oracle_sample_step(tile: int = 32):
+def oracle_sample_step(tile: int = 32, barrier=None):
     """The oracle on one tile x tile block of outputs of each of the step's 9
     GEMMs at full K, quantizing the operand slices that block needs (whole
-    128-row weight blocks, whole 128-token groups).  Returns (flop, seconds)."""
+    128-row weight blocks, whole 128-token groups).  Returns (flop, seconds).
+    barrier: waited on after the inputs are generated, before the clock starts
+    (several processes then time the same interval)."""
     import oracle
     from fp8_hybrid_granularity_gb300 import workloads as wl
     oracle.build()
@@ -256,6 +258,8 @@ def oracle_sample_step(tile: int = 32):
     dyd_c = gen("grad", M_TOK, t, "dYdc")                               # t channels, all tokens
     x_c, h_c = gen("act", M_TOK, t, "Xc"), gen("act", M_TOK, t, "Hc")
     R, B128, T = oracle.GRAN_ROW, oracle.GRAN_128x128, oracle.GRAN_1x128
+    if barrier is not None:
+        barrier.wait(timeout=600)
 
     def gemm(qa, sa, ga, fa, qb, sb, gb, fb):
         qa, qb = qa[:t], qb[:t]
@@ -285,29 +289,98 @@ def oracle_sample_step(tile: int = 32):
     return flop, time.perf_counter() - t0
 
 
+def _oracle_worker(barrier, queue, steps):
+    try:
+        queue.put([oracle_sample_step(barrier=barrier) for _ in range(steps)])
+    except Exception as e:  # reported by the parent
+        queue.put(("error", repr(e)))
+
+
+def oracle_all_cores(steps: int = 1, skip: int = 0):
+    """The oracle sample step in one spawned process per host core, `steps`
+    times, every process starting each step's clock together (a barrier).
+    Returns (flop of all processes over the last steps - skip steps, the sum
+    over those steps of the slowest process's seconds, processes), or None if
+    the processes could not be run."""
+    import multiprocessing as mp
+    import queue as _queue
+    import oracle
+    oracle.build()
+    n = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    if n < 2:
+        return None
+    ctx = mp.get_context("spawn")
+    barrier, q = ctx.Barrier(n), ctx.Queue()
+    procs = [ctx.Process(target=_oracle_worker, args=(barrier, q, steps), daemon=True)
+             for _ in range(n)]
+    for p in procs:
+        p.start()
+    res = []
+    try:
+        for _ in range(n):
+            res.append(q.get(timeout=900))
+    except _queue.Empty:
+        res = []
+    for p in procs:
+        p.join(timeout=60)
+        if p.is_alive():
+            p.terminate()
+    if len(res) != n or any(r[0] == "error" for r in res):
+        return None
+    flop = sum(r[i][0] for r in res for i in range(skip, steps))
+    secs = sum(max(r[i][1] for r in res) for i in range(skip, steps))
+    return flop, secs, n
+
+
+def cpu_baseline_entry():
+    """cpu_baseline: the oracle on all host cores (one process per core), with
+    the single-thread figure beside it."""
+    flop1, secs1 = oracle_sample_step()
+    one = {"value": flop1 / secs1 / 1e12, "unit": "TFLOP/s", "cores": 1, "seconds": secs1}
+    allc = oracle_all_cores()
+    if allc is None:
+        return dict(one, kind="oracle", sample=SAMPLE_DESC)
+    flop, secs, n = allc
+    return {"value": flop / secs / 1e12, "unit": "TFLOP/s", "cores": n, "kind": "oracle",
+            "sample": SAMPLE_DESC_ALL.format(n=n), "seconds": secs, "single_thread": one}
+
+
+SAMPLE_DESC_ALL = ("{n} processes at once (one per host core), each running the oracle (plain C, "
+                   "fp64, 1 thread) on a 32x32 block of outputs of each of the step's 9 GEMMs at "
+                   "full K, including quantizing the operand slices it needs (whole 128-row "
+                   "weight blocks, whole 128-token groups)")
+
 SAMPLE_DESC = ("oracle (plain C, fp64, 1 thread) on a 32x32 block of outputs of each of the "
                "step's 9 GEMMs at full K, including quantizing the operand slices it needs "
                "(whole 128-row weight blocks, whole 128-token groups)")
 
 
 def run_reference(args):
+    """The oracle as it stands on the host cores: one process per core, each
+    running the sample step; W untimed steps, then K timed ones."""
     if not replicas.rank_info().is_root:
         return
-    for _ in range(args.warmup):
-        oracle_sample_step()
-    flop, secs = 0.0, 0.0
-    for _ in range(args.steps):
-        f, s = oracle_sample_step()
-        flop += f
-        secs += s
+    allc = oracle_all_cores(args.warmup + args.steps, skip=args.warmup)
+    if allc is not None:
+        flop, secs, cores = allc
+        sample = SAMPLE_DESC_ALL.format(n=cores)
+    else:   # processes could not be started: one thread, in this process
+        for _ in range(args.warmup):
+            oracle_sample_step()
+        flop, secs, cores = 0.0, 0.0, 1
+        for _ in range(args.steps):
+            f, s = oracle_sample_step()
+            flop += f
+            secs += s
+        sample = SAMPLE_DESC
     tf = flop / secs / 1e12
     line = {"impl": "reference", "metric": METRIC, "value": tf, "unit": "TFLOP/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "sample": "32x32 outputs per GEMM at full K"},
-            "cpu_baseline": {"value": tf, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-                             "sample": SAMPLE_DESC},
+            "cpu_baseline": {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
             "e2e": {"value": tf, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -452,9 +525,7 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        flop, secs = oracle_sample_step()
-        cpu = {"value": flop / secs / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-               "sample": SAMPLE_DESC, "seconds": secs}
+        cpu = cpu_baseline_entry()
 
     if rank == 0:
         traffic = _gemm_traffic()
