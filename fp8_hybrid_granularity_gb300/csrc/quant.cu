@@ -343,10 +343,11 @@ __global__ void __launch_bounds__(256) k_quant_groups(const uint16_t *__restrict
 // One CTA per 128-row x 64-column tile of x.  The tile is staged in shared
 // memory, each column's amax over the 128 rows is reduced, and the codes are
 // staged again so that the transposed output rows (64 of 128 bytes) are
-// written with full, coalesced 16-byte stores.
+// written with full, coalesced 16-byte stores.  At most 40 registers a thread
+// (six CTAs per SM instead of five at 48): more tiles' loads in flight.
 constexpr int kTC = 64;  // tile columns
 template <int FMT>
-__global__ void __launch_bounds__(256) k_quant_t(const uint16_t *__restrict__ x, int64_t ld_x,
+__global__ void __launch_bounds__(256, 6) k_quant_t(const uint16_t *__restrict__ x, int64_t ld_x,
                                                  uint8_t *__restrict__ qt, int64_t ld_q,
                                                  uint8_t *__restrict__ st, int64_t ld_s) {
     __shared__ __align__(16) uint16_t tile[128][kTC + 8];
