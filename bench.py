@@ -19,10 +19,10 @@ no explicit flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
---impl reference times the CPU oracle (plain C, fp64, one core) on a bounded
-sample of the same step: a 32x32 block of outputs of each of the 9 GEMMs at
-full K, including the oracle's quantization of the operand slices that block
-needs.
+--impl reference times the CPU oracle (plain C, fp64, single-threaded) on a
+bounded sample of the same step, in one process per host core: a 32x32 block
+of outputs of each of the 9 GEMMs at full K, including the oracle's
+quantization of the operand slices that block needs.
 """
 from __future__ import annotations
 
@@ -494,7 +494,9 @@ def main():
     # while step i computes (copy engines and SMs work concurrently); with
     # two sets a step's input copy would wait for the output copy of the
     # step before last, and the chain copy-in -> compute -> copy-out would
-    # set the period instead of the copy bandwidth.
+    # set the period instead of the copy bandwidth.  Per-tensor events let a
+    # launch start once its own inputs have arrived and an output leave as
+    # soon as it is final.
     e2e = None
     if not args.no_e2e:
         host_in = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in step.inp.items()}
