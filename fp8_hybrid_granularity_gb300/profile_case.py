@@ -23,6 +23,8 @@ kernel, and prints the mean launch time from CUDA events.  Cases:
   quant_t    1x128-along-tokens transposed quantization of H [M, 18944]
   block128   128x128 quantization (+ transposed copy) of W_down [3584, 18944]
   mx32       MXFP8 quantization of [M, 4096]
+  gemm_mx    MXFP8 x MXFP8 GEMM: A [M, 4096], B [4096, 4096] (layer-norm-like
+             and normal rows), both quantized in 32-element blocks, BF16 out
   mx32_mon   the same with the clamp monitor's counts
   requant    stored per-token FP8 codes of H [M, 18944] -> 1x128 along the
              tokens, transposed (the weight-gradient operand)
@@ -48,7 +50,7 @@ HID, MLP = 3584, 18944
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("case", choices=["gemm", "gemm_gate", "gemm_gate_q", "gemm_gate_f32s", "gemm_f32s",
-                                     "quant_row_f32s", "wgrad", "quant_row", "quant_1x128", "quant_t", "block128",
+                                     "quant_row_f32s", "wgrad", "quant_row", "quant_1x128", "quant_t", "block128", "gemm_mx",
                                      "mx32", "mx32_mon", "requant", "sweep"])
     ap.add_argument("--m", type=int, default=4096)
     ap.add_argument("--warmup", type=int, default=2)
@@ -111,6 +113,12 @@ def main():
         out = fp8hg.alloc_token(M, MLP, group, E4, tr, dev)
         fn = lambda: fp8hg.fp8_quant_token(h, group, E4, tr, out=out)
         work, unit = 3.0 * M * MLP + (M if group == 0 else M * MLP / 128), "byte"
+    elif args.case == "gemm_mx":
+        a = fp8hg.fp8_quant_mx32(mk("mx_ln", M, 4096, "A"), E4)
+        b = fp8hg.fp8_quant_mx32(mk("mx_ln", 4096, 4096, "B"), E4)
+        out = torch.empty((M, 4096), dtype=torch.bfloat16, device=dev)
+        fn = lambda: fp8hg.fp8_gemm_scaled(fp8hg.FPROP, a, b, out=out)
+        work, unit = 2.0 * M * 4096 * 4096, "flop"
     elif args.case == "block128":
         w = mk("weight", HID, MLP, "W_down")
         o, ot = fp8hg.alloc_block128(HID, MLP, E4, True, dev)
