@@ -23,6 +23,8 @@ kernel, and prints the mean launch time from CUDA events.  Cases:
   quant_t    1x128-along-tokens transposed quantization of H [M, 18944]
   block128   128x128 quantization (+ transposed copy) of W_down [3584, 18944]
   mx32       MXFP8 quantization of [M, 4096]
+  gemm_shape fprop on any shape: A [M, K] per token, B [N, K] 128x128 blocks,
+             BF16 out (--n, --k; e.g. the 1.5B layers at M = 8192)
   gemm_mx    MXFP8 x MXFP8 GEMM: A [M, 4096], B [4096, 4096] (layer-norm-like
              and normal rows), both quantized in 32-element blocks, BF16 out
   mx32_mon   the same with the clamp monitor's counts
@@ -50,11 +52,13 @@ HID, MLP = 3584, 18944
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("case", choices=["gemm", "gemm_gate", "gemm_gate_q", "gemm_gate_f32s", "gemm_f32s",
-                                     "quant_row_f32s", "wgrad", "quant_row", "quant_1x128", "quant_t", "block128", "gemm_mx",
+                                     "quant_row_f32s", "wgrad", "quant_row", "quant_1x128", "quant_t", "block128", "gemm_mx", "gemm_shape",
                                      "mx32", "mx32_mon", "requant", "sweep"])
     ap.add_argument("--m", type=int, default=4096)
     ap.add_argument("--warmup", type=int, default=2)
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--n", type=int, default=HID)
+    ap.add_argument("--k", type=int, default=MLP)
     args = ap.parse_args()
     fp8hg.load_library()
     dev = torch.device("cuda", 0)
@@ -113,6 +117,12 @@ def main():
         out = fp8hg.alloc_token(M, MLP, group, E4, tr, dev)
         fn = lambda: fp8hg.fp8_quant_token(h, group, E4, tr, out=out)
         work, unit = 3.0 * M * MLP + (M if group == 0 else M * MLP / 128), "byte"
+    elif args.case == "gemm_shape":
+        a = fp8hg.fp8_quant_token(mk("act", M, args.k, "A"), 0, E4)
+        b = fp8hg.fp8_quant_block128(mk("weight", args.n, args.k, "W"), E4)
+        out = torch.empty((M, args.n), dtype=torch.bfloat16, device=dev)
+        fn = lambda: fp8hg.fp8_gemm_scaled(fp8hg.FPROP, a, b, out=out)
+        work, unit = 2.0 * M * args.n * args.k, "flop"
     elif args.case == "gemm_mx":
         a = fp8hg.fp8_quant_mx32(mk("mx_ln", M, 4096, "A"), E4)
         b = fp8hg.fp8_quant_mx32(mk("mx_ln", 4096, 4096, "B"), E4)
@@ -157,7 +167,7 @@ def main():
         raise SystemExit(f"device error {fp8hg.fp8hg_status_str(status)}")
     ms = sum(a0.elapsed_time(b0) for a0, b0 in evs) / len(evs)
     rate = work / (ms * 1e-3) / (1e12 if unit == "flop" else 1e9)
-    print(json.dumps({"case": args.case, "m": M, "ms": ms,
+    print(json.dumps({"case": args.case, "m": M, **({"n": args.n, "k": args.k} if args.case == "gemm_shape" else {}), "ms": ms,
                       ("tflops" if unit == "flop" else "gbs"): rate}))
 
 
