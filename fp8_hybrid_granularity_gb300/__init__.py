@@ -63,6 +63,18 @@ class GemmOpts(ctypes.Structure):
                 ("tile", ctypes.c_int32)]
 
 
+class WaitOpts(ctypes.Structure):
+    _fields_ = [("wait_limit_ns", ctypes.c_uint64), ("inject_fault", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+def _wait_opts(wait_limit_ns: int, inject_fault: int):
+    """A WaitOpts by reference, or None (library defaults) when both are 0."""
+    if not wait_limit_ns and not inject_fault:
+        return None
+    return ctypes.byref(WaitOpts(wait_limit_ns, inject_fault, 0))
+
+
 _lib = None
 _lock = threading.Lock()
 
@@ -87,6 +99,10 @@ def load_library(build_if_stale: bool = True):
         lib = ctypes.CDLL(_build.LIB_PATH)
         P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         lib.fp8_quant_token.argtypes = [P, I64, I64, I64, I, I, I, P, I64, P, I64, P]
+        lib.fp8_quant_token_ex.argtypes = [P, I64, I64, I64, I, I, I, P, I64, P, I64, P, P]
+        lib.fp8_requant_t_ex.argtypes = [P, I64, I64, I64, P, I64, I, I, I, P, I64, P, I64, P, P]
+        lib.fp8_gemm_scaled_f32s_ex.argtypes = [I, ctypes.POINTER(Operand),
+                                                ctypes.POINTER(Operand), P, I64, I, P, P]
         lib.fp8_quant_block128.argtypes = [P, I64, I64, I64, I, P, I64, P, I64, P, I64, P, I64, P]
         lib.fp8_quant_mx32.argtypes = [P, I64, I64, I64, I, P, I64, P, I64, P, P]
         lib.fp8_quant_mx32_monitor.argtypes = [P, I64, I64, I64, I, P, I64, P, I64, P, P, P]
@@ -107,7 +123,8 @@ def load_library(build_if_stale: bool = True):
         lib.fp8hg_status_str.restype = ctypes.c_char_p
         lib.fp8hg_status_str.argtypes = [I]
         for fn in ("fp8_quant_token", "fp8_quant_block128", "fp8_quant_mx32", "fp8_gemm_scaled",
-                   "fp8_gemm_scaled_ex", "fp8hg_get_device_error", "fp8hg_version"):
+                   "fp8_gemm_scaled_ex", "fp8hg_get_device_error", "fp8hg_version",
+                   "fp8_quant_token_ex", "fp8_requant_t_ex", "fp8_gemm_scaled_f32s_ex"):
             getattr(lib, fn).restype = I
         _lib = lib
         return lib
@@ -167,16 +184,19 @@ def _check_bf16(x):
 
 
 def fp8_quant_token(x, group: int = 0, fmt: int = E4M3, transpose: bool = False,
-                    out: Optional[QTensor] = None, stream=None) -> QTensor:
+                    out: Optional[QTensor] = None, stream=None, wait_limit_ns: int = 0,
+                    inject_fault: int = 0) -> QTensor:
     """Per-token (group=0) or per-1x128 (group=128) UE8M0 quantization;
     transpose=True quantizes 128-row groups and writes [cols, rows].
-    out: optional preallocated QTensor (e.g. from alloc_token)."""
+    out: optional preallocated QTensor (e.g. from alloc_token).
+    wait_limit_ns / inject_fault: see fp8hg_wait_opts (tests of the timeout path)."""
     _check_bf16(x)
     rows, cols = x.shape
     out = out if out is not None else alloc_token(rows, cols, group, fmt, transpose, x.device)
-    rc = lib().fp8_quant_token(_ptr(x), rows, cols, x.stride(0), group, 1 if transpose else 0,
-                               fmt, _ptr(out.codes), out.codes.stride(0), _ptr(out.scale),
-                               out.scale.stride(0), _stream(stream))
+    rc = lib().fp8_quant_token_ex(_ptr(x), rows, cols, x.stride(0), group, 1 if transpose else 0,
+                                  fmt, _ptr(out.codes), out.codes.stride(0), _ptr(out.scale),
+                                  out.scale.stride(0), _wait_opts(wait_limit_ns, inject_fault),
+                                  _stream(stream))
     _check(rc, "fp8_quant_token")
     return out
 
@@ -257,7 +277,7 @@ def fp8_quant_mx32(x, fmt: int = E4M3, clamp_count=None, out=None, stream=None) 
 
 
 def fp8_requant_t(src: QTensor, fmt: int = E4M3, out: Optional[QTensor] = None,
-                  stream=None) -> QTensor:
+                  stream=None, wait_limit_ns: int = 0, inject_fault: int = 0) -> QTensor:
     """Re-quantize a stored per-token or 1x128 operand [tokens, cols] into
     1x128 groups along the tokens, transposed ([cols, tokens]): the
     weight-gradient operand, from the FP8 codes instead of the BF16 source."""
@@ -265,10 +285,10 @@ def fp8_requant_t(src: QTensor, fmt: int = E4M3, out: Optional[QTensor] = None,
         raise ValueError("source must have per-token or 1x128 scales")
     rows, cols = src.codes.shape
     out = out if out is not None else alloc_token(rows, cols, 128, fmt, True, src.codes.device)
-    rc = lib().fp8_requant_t(_ptr(src.codes), rows, cols, src.codes.stride(0), _ptr(src.scale),
-                             src.scale.stride(0), src.gran, src.fmt, fmt, _ptr(out.codes),
-                             out.codes.stride(0), _ptr(out.scale), out.scale.stride(0),
-                             _stream(stream))
+    rc = lib().fp8_requant_t_ex(_ptr(src.codes), rows, cols, src.codes.stride(0), _ptr(src.scale),
+                                src.scale.stride(0), src.gran, src.fmt, fmt, _ptr(out.codes),
+                                out.codes.stride(0), _ptr(out.scale), out.scale.stride(0),
+                                _wait_opts(wait_limit_ns, inject_fault), _stream(stream))
     _check(rc, "fp8_requant_t")
     return out
 
@@ -346,7 +366,8 @@ def fp8_quant_block128_f32s(x, fmt: int = E4M3, transposed_copy: bool = False, s
     return (out, out_t) if transposed_copy else out
 
 
-def fp8_gemm_scaled_f32s(op: int, a: QTensor, b: QTensor, out=None, out_dtype=None, stream=None):
+def fp8_gemm_scaled_f32s(op: int, a: QTensor, b: QTensor, out=None, out_dtype=None, stream=None,
+                         wait_limit_ns: int = 0, inject_fault: int = 0):
     """C = A * B^T on FP8 operands with FP32 scales (promotion GEMM)."""
     import torch
     if out is None:
@@ -361,8 +382,9 @@ def fp8_gemm_scaled_f32s(op: int, a: QTensor, b: QTensor, out=None, out_dtype=No
     if a.scale.dtype != torch.float32 or b.scale.dtype != torch.float32:
         raise ValueError("operands must carry float32 scales")
     oa, ob = a.operand(), b.operand()
-    rc = lib().fp8_gemm_scaled_f32s(op, ctypes.byref(oa), ctypes.byref(ob), _ptr(out),
-                                    out.stride(0), kind, _stream(stream))
+    rc = lib().fp8_gemm_scaled_f32s_ex(op, ctypes.byref(oa), ctypes.byref(ob), _ptr(out),
+                                       out.stride(0), kind, _wait_opts(wait_limit_ns, inject_fault),
+                                       _stream(stream))
     _check(rc, "fp8_gemm_scaled_f32s")
     return out
 

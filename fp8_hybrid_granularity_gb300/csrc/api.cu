@@ -69,6 +69,17 @@ int check_quant_common(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld
     return FP8HG_OK;
 }
 
+// fp8hg_wait_opts -> WaitOpts (NULL = defaults).
+int wait_opts(const fp8hg_wait_opts *opts, fp8hg::WaitOpts &w) {
+    w = fp8hg::WaitOpts{};
+    if (!opts) return FP8HG_OK;
+    if (opts->inject_fault < 0 || opts->inject_fault > 1 || opts->reserved != 0)
+        return FP8HG_ERR_INVALID_ARG;
+    w.limit_ns = opts->wait_limit_ns;
+    w.inject = opts->inject_fault;
+    return FP8HG_OK;
+}
+
 }  // namespace
 
 namespace {
@@ -117,10 +128,13 @@ int run_gemm(fp8hg::GemmArgs &g, const fp8hg_gemm_opts *opts, void *stream) {
 
 extern "C" {
 
-int fp8_quant_token(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int group,
-                    int transpose, int fmt, uint8_t *q, int64_t ld_q, uint8_t *scale, int64_t ld_s,
-                    void *stream) {
-    int st = check_quant_common(x, rows, cols, ld_x, fmt, q, ld_q, scale);
+int fp8_quant_token_ex(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int group,
+                       int transpose, int fmt, uint8_t *q, int64_t ld_q, uint8_t *scale,
+                       int64_t ld_s, const fp8hg_wait_opts *opts, void *stream) {
+    fp8hg::WaitOpts w;
+    int st = wait_opts(opts, w);
+    if (st != FP8HG_OK) return st;
+    st = check_quant_common(x, rows, cols, ld_x, fmt, q, ld_q, scale);
     if (st != FP8HG_OK) return st;
     if (group != 0 && group != 128) return FP8HG_ERR_INVALID_ARG;
     if (transpose != 0 && transpose != 1) return FP8HG_ERR_INVALID_ARG;
@@ -136,9 +150,17 @@ int fp8_quant_token(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
         if (ld_s < (group ? cols / 128 : 1)) return FP8HG_ERR_INVALID_ARG;
         if (group == 0 && rows > 2147483647LL) return FP8HG_ERR_SHAPE;
     }
+    if (w.inject && !fp8hg::quant_token_waits(cols, group, transpose)) return FP8HG_ERR_UNSUPPORTED;
     return status_from_cuda(fp8hg::launch_quant_token(x, rows, cols, ld_x, group, transpose, fmt, q,
-                                                      ld_q, scale, ld_s,
+                                                      ld_q, scale, ld_s, w,
                                                       static_cast<cudaStream_t>(stream)));
+}
+
+int fp8_quant_token(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int group,
+                    int transpose, int fmt, uint8_t *q, int64_t ld_q, uint8_t *scale, int64_t ld_s,
+                    void *stream) {
+    return fp8_quant_token_ex(x, rows, cols, ld_x, group, transpose, fmt, q, ld_q, scale, ld_s,
+                              nullptr, stream);
 }
 
 int fp8_quant_block128(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
@@ -191,9 +213,13 @@ int fp8_quant_mx32_monitor(const uint16_t *x, int64_t rows, int64_t cols, int64_
         static_cast<cudaStream_t>(stream)));
 }
 
-int fp8_requant_t(const uint8_t *q, int64_t rows, int64_t cols, int64_t ld_q, const uint8_t *scale,
-                  int64_t ld_s, int gran, int fmt_in, int fmt_out, uint8_t *q_t, int64_t ld_qt,
-                  uint8_t *scale_t, int64_t ld_st, void *stream) {
+int fp8_requant_t_ex(const uint8_t *q, int64_t rows, int64_t cols, int64_t ld_q,
+                     const uint8_t *scale, int64_t ld_s, int gran, int fmt_in, int fmt_out,
+                     uint8_t *q_t, int64_t ld_qt, uint8_t *scale_t, int64_t ld_st,
+                     const fp8hg_wait_opts *opts, void *stream) {
+    fp8hg::WaitOpts w;
+    const int wst = wait_opts(opts, w);
+    if (wst != FP8HG_OK) return wst;
     if (!valid_fmt(fmt_in) || !valid_fmt(fmt_out)) return FP8HG_ERR_INVALID_ARG;
     if (gran != FP8HG_GRAN_ROW && gran != FP8HG_GRAN_1x128) return FP8HG_ERR_UNSUPPORTED;
     if (rows < 0 || cols < 0) return FP8HG_ERR_INVALID_ARG;
@@ -206,8 +232,15 @@ int fp8_requant_t(const uint8_t *q, int64_t rows, int64_t cols, int64_t ld_q, co
     if (ld_s < (gran == FP8HG_GRAN_ROW ? 1 : cols / 128)) return FP8HG_ERR_INVALID_ARG;
     return status_from_cuda(fp8hg::launch_requant_t(q, rows, cols, ld_q, scale, ld_s,
                                                     gran == FP8HG_GRAN_ROW ? 1 : 0, fmt_in,
-                                                    fmt_out, q_t, ld_qt, scale_t, ld_st,
+                                                    fmt_out, q_t, ld_qt, scale_t, ld_st, w,
                                                     static_cast<cudaStream_t>(stream)));
+}
+
+int fp8_requant_t(const uint8_t *q, int64_t rows, int64_t cols, int64_t ld_q, const uint8_t *scale,
+                  int64_t ld_s, int gran, int fmt_in, int fmt_out, uint8_t *q_t, int64_t ld_qt,
+                  uint8_t *scale_t, int64_t ld_st, void *stream) {
+    return fp8_requant_t_ex(q, rows, cols, ld_q, scale, ld_s, gran, fmt_in, fmt_out, q_t, ld_qt,
+                            scale_t, ld_st, nullptr, stream);
 }
 
 int fp8_gemm_scaled_ex(int op, const fp8hg_operand *a, const fp8hg_operand *b, void *c, int64_t ldc,
@@ -294,8 +327,12 @@ int fp8_quant_block128_f32s(const uint16_t *x, int64_t rows, int64_t cols, int64
                                                               static_cast<cudaStream_t>(stream)));
 }
 
-int fp8_gemm_scaled_f32s(int op, const fp8hg_operand_f32s *a, const fp8hg_operand_f32s *b, void *c,
-                         int64_t ldc, int out, void *stream) {
+int fp8_gemm_scaled_f32s_ex(int op, const fp8hg_operand_f32s *a, const fp8hg_operand_f32s *b,
+                            void *c, int64_t ldc, int out, const fp8hg_wait_opts *opts,
+                            void *stream) {
+    fp8hg::WaitOpts w;
+    const int wst = wait_opts(opts, w);
+    if (wst != FP8HG_OK) return wst;
     if (op < FP8HG_FPROP || op > FP8HG_WGRAD) return FP8HG_ERR_INVALID_ARG;
     if (out != FP8HG_OUT_BF16 && out != FP8HG_OUT_FP32) return FP8HG_ERR_INVALID_ARG;
     if (!a || !b) return FP8HG_ERR_INVALID_ARG;
@@ -338,11 +375,17 @@ int fp8_gemm_scaled_f32s(int op, const fp8hg_operand_f32s *a, const fp8hg_operan
     g.c = c;
     g.ldc = ldc;
     g.out_fp32 = out == FP8HG_OUT_FP32;
-    g.wait_limit_ns = kDefaultWaitNs;
+    g.wait_limit_ns = w.limit_ns ? w.limit_ns : kDefaultWaitNs;
+    g.inject_fault = w.inject;
     g.err = err;
     const int rc = fp8hg::launch_gemm_f32s(g, static_cast<cudaStream_t>(stream));
     if (rc == 1) return FP8HG_ERR_UNSUPPORTED;
     return rc == 0 ? FP8HG_OK : FP8HG_ERR_CUDA;
+}
+
+int fp8_gemm_scaled_f32s(int op, const fp8hg_operand_f32s *a, const fp8hg_operand_f32s *b, void *c,
+                         int64_t ldc, int out, void *stream) {
+    return fp8_gemm_scaled_f32s_ex(op, a, b, c, ldc, out, nullptr, stream);
 }
 
 int fp8hg_get_device_error(void *stream) {

@@ -69,9 +69,16 @@ constexpr uint32_t OFF_B = OFF_A + STAGES * A_TILE;
 constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_TILE;
 constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_TILE;
 constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_TILE;
+// Barriers (8 bytes each) from OFF_BAR: tma[STAGES] at 0 (the stage's operand
+// bytes landed), empty[STAGES] at 32 (the MMAs that read the stage are done),
+// tfull 64, tempty 72, drain 80, sf[STAGES] at 128 (the scale warp wrote the
+// stage's scale words).  The operand copies and the scale words complete on
+// separate barriers, so a CTA that stops early can wait for its own copies
+// alone.
+constexpr uint32_t BAR_SF = 128;
 constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + 96;
 constexpr uint32_t OFF_ABORT = OFF_BAR + 100;
-constexpr uint32_t OFF_EPI = OFF_BAR + 128;      // 4 KB per epilogue warp: store staging
+constexpr uint32_t OFF_EPI = OFF_BAR + 256;      // 4 KB per epilogue warp: store staging
 constexpr uint32_t EPI_WARP_BYTES = 32 * 128;
 constexpr uint32_t SMEM_USED = OFF_EPI + 4 * EPI_WARP_BYTES;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
@@ -247,8 +254,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(sBAR + 8 * s, 1 + 32);  // TMA expect_tx + one arrival per scale-warp lane
-            ptx::mbar_init(sBAR + 32 + 8 * s, 1);  // tcgen05.commit
+            ptx::mbar_init(sBAR + 8 * s, 1);            // TMA expect_tx
+            ptx::mbar_init(sBAR + BAR_SF + 8 * s, 32);  // one arrival per scale-warp lane
+            ptx::mbar_init(sBAR + 32 + 8 * s, 1);       // tcgen05.commit
         }
         ptx::mbar_init(tfull, 1);
         ptx::mbar_init(tempty, 128);
@@ -288,7 +296,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ++it;
             }
         }
-        // wait for the last loads to land before the CTA may exit
+        // wait for the last loads to land before the CTA may exit (the tma
+        // barriers count the copies' bytes alone, not the scale arrivals)
         const uint32_t nd = it < static_cast<uint32_t>(STAGES) ? it : static_cast<uint32_t>(STAGES);
         for (uint32_t i = it - nd; i < it; ++i)
             wait_phase(sBAR + 8 * (i % STAGES), (i / STAGES) & 1u, drain_limit, abort_flag, p.err,
@@ -304,7 +313,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::tc_fence_after();
             for (int kb = 0; kb < p.nk; ++kb) {
                 const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-                ok = wait_phase(sBAR + 8 * s, ph, limit, abort_flag, p.err, WHO_MMA);
+                ok = wait_phase(sBAR + 8 * s, ph, limit, abort_flag, p.err, WHO_MMA) &&
+                     wait_phase(sBAR + BAR_SF + 8 * s, ph, limit, abort_flag, p.err, WHO_MMA);
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) break;
                 ptx::tc_fence_after();
@@ -373,7 +383,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 st_shared_v4(dB + 512, cur.b[4][wi], cur.b[5][wi], cur.b[6][wi], cur.b[7][wi]);
                 if (!(p.inject == 1 && it == 0)) {
                     ptx::fence_proxy_async_smem();  // make the words visible to tcgen05.cp
-                    ptx::mbar_arrive(sBAR + 8 * s);
+                    ptx::mbar_arrive(sBAR + BAR_SF + 8 * s);
                 }
                 ++it;
             }
@@ -588,9 +598,11 @@ constexpr uint32_t WOFF_B = WOFF_A + WSTAGES * WA_TILE;
 constexpr uint32_t WOFF_SFA = WOFF_B + WSTAGES * WB_TILE;
 constexpr uint32_t WOFF_SFB = WOFF_SFA + WSTAGES * WSF_TILE;
 constexpr uint32_t WOFF_BAR = WOFF_SFB + WSTAGES * WSF_TILE;
+// barriers as in the 128 x 256 kernel: tma[3] at 0, empty[3] at 32, tfull 64,
+// tempty 72, drain 80, sf[3] at BAR_SF
 constexpr uint32_t WOFF_TMEM_SLOT = WOFF_BAR + 96;
 constexpr uint32_t WOFF_ABORT = WOFF_BAR + 100;
-constexpr uint32_t WOFF_EPI = WOFF_BAR + 128;
+constexpr uint32_t WOFF_EPI = WOFF_BAR + 256;
 constexpr uint32_t W_SMEM_BYTES = WOFF_EPI + 8 * EPI_WARP_BYTES + 1024;
 static_assert(WSFB_COL + 8 * WSTAGES <= TMEM_COLS, "tensor memory overflow");
 static_assert(W_SMEM_BYTES <= 232448, "shared memory overflow");
@@ -669,8 +681,9 @@ __global__ void __launch_bounds__(W_THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < WSTAGES; ++s) {
-            ptx::mbar_init(sBAR + 8 * s, 1 + 64);  // TMA expect_tx + both scale warps' lanes
-            ptx::mbar_init(sBAR + 32 + 8 * s, 1);  // tcgen05.commit
+            ptx::mbar_init(sBAR + 8 * s, 1);            // TMA expect_tx
+            ptx::mbar_init(sBAR + BAR_SF + 8 * s, 64);  // both scale warps' lanes
+            ptx::mbar_init(sBAR + 32 + 8 * s, 1);       // tcgen05.commit
         }
         ptx::mbar_init(tfull, 1);
         ptx::mbar_init(tempty, 256);
@@ -725,7 +738,8 @@ __global__ void __launch_bounds__(W_THREADS, 1)
             ptx::tc_fence_after();
             for (int kb = 0; kb < p.nk; ++kb) {
                 const uint32_t s = it % WSTAGES, ph = (it / WSTAGES) & 1u;
-                ok = wait_phase(sBAR + 8 * s, ph, limit, abort_flag, p.err, WHO_MMA);
+                ok = wait_phase(sBAR + 8 * s, ph, limit, abort_flag, p.err, WHO_MMA) &&
+                     wait_phase(sBAR + BAR_SF + 8 * s, ph, limit, abort_flag, p.err, WHO_MMA);
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) break;
                 ptx::tc_fence_after();
@@ -798,7 +812,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
                 st_shared_v4(d + 512, cur.w[4][wi], cur.w[5][wi], cur.w[6][wi], cur.w[7][wi]);
                 if (!(p.inject == 1 && it == 0)) {
                     ptx::fence_proxy_async_smem();
-                    ptx::mbar_arrive(sBAR + 8 * s);
+                    ptx::mbar_arrive(sBAR + BAR_SF + 8 * s);
                 }
                 ++it;
             }

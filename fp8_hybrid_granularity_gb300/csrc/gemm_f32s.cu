@@ -68,6 +68,7 @@ struct PParams {
     int out_fp32;
     uint32_t idesc;
     uint64_t wait_limit_ns;
+    int inject;  // 1: CTA 0 withholds its first stage's copies (timeout-path test)
     unsigned int *err;
 };
 
@@ -119,6 +120,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
+        const bool withhold_first = p.inject == 1 && blockIdx.x == 0;
         uint32_t it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
@@ -129,7 +131,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                 ok = wait_phase(empty + 8 * s, ph ^ 1u, limit, abort_flag, p.err, WHO_PRODUCER);
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) break;
-                if (lane == 0) {
+                if (lane == 0 && !(withhold_first && it == 0)) {
                     ptx::mbar_arrive_expect_tx(full + 8 * s, PA_TILE + PB_TILE);
                     ptx::tma_load_2d(sA + s * PA_TILE, &tmap_a, full + 8 * s, kb * PK, mb * PM);
                     ptx::tma_load_2d(sB + s * PB_TILE, &tmap_b, full + 8 * s, kb * PK, nb * PN);
@@ -138,10 +140,13 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                 ++it;
             }
         }
+        // wait for the last loads to land before the CTA may exit
         const uint32_t nd = it < static_cast<uint32_t>(PSTAGES) ? it : static_cast<uint32_t>(PSTAGES);
-        for (uint32_t i = it - nd; i < it; ++i)
+        for (uint32_t i = it - nd; i < it; ++i) {
+            if (withhold_first && i == 0) continue;   // never issued
             wait_phase(full + 8 * (i % PSTAGES), (i / PSTAGES) & 1u, drain_limit, abort_flag, p.err,
                        WHO_PRODUCER, false);
+        }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
         uint32_t it = 0, g = 0;
@@ -316,6 +321,7 @@ int launch_gemm_f32s(const GemmF32sArgs &g, cudaStream_t stream) {
               (static_cast<uint32_t>(g.fmt_b) << 10) | (static_cast<uint32_t>(PN >> 3) << 17) |
               (static_cast<uint32_t>(PM >> 4) << 24);
     p.wait_limit_ns = g.wait_limit_ns;
+    p.inject = g.inject_fault;
     p.err = g.err;
     int grid = g_psms[dev];
     if (grid > p.num_tiles) grid = p.num_tiles;

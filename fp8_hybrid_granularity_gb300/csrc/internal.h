@@ -17,9 +17,21 @@ using TensorMapEncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuin
                                        CUtensorMapFloatOOBfill);
 TensorMapEncodeFn tensor_map_encoder();
 
+// Wait options of the kernels that wait on copies: limit_ns bounds one wait
+// (0 = the kernel's default, 2 s); inject = 1 withholds the first copy of
+// CTA 0, so that wait can only run out (a GPU-safe test of the timeout path).
+struct WaitOpts {
+    uint64_t limit_ns = 0;
+    int inject = 0;
+};
+
+// True when fp8_quant_token runs the bulk-copy row kernel (the only
+// configuration of it that waits on copies).
+bool quant_token_waits(int64_t cols, int group, int transpose);
+
 cudaError_t launch_quant_token(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
                                int group, int transpose, int fmt, uint8_t *q, int64_t ld_q,
-                               uint8_t *s, int64_t ld_s, cudaStream_t stream);
+                               uint8_t *s, int64_t ld_s, const WaitOpts &w, cudaStream_t stream);
 
 cudaError_t launch_quant_mx32(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
                               uint8_t *q, int64_t ld_q, uint8_t *s, int64_t ld_s,
@@ -33,7 +45,7 @@ cudaError_t launch_quant_mx32_monitor(const uint16_t *x, int64_t rows, int64_t c
 cudaError_t launch_requant_t(const uint8_t *q, int64_t rows, int64_t cols, int64_t ld_q,
                              const uint8_t *s, int64_t ld_s, int per_token, int fmt_in,
                              int fmt_out, uint8_t *qt, int64_t ld_qt, uint8_t *st, int64_t ld_st,
-                             cudaStream_t stream);
+                             const WaitOpts &w, cudaStream_t stream);
 
 cudaError_t launch_quant_block128(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
                                   int fmt, uint8_t *q, int64_t ld_q, uint8_t *s, int64_t ld_s,
@@ -83,6 +95,7 @@ struct GemmF32sArgs {
     int64_t ldc;
     int out_fp32;
     uint64_t wait_limit_ns;
+    int inject_fault;   // 1: the producer withholds the first stage's copies
     unsigned int *err;
 };
 int launch_gemm_f32s(const GemmF32sArgs &args, cudaStream_t stream);

@@ -59,7 +59,8 @@ __global__ void __launch_bounds__(kRowThreads) k_quant_row(const uint16_t *__res
                                                               int64_t rows, int nvec, int64_t ld_x,
                                                               uint8_t *__restrict__ q, int64_t ld_q,
                                                               uint8_t *__restrict__ s, int64_t ld_s,
-                                                              int nslots, unsigned int *err) {
+                                                              int nslots, uint64_t wait_ns,
+                                                              int inject, unsigned int *err) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t full[kMaxRowSlots];
     __shared__ uint32_t red[kRowThreads / 32];
@@ -70,6 +71,9 @@ __global__ void __launch_bounds__(kRowThreads) k_quant_row(const uint16_t *__res
     const uint32_t sbase = ptx::smem_u32(smem);
     const uint32_t fbase = ptx::smem_u32(full);
     const int64_t step = gridDim.x;
+    // inject = 1 (a test of the timeout path): CTA 0 never issues the copy of
+    // its first row, so the wait for it can only run out.
+    const bool withhold_first = inject == 1 && blockIdx.x == 0;
     if (tid == 0) {
         for (int i = 0; i < nslots; ++i) ptx::mbar_init(fbase + 8 * i, 1);
         ptx::fence_mbar_init();
@@ -77,6 +81,7 @@ __global__ void __launch_bounds__(kRowThreads) k_quant_row(const uint16_t *__res
         for (int i = 0; i < nslots - 1; ++i) {
             const int64_t r = blockIdx.x + i * step;
             if (r >= rows) break;
+            if (i == 0 && withhold_first) continue;
             ptx::mbar_arrive_expect_tx(fbase + 8 * i, row_bytes);
             ptx::bulk_load(sbase + i * row_bytes, x + r * ld_x, row_bytes, fbase + 8 * i);
         }
@@ -88,14 +93,14 @@ __global__ void __launch_bounds__(kRowThreads) k_quant_row(const uint16_t *__res
         // issue the row nslots - 1 ahead into the slot the previous row freed
         if (tid == 0) {
             const int64_t r = row + static_cast<int64_t>(nslots - 1) * step;
-            if (r < rows) {
+            if (r < rows && !(withhold_first && k + nslots - 1 == 0)) {
                 const int sl = (k + nslots - 1) % nslots;
                 ptx::mbar_arrive_expect_tx(fbase + 8 * sl, row_bytes);
                 ptx::bulk_load(sbase + sl * row_bytes, x + r * ld_x, row_bytes, fbase + 8 * sl);
             }
         }
         if (tid == 0) {
-            row_ok = row_wait(fbase + 8 * slot, static_cast<uint32_t>(k / nslots) & 1u, kRowWaitNs);
+            row_ok = row_wait(fbase + 8 * slot, static_cast<uint32_t>(k / nslots) & 1u, wait_ns);
             if (!row_ok) {
                 atomicOr(err, 2u);
                 // let this CTA's other copies in flight land before it exits
@@ -469,6 +474,7 @@ __global__ void __launch_bounds__(256, 2) k_requant_t(const __grid_constant__ CU
                                                       int scale_col_step, int tiles_x, int ntiles,
                                                       uint8_t *__restrict__ qt, int64_t ld_qt,
                                                       uint8_t *__restrict__ st, int64_t ld_st,
+                                                      uint64_t wait_ns, int inject,
                                                       unsigned int *err) {
     extern __shared__ __align__(128) uint8_t rq_smem[];
     RqSmem &sm = *reinterpret_cast<RqSmem *>(rq_smem);
@@ -486,7 +492,10 @@ __global__ void __launch_bounds__(256, 2) k_requant_t(const __grid_constant__ CU
         return s[(static_cast<int64_t>(by) * kRQ + tid) * ld_s +
                  static_cast<int64_t>(bx) * scale_col_step];
     };
-    int issued = 0;  // tiles whose copy thread 0 has issued
+    // inject = 1 (a test of the timeout path): CTA 0 never issues the copy of
+    // its first tile, so the wait for it can only run out.
+    const bool withhold_first = inject == 1 && blockIdx.x == 0;
+    int issued = 0;  // tiles whose copy thread 0 has issued (or withheld)
     if (tid == 0) {
         ptx::prefetch_tmap(&tq);
         for (int i = 0; i < kRqStages; ++i) ptx::mbar_init(fbar + 8 * i, 1);
@@ -494,7 +503,7 @@ __global__ void __launch_bounds__(256, 2) k_requant_t(const __grid_constant__ CU
         for (int i = 0; i < kRqStages; ++i) {
             const int tile = blockIdx.x + i * step;
             if (tile >= ntiles) break;
-            issue(tile, i);
+            if (!(i == 0 && withhold_first)) issue(tile, i);
             ++issued;
         }
     }
@@ -515,7 +524,7 @@ __global__ void __launch_bounds__(256, 2) k_requant_t(const __grid_constant__ CU
             if (!ok) {
                 const uint64_t t0 = ptx::globaltimer();
                 while (!(ok = ptx::mbar_try_wait(bar, parity)))
-                    if (ptx::globaltimer() - t0 > kRqWaitNs) break;
+                    if (ptx::globaltimer() - t0 > wait_ns) break;
             }
             sm.ok = ok;
         }
@@ -592,6 +601,7 @@ __global__ void __launch_bounds__(256, 2) k_requant_t(const __grid_constant__ CU
         // still in flight before the CTA's shared memory is released
         atomicOr(err, 4u);
         for (int j = k; j < issued; ++j) {
+            if (j == 0 && withhold_first) continue;   // never issued
             const uint32_t bar = fbar + 8 * (j % kRqStages);
             const uint32_t parity = static_cast<uint32_t>(j / kRqStages) & 1u;
             const uint64_t t0 = ptx::globaltimer();
@@ -780,7 +790,8 @@ cudaError_t launch_row_regs(const uint16_t *x, int64_t rows, int64_t cols, int64
 
 template <int FMT, int SM>
 cudaError_t launch_row(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, uint8_t *q,
-                       int64_t ld_q, uint8_t *s, int64_t ld_s, cudaStream_t stream) {
+                       int64_t ld_q, uint8_t *s, int64_t ld_s, const WaitOpts &w,
+                       cudaStream_t stream) {
     const int nvec = static_cast<int>(cols / 8);
     const int64_t row_bytes = cols * 2;
     if (row_bytes <= 8192) return launch_row_regs<FMT, SM>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream);
@@ -816,7 +827,8 @@ cudaError_t launch_row(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld
     unsigned int *err = device_error_word();
     if (!err) return cudaErrorInvalidValue;
     k_quant_row<FMT, SM><<<static_cast<unsigned>(grid), threads, static_cast<size_t>(nslots) * row_bytes,
-                       stream>>>(x, rows, nvec, ld_x, q, ld_q, s, ld_s, nslots, err);
+                       stream>>>(x, rows, nvec, ld_x, q, ld_q, s, ld_s, nslots,
+                                 w.limit_ns ? w.limit_ns : kRowWaitNs, w.inject, err);
     return cudaGetLastError();
 }
 
@@ -857,9 +869,18 @@ cudaError_t launch_groups(const uint16_t *x, int64_t rows, int64_t cols, int64_t
 }
 }  // namespace
 
+bool quant_token_waits(int64_t cols, int group, int transpose) {
+    if (transpose || group != 0) return false;
+    const int64_t row_bytes = cols * 2;
+    if (row_bytes <= 8192) return false;
+    int64_t per_sm = kRowSmemBudget / (2 * row_bytes);
+    const int64_t ctas = per_sm < 1 ? 1 : (per_sm > 4 ? 4 : per_sm);
+    return kRowSmemBudget / ctas / row_bytes >= 2;
+}
+
 cudaError_t launch_quant_token(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
                                int group, int transpose, int fmt, uint8_t *q, int64_t ld_q,
-                               uint8_t *s, int64_t ld_s, cudaStream_t stream) {
+                               uint8_t *s, int64_t ld_s, const WaitOpts &w, cudaStream_t stream) {
     if (rows == 0 || cols == 0) return cudaSuccess;
     if (transpose) {
         const dim3 grid(static_cast<unsigned>(cols / kTC), static_cast<unsigned>(rows / 128));
@@ -869,8 +890,8 @@ cudaError_t launch_quant_token(const uint16_t *x, int64_t rows, int64_t cols, in
     }
     if (group == 0) {
         return fmt == FMT_E4M3
-                   ? launch_row<FMT_E4M3, SCALE_UE8M0>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream)
-                   : launch_row<FMT_E5M2, SCALE_UE8M0>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream);
+                   ? launch_row<FMT_E4M3, SCALE_UE8M0>(x, rows, cols, ld_x, q, ld_q, s, ld_s, w, stream)
+                   : launch_row<FMT_E5M2, SCALE_UE8M0>(x, rows, cols, ld_x, q, ld_q, s, ld_s, w, stream);
     }
     if (cols * 2 <= 8192)   // short rows: one row per CTA, held in registers
         return fmt == FMT_E4M3
@@ -923,7 +944,7 @@ cudaError_t launch_quant_mx32_monitor(const uint16_t *x, int64_t rows, int64_t c
 cudaError_t launch_requant_t(const uint8_t *q, int64_t rows, int64_t cols, int64_t ld_q,
                              const uint8_t *s, int64_t ld_s, int per_token, int fmt_in,
                              int fmt_out, uint8_t *qt, int64_t ld_qt, uint8_t *st, int64_t ld_st,
-                             cudaStream_t stream) {
+                             const WaitOpts &w, cudaStream_t stream) {
     if (rows == 0 || cols == 0) return cudaSuccess;
     CUtensorMap tq;
     std::memset(&tq, 0, sizeof(tq));
@@ -954,8 +975,9 @@ cudaError_t launch_requant_t(const uint8_t *q, int64_t rows, int64_t cols, int64
         if (e != cudaSuccess) return e;
         int64_t grid = static_cast<int64_t>(num_sms()) * (per_sm > 0 ? per_sm : 1);
         if (grid > ntiles) grid = ntiles;
-        kern<<<static_cast<unsigned>(grid), 256, smem, stream>>>(tq, s, ld_s, step, tiles_x, ntiles,
-                                                                 qt, ld_qt, st, ld_st, err);
+        kern<<<static_cast<unsigned>(grid), 256, smem, stream>>>(
+            tq, s, ld_s, step, tiles_x, ntiles, qt, ld_qt, st, ld_st,
+            w.limit_ns ? w.limit_ns : kRqWaitNs, w.inject, err);
         return cudaGetLastError();
     };
     if (fmt_in == FMT_E4M3)
@@ -1003,8 +1025,8 @@ cudaError_t launch_quant_token_f32s(const uint16_t *x, int64_t rows, int64_t col
     uint8_t *s = reinterpret_cast<uint8_t *>(sf);
     if (group == 0)
         return fmt == FMT_E4M3
-                   ? launch_row<FMT_E4M3, SCALE_F32>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream)
-                   : launch_row<FMT_E5M2, SCALE_F32>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream);
+                   ? launch_row<FMT_E4M3, SCALE_F32>(x, rows, cols, ld_x, q, ld_q, s, ld_s, WaitOpts{}, stream)
+                   : launch_row<FMT_E5M2, SCALE_F32>(x, rows, cols, ld_x, q, ld_q, s, ld_s, WaitOpts{}, stream);
     if (cols * 2 <= 8192)
         return fmt == FMT_E4M3
                    ? launch_row_regs<FMT_E4M3, SCALE_F32, 16>(x, rows, cols, ld_x, q, ld_q, s, ld_s, stream)

@@ -380,11 +380,50 @@ int fp8_gemm_scaled_ex(int op, const fp8hg_operand *a, const fp8hg_operand *b, v
                        void *stream);
 
 /*
+ * Options of the quantizer and GEMM entry points whose kernels wait on
+ * copies (the per-token quantizer's row staging, the re-quantizer's tile
+ * ring, the FP32-scale GEMM's operand pipeline).  No passage: these exist to
+ * bound and test the library's own waits.
+ *   wait_limit_ns  upper bound on any single wait for a copy (0 = the
+ *                  default, 2 s).  When it runs out the kernel records
+ *                  FP8HG_ERR_TIMEOUT in the device error word, waits (bounded)
+ *                  for the copies it still has in flight and returns; the
+ *                  outputs are then unspecified.
+ *   inject_fault   0 = none.  1 = the first CTA never issues its first copy,
+ *                  so the wait for it can only run out: a host-chosen,
+ *                  GPU-safe way to exercise the timeout path in tests.
+ *   reserved       must be 0.
+ */
+typedef struct {
+    uint64_t wait_limit_ns;
+    int32_t inject_fault;
+    int32_t reserved;
+} fp8hg_wait_opts;
+
+/*
+ * fp8_quant_token, fp8_requant_t and fp8_gemm_scaled_f32s with wait options
+ * (opts may be NULL = defaults; an inject_fault outside {0, 1} is
+ * FP8HG_ERR_INVALID_ARG).  For fp8_quant_token_ex only the per-token
+ * quantizer of rows longer than 4096 elements waits on copies; asking it to
+ * inject a fault in any other configuration returns FP8HG_ERR_UNSUPPORTED.
+ */
+int fp8_quant_token_ex(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int group,
+                       int transpose, int fmt, uint8_t *q, int64_t ld_q, uint8_t *scale,
+                       int64_t ld_s, const fp8hg_wait_opts *opts, void *stream);
+int fp8_requant_t_ex(const uint8_t *q, int64_t rows, int64_t cols, int64_t ld_q,
+                     const uint8_t *scale, int64_t ld_s, int gran, int fmt_in, int fmt_out,
+                     uint8_t *q_t, int64_t ld_qt, uint8_t *scale_t, int64_t ld_st,
+                     const fp8hg_wait_opts *opts, void *stream);
+int fp8_gemm_scaled_f32s_ex(int op, const fp8hg_operand_f32s *a, const fp8hg_operand_f32s *b,
+                            void *c, int64_t ldc, int out, const fp8hg_wait_opts *opts,
+                            void *stream);
+
+/*
  * fp8hg_get_device_error — synchronizes `stream`, then reads and clears the
  * device error word of the current device.  Returns FP8HG_OK,
- * FP8HG_ERR_TIMEOUT (a bounded wait in a GEMM or per-token quantizer kernel
- * expired since the last call) or FP8HG_ERR_CUDA (the synchronization itself
- * failed).
+ * FP8HG_ERR_TIMEOUT (a bounded wait in a GEMM, the per-token quantizer or
+ * the re-quantizer expired since the last call) or FP8HG_ERR_CUDA (the
+ * synchronization itself failed).
  */
 int fp8hg_get_device_error(void *stream);
 

@@ -12,7 +12,8 @@ EXPECTED = {"fp8_quant_token", "fp8_quant_block128", "fp8_quant_mx32", "fp8_quan
             "fp8_requant_t", "fp8_gemm_scaled_q", "fp8_quant_token_f32s",
             "fp8_quant_block128_f32s", "fp8_gemm_scaled_f32s",
             "fp8_gemm_scaled",
-            "fp8_gemm_scaled_ex", "fp8hg_get_device_error", "fp8hg_status_str", "fp8hg_version"}
+            "fp8_gemm_scaled_ex", "fp8hg_get_device_error", "fp8hg_status_str", "fp8hg_version",
+            "fp8_quant_token_ex", "fp8_requant_t_ex", "fp8_gemm_scaled_f32s_ex"}
 
 OK, INVALID, ALIGN, SHAPE, UNSUP = 0, 1, 2, 3, 4
 FAKE = 0x10000  # never dereferenced: every call below fails validation first
@@ -181,3 +182,30 @@ def test_gemm_validation(lib):
     a = _op()
     a.fmt = 9
     assert call(a, _op(**blk)) == INVALID
+
+
+def test_wait_options_validation(lib):
+    """fp8hg_wait_opts: inject_fault in {0, 1}, reserved 0, and fault injection
+    only where the kernel waits on copies (per-token rows of more than 4096
+    elements for fp8_quant_token_ex)."""
+    W = fp8hg.WaitOpts
+    qx = lib.fp8_quant_token_ex
+
+    def tok(opts, cols=8192, group=0, transpose=0):
+        return qx(FAKE, 128, cols, cols, group, transpose, E4M3, FAKE, cols, FAKE,
+                  cols // 128, ctypes.byref(opts), None)
+
+    assert tok(W(0, 2, 0)) == INVALID
+    assert tok(W(0, 0, 1)) == INVALID                       # reserved
+    assert tok(W(0, 1, 0), cols=1024) == UNSUP               # 2 KB rows: register kernel, no wait
+    assert tok(W(0, 1, 0), group=128) == UNSUP               # 1x128: no wait
+    assert tok(W(0, 1, 0), group=128, transpose=1) == UNSUP  # transposed: no wait
+    assert qx(FAKE, 0, 8192, 8192, 0, 0, E4M3, FAKE, 8192, FAKE, 1,
+              ctypes.byref(W(5, 1, 0)), None) == OK           # empty: nothing launched
+    r = lib.fp8_requant_t_ex
+    assert r(FAKE, 256, 256, 256, FAKE, 2, GRAN_1x128, E4M3, E4M3, FAKE, 256, FAKE, 2,
+             ctypes.byref(W(0, 3, 0)), None) == INVALID
+    g = lib.fp8_gemm_scaled_f32s_ex
+    blk = dict(gran=GRAN_128x128, lds=2)
+    assert g(0, ctypes.byref(_op()), ctypes.byref(_op(**blk)), FAKE, 256, 0,
+             ctypes.byref(W(0, -1, 0)), None) == INVALID

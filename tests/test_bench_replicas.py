@@ -1,0 +1,44 @@
+"""bench.py --gpus N without a torchrun environment starts N replicas itself
+(one process per local GPU, torchrun's environment variables, 127.0.0.1
+rendezvous).  The launcher runs here with gloo stand-in ranks on the CPU."""
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_spawn_replicas_runs_n_ranks_and_one_line():
+    code = ("import sys, bench; sys.exit(bench.spawn_replicas(2, ['--steps', '3'], "
+            f"script={os.path.join(ROOT, 'tests', 'replica_worker.py')!r}))")
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("RANK", "LOCAL_RANK", "WORLD_SIZE", "MASTER_ADDR", "MASTER_PORT")}
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
+                       text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1                       # rank 0 alone prints
+    d = json.loads(lines[0])
+    assert d["n_gpus"] == 2 and d["local_ranks_seen"] == 2
+    assert d["ms_per_step"] == 15.0              # the slower rank sets the step time
+    assert abs(d["value"] - 2 * 1e12 / 15e-3 / 1e12) < 1e-9
+    assert d["argv"] == ["--steps", "3"] and d["master"] == "127.0.0.1"
+
+
+def test_gpus_flag_without_torchrun_dispatches_to_the_launcher(monkeypatch):
+    seen = {}
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.setattr(bench, "spawn_replicas", lambda n, argv: seen.update(n=n, argv=argv) or 0)
+    assert bench.main(["--gpus", "4", "--steps", "2"]) == 0
+    assert seen == {"n": 4, "argv": ["--gpus", "4", "--steps", "2"]}
+
+
+def test_a_rank_under_torchrun_does_not_spawn(monkeypatch):
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setattr(bench, "spawn_replicas", lambda *a: (_ for _ in ()).throw(AssertionError))
+    monkeypatch.setattr(bench, "run_reference", lambda args: None)
+    assert bench.main(["--gpus", "2", "--impl", "reference"]) == 0

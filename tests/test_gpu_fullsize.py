@@ -30,7 +30,9 @@ def data(cuda_lib):
     dev = torch.device("cuda", 0)
     mk = lambda kind, r, c, n: workloads.make_tensor(kind, r, c, 2, n, device=dev)
     d = {"H": mk("act", M, MLP, "H"), "X": mk("act", M, HID, "X"),
-         "W_down": mk("weight", HID, MLP, "W_down"), "dY_gate": mk("grad", M, MLP, "dY_gate")}
+         "W_down": mk("weight", HID, MLP, "W_down"), "dY_gate": mk("grad", M, MLP, "dY_gate"),
+         "dY_down": mk("grad", M, HID, "dY_down"), "W_gate": mk("weight", MLP, HID, "W_gate"),
+         "W_up": mk("weight", MLP, HID, "W_up"), "dY_up": mk("grad", M, MLP, "dY_up")}
     yield d
     del d
     torch.cuda.empty_cache()
@@ -120,3 +122,65 @@ def test_wgrad_gemm_full_size(data):
                                          I.ravel(), J.ravel())
     g = dw[torch.from_numpy(ii).cuda()][:, torch.from_numpy(jj).cuda()].cpu().numpy().ravel()
     check_gemm(g, c_ref, s_abs, "wgrad")
+
+
+def _dgrad_ref(dy, w, ii, b, jj, fmt_dy):
+    """Oracle C_ref, S for dX[ii, 128 b + jj] of dX = dY W: A = dY rows ii
+    quantized per token, B rows = columns 128b..128b+127 of W, i.e. the
+    transposed copy of W's 128x128 blocks in that block column."""
+    qa, sa = oracle.quant_token(_bits(dy[torch.from_numpy(ii).cuda()]), 0, fmt_dy)
+    _, _, qbt, sbt = oracle.quant_block128(_bits(w[:, 128 * b:128 * b + 128]), E4M3,
+                                           transposed_copy=True)
+    I, J = np.meshgrid(np.arange(len(ii)), jj, indexing="ij")
+    return oracle.gemm_ref_pairs(qa, sa, GRAN_ROW, fmt_dy, qbt, sbt, GRAN_128x128, E4M3,
+                                 I.ravel(), J.ravel())
+
+
+def test_dgrad_down_gemm_full_size(data):
+    """dH = dY_down W_down as the step runs it: A = dY_down [16384, 3584] per
+    token E5M2, B = W_down^T [18944, 3584] (the transposed block copy);
+    contraction 3584, N = 18944, BF16 out; 192 sampled outputs."""
+    dy, w = data["dY_down"], data["W_down"]
+    a = fp8hg.fp8_quant_token(dy, 0, E5M2)
+    _, bt = fp8hg.fp8_quant_block128(w, E4M3, transposed_copy=True)
+    dh = fp8hg.fp8_gemm_scaled(fp8hg.DGRAD, a, bt)
+    assert dh.shape == (M, MLP)
+    assert fp8hg.fp8hg_get_device_error() == 0
+    rng = np.random.default_rng(5)
+    ii = np.concatenate([[0, M - 1], rng.choice(np.arange(1, M - 1), 10, replace=False)])
+    c_gpu, c_ref, s_abs = [], [], []
+    for b in [0, MLP // 128 - 1] + list(rng.choice(np.arange(1, MLP // 128 - 1), 2, replace=False)):
+        jj = np.concatenate([[0, 127], rng.choice(np.arange(1, 127), 2, replace=False)])
+        c, s = _dgrad_ref(dy, w, ii, int(b), jj, E5M2)
+        c_ref.append(c)
+        s_abs.append(s)
+        g = dh[torch.from_numpy(ii).cuda()][:, torch.from_numpy(128 * int(b) + jj).cuda()]
+        c_gpu.append(g.float().cpu().numpy().ravel())
+    check_gemm(np.concatenate(c_gpu), np.concatenate(c_ref), np.concatenate(s_abs), "dgrad down")
+
+
+def test_dgrad_accumulate_full_size(data):
+    """dX = dY_gate W_gate + dY_up W_up in BF16, the second product accumulated
+    onto the first (C += A B^T) exactly as the step launches it: contraction
+    18944, N = 3584.  The stored first product is rounded to BF16 once more
+    before the sum, which the |C_ref(gate)| term of the tolerance covers."""
+    dyg, dyu, wg, wu = data["dY_gate"], data["dY_up"], data["W_gate"], data["W_up"]
+    ag, au = fp8hg.fp8_quant_token(dyg, 0, E5M2), fp8hg.fp8_quant_token(dyu, 0, E5M2)
+    _, btg = fp8hg.fp8_quant_block128(wg, E4M3, transposed_copy=True)
+    _, btu = fp8hg.fp8_quant_block128(wu, E4M3, transposed_copy=True)
+    dx = fp8hg.fp8_gemm_scaled(fp8hg.DGRAD, ag, btg)
+    fp8hg.fp8_gemm_scaled(fp8hg.DGRAD, au, btu, out=dx, accumulate=True)
+    assert fp8hg.fp8hg_get_device_error() == 0
+    rng = np.random.default_rng(6)
+    ii = np.concatenate([[0, M - 1], rng.choice(np.arange(1, M - 1), 8, replace=False)])
+    c_gpu, c_ref, s_abs = [], [], []
+    for b in [0, HID // 128 - 1, int(rng.integers(1, HID // 128 - 1))]:
+        jj = np.concatenate([[0, 127], rng.choice(np.arange(1, 127), 2, replace=False)])
+        r1, s1 = _dgrad_ref(dyg, wg, ii, b, jj, E5M2)
+        r2, s2 = _dgrad_ref(dyu, wu, ii, b, jj, E5M2)
+        c_ref.append(r1 + r2)
+        s_abs.append(s1 + s2 + np.abs(r1))
+        g = dx[torch.from_numpy(ii).cuda()][:, torch.from_numpy(128 * b + jj).cuda()]
+        c_gpu.append(g.float().cpu().numpy().ravel())
+    check_gemm(np.concatenate(c_gpu), np.concatenate(c_ref), np.concatenate(s_abs),
+               "dgrad accumulate")

@@ -39,6 +39,11 @@ CASES = [
     (WGRAD, (GRAN_1x128, E5M2, "grad"), (GRAN_1x128, E4M3, "act"), 256, 256, 1024),
     (FPROP, (GRAN_MX32, E4M3, "mx_ln"), (GRAN_MX32, E4M3, "mx_ln"), 256, 512, 512),
     (FPROP, (GRAN_MX32, E5M2, "mx_ln_clamp"), (GRAN_MX32, E4M3, "normal"), 128, 384, 256),
+    # E5M2 on the B side (instruction-descriptor bits 10-12), alone and with E5M2 A
+    (FPROP, (GRAN_ROW, E4M3, "act"), (GRAN_128x128, E5M2, "weight"), 256, 384, 512),
+    (WGRAD, (GRAN_1x128, E4M3, "act"), (GRAN_1x128, E5M2, "grad"), 256, 640, 640),
+    (DGRAD, (GRAN_ROW, E5M2, "grad"), (GRAN_128x128, E5M2, "weight"), 512, 256, 384),
+    (FPROP, (GRAN_MX32, E4M3, "normal"), (GRAN_MX32, E5M2, "mx_ln"), 256, 256, 384),
 ]
 
 
@@ -83,19 +88,23 @@ def test_gemm_accumulate(cuda_lib, tile, out_dtype):
 
 
 @pytest.mark.parametrize("tile", TILES)
-def test_gemm_unit_scales_exact(cuda_lib, tile):
+@pytest.mark.parametrize("fmt_a,fmt_b", [(E4M3, E4M3), (E4M3, E5M2), (E5M2, E5M2)])
+def test_gemm_unit_scales_exact(cuda_lib, tile, fmt_a, fmt_b):
     """Small-integer codes with unit scales: the product is an exact integer
-    matrix that FP32 accumulation represents exactly."""
+    matrix that FP32 accumulation represents exactly.  Every integer in
+    [-8, 8] is exact in both encodings, so a wrong format field decodes
+    different values and breaks the equality."""
     rng = np.random.default_rng(0)
     ints = np.arange(-8, 9)
-    codes = torch.tensor(ints, dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    f8 = {E4M3: torch.float8_e4m3fn, E5M2: torch.float8_e5m2}
+    enc = lambda f: torch.tensor(ints, dtype=torch.float32).to(f8[f]).view(torch.uint8).numpy()
     M, N, K = 256, 256, 256
     ia, ib = rng.integers(0, 17, (M, K)), rng.integers(0, 17, (N, K))
-    qa, qb = codes[ia], codes[ib]
+    qa, qb = enc(fmt_a)[ia], enc(fmt_b)[ib]
     sa = np.full((M, K // 128), 127, np.uint8)
     sb = np.full((N // 128, K // 128), 127, np.uint8)
-    c = fp8hg.fp8_gemm_scaled(FPROP, to_qtensor(qa, sa, E4M3, GRAN_1x128),
-                              to_qtensor(qb, sb, E4M3, GRAN_128x128), out_dtype=torch.float32,
+    c = fp8hg.fp8_gemm_scaled(FPROP, to_qtensor(qa, sa, fmt_a, GRAN_1x128),
+                              to_qtensor(qb, sb, fmt_b, GRAN_128x128), out_dtype=torch.float32,
                               tile=tile)
     exact = ints[ia].astype(np.int64) @ ints[ib].astype(np.int64).T
     assert np.array_equal(c.cpu().numpy().astype(np.int64), exact)

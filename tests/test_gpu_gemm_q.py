@@ -15,7 +15,7 @@ import pytest
 import torch
 
 import oracle
-from oracle import E4M3, E5M2, GRAN_ROW, GRAN_1x128, GRAN_128x128
+from oracle import E4M3, E5M2, GRAN_ROW, GRAN_1x128, GRAN_128x128, GRAN_MX32
 import fp8_hybrid_granularity_gb300 as fp8hg
 from fp8_hybrid_granularity_gb300 import workloads
 from helpers import np_u8, to_qtensor, assert_codes_equal, oracle_quant, check_gemm
@@ -133,3 +133,42 @@ def test_1p5b_gate_sampled_rows(cuda_lib):
                                          GRAN_128x128, E4M3, I.ravel(), J.ravel())
     check_quantized_output(codes, scales, c_ref.reshape(len(rows), 8960),
                            s_abs.reshape(len(rows), 8960), E4M3, "1.5B gate")
+
+
+@pytest.mark.parametrize("fmt_c", [E4M3, E5M2])
+def test_mx32_operands_exact_products(cuda_lib, fmt_c):
+    """MX32 x MX32 operands (the G = 4 instantiation of the quantized epilogue):
+    codes -1 / 0 / +1 and per-32-K scale bytes that are the row's byte in every
+    block, so C is exact in FP32 and BF16 and its quantization must equal the
+    oracle's bit for bit; a wrong scale slot or byte changes C by a power of two."""
+    rng = np.random.default_rng(60 + fmt_c)
+    M, N, K = 256, 384, 256
+    qa, sa_row, qb, sb_blk = _int_operands(rng, M, N, K)
+    sa = np.repeat(sa_row, K // 32, axis=1)                      # [M, K/32]
+    sb = np.repeat(np.repeat(sb_blk[:, :1], 128, axis=0), K // 32, axis=1)  # [N, K/32]
+    a = to_qtensor(qa, sa, E4M3, GRAN_MX32)
+    b = to_qtensor(qb, sb, E4M3, GRAN_MX32)
+    out = fp8hg.fp8_gemm_scaled_q(fp8hg.FPROP, a, b, fmt_c)
+    assert fp8hg.fp8hg_get_device_error() == 0
+    c_ref, _ = oracle.gemm_ref_dense(oracle.dequant(qa, sa, GRAN_MX32, E4M3),
+                                     oracle.dequant(qb, sb, GRAN_MX32, E4M3))
+    qo, so = oracle.quant_token(_bf16_exact(c_ref), 128, fmt_c)
+    assert_codes_equal(np_u8(out.codes), qo, "codes")
+    assert_codes_equal(np_u8(out.scales()), so, "scales")
+
+
+@pytest.mark.parametrize("fmt_c", [E4M3, E5M2])
+def test_mx32_operands_tolerance(cuda_lib, fmt_c):
+    """MX32 x MX32 on the MX workload's layer-norm-like and normal rows (scales
+    that differ from block to block along K), C quantized in the epilogue."""
+    M, N, K = 256, 256, 512
+    xa = workloads.bf16_bits(workloads.make_tensor("mx_ln", M, K, 61, "qa"))
+    xb = workloads.bf16_bits(workloads.make_tensor("normal", N, K, 62, "qb"))
+    qa, sa = oracle_quant(xa, GRAN_MX32, E4M3)
+    qb, sb = oracle_quant(xb, GRAN_MX32, E5M2)
+    out = fp8hg.fp8_gemm_scaled_q(fp8hg.FPROP, to_qtensor(qa, sa, E4M3, GRAN_MX32),
+                                  to_qtensor(qb, sb, E5M2, GRAN_MX32), fmt_c)
+    assert fp8hg.fp8hg_get_device_error() == 0
+    c_ref, s_abs = oracle.gemm_ref_dense(oracle.dequant(qa, sa, GRAN_MX32, E4M3),
+                                         oracle.dequant(qb, sb, GRAN_MX32, E5M2))
+    check_quantized_output(np_u8(out.codes), np_u8(out.scales()), c_ref, s_abs, fmt_c, "mx32")
