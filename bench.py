@@ -31,7 +31,7 @@ quantization pass inside the timed region); the sweep's is the quantizers'
 algorithmic bytes over their time (GB/s).  Inputs are seeded synthetic BF16
 tensors resident in HBM.  The JSON line carries the roofline of the dominant
 kernel against a dense FP8 peak measured in the same run (cuBLAS E4M3 8192^3
-through torch._scaled_mm, best of 10), the quantizers' GB/s against the
+through torch._scaled_mm, best of 20), the quantizers' GB/s against the
 measured HBM copy rate, an end-to-end figure with host buffers, the SM clocks
 seen, and the CPU oracle's rate on a bounded sample of the same work.
 
@@ -84,6 +84,8 @@ def _parse(argv=None):
     ap.add_argument("--m", type=int, default=4096, help="tokens of a --kernel case")
     ap.add_argument("--n", type=int, default=HID, help="N of the gemm_shape case")
     ap.add_argument("--k", type=int, default=MLP, help="K of the gemm_shape case")
+    ap.add_argument("--tile", type=int, default=0,
+                    help="GEMM tile of a --kernel case (0 = the library's choice; see fp8hg_gemm_opts)")
     return ap.parse_args(argv)
 
 
@@ -229,6 +231,10 @@ def _tok_bytes(n_el, rows):        # per token: 2 B read + 1 B written + 1 B per
 
 def _g128_bytes(n_el):             # 1x128 groups (either direction): + 1 B per 128
     return 3.0 * n_el + n_el / 128.0
+
+
+def _dual_bytes(n_el, rows):       # one read, both outputs: 2 + 1 + 1 B per element + scales
+    return 4.0 * n_el + rows + n_el / 128.0
 
 
 def _blk_bytes(n_el, transposed):  # 128x128 blocks (+ transposed copy and its scales)
@@ -429,7 +435,7 @@ STEPS = {"linear_step_7b": LinearStep7B, "fprop_1p5b": Fprop1p5B, "tiny_fprop": 
 def fp8_peak_probe(torch, dev, n=8192, sustain_s=4.0):
     """Dense FP8 peak of this GPU, measured: cuBLAS E4M3 x E4M3 -> BF16 at
     n^3 through torch._scaled_mm (tensor-wise unit scales).  Burst = best of
-    10 single launches; sustained = back-to-back launches for ~sustain_s
+    20 single launches; sustained = back-to-back launches for ~sustain_s
     seconds, with the SM clocks sampled meanwhile.  None if unavailable."""
     try:
         a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
@@ -443,7 +449,7 @@ def fp8_peak_probe(torch, dev, n=8192, sustain_s=4.0):
         flop = 2.0 * n ** 3
         clk = ClockSampler(dev.index or 0, period_ms=20).start()
         best = float("inf")
-        for _ in range(10):
+        for _ in range(20):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             f()
@@ -465,7 +471,7 @@ def fp8_peak_probe(torch, dev, n=8192, sustain_s=4.0):
                 "burst_ms": best, "sustained_launches": iters, "burst_clocks": burst_clk,
                 "sustained_clocks": sus_clk,
                 "how": f"cuBLAS E4M3 x E4M3 -> BF16, {n}^3, torch._scaled_mm with tensor-wise unit "
-                       f"scales: best of 10 launches (burst) and {iters} back-to-back launches (sustained)"}
+                       f"scales: best of 20 launches (burst) and {iters} back-to-back launches (sustained)"}
     except Exception as e:   # reported in the line; the fallback denominator is used
         return {"error": repr(e)}
 
@@ -1098,6 +1104,8 @@ KERNEL_CASES = {
     "quant_row": "per-token quantization of H [M, 18944]",
     "quant_1x128": "1x128 quantization of H [M, 18944]",
     "quant_t": "1x128-along-tokens transposed quantization of H [M, 18944]",
+    "quant_dual": "both quantizations of H [M, 18944] (per token, 1x128 along tokens "
+                  "transposed) from one read",
     "block128": "128x128 quantization (+ transposed copy) of W_down [3584, 18944]",
     "mx32": "MXFP8 quantization of [M, 4096]",
     "mx32_mon": "MXFP8 quantization of [M, 4096] with the clamp monitor's counts",
@@ -1124,7 +1132,7 @@ def run_kernel_case(args):
         y = torch.empty((M, HID), dtype=bf, device=dev)
         if c == "gemm_down":
             a, b = fp8hg.fp8_quant_token(h, 0, E4), fp8hg.fp8_quant_block128(w, E4)
-            fn = lambda: fp8hg.fp8_gemm_scaled(fp8hg.FPROP, a, b, out=y)
+            fn = lambda: fp8hg.fp8_gemm_scaled(fp8hg.FPROP, a, b, out=y, tile=args.tile)
         else:
             a, b = fp8hg.fp8_quant_token_f32s(h, 0, E4), fp8hg.fp8_quant_block128_f32s(w, E4)
             fn = lambda: fp8hg.fp8_gemm_scaled_f32s(fp8hg.FPROP, a, b, out=y)
@@ -1134,7 +1142,7 @@ def run_kernel_case(args):
         a, b = fp8hg.fp8_quant_token(x, 0, E4), fp8hg.fp8_quant_block128(w, E4)
         if c == "gemm_gate":
             y = torch.empty((M, MLP), dtype=bf, device=dev)
-            fn = lambda: fp8hg.fp8_gemm_scaled(fp8hg.FPROP, a, b, out=y)
+            fn = lambda: fp8hg.fp8_gemm_scaled(fp8hg.FPROP, a, b, out=y, tile=args.tile)
         else:
             yq = fp8hg.alloc_token(M, MLP, 128, E4, False, dev)
             fn = lambda: fp8hg.fp8_gemm_scaled_q(fp8hg.FPROP, a, b, E4, out=yq)
@@ -1143,20 +1151,28 @@ def run_kernel_case(args):
         dy, x = mk("grad", M, MLP, "dY"), mk("act", M, HID, "X")
         a, b = fp8hg.fp8_quant_token(dy, 128, E5, True), fp8hg.fp8_quant_token(x, 128, E4, True)
         y = torch.empty((MLP, HID), dtype=torch.float32, device=dev)
-        fn = lambda: fp8hg.fp8_gemm_scaled(fp8hg.WGRAD, a, b, out=y)
+        fn = lambda: fp8hg.fp8_gemm_scaled(fp8hg.WGRAD, a, b, out=y, tile=args.tile)
         work, unit = 2.0 * M * HID * MLP, "flop"
     elif c == "gemm_shape":
         x, w = mk("act", M, args.k, "X"), mk("weight", args.n, args.k, "W")
         a, b = fp8hg.fp8_quant_token(x, 0, E4), fp8hg.fp8_quant_block128(w, E4)
         y = torch.empty((M, args.n), dtype=bf, device=dev)
-        fn = lambda: fp8hg.fp8_gemm_scaled(fp8hg.FPROP, a, b, out=y)
+        fn = lambda: fp8hg.fp8_gemm_scaled(fp8hg.FPROP, a, b, out=y, tile=args.tile)
         work, unit = 2.0 * M * args.n * args.k, "flop"
     elif c == "gemm_mx":
         xa, xb = mk("mx_ln", M, 4096, "A"), mk("mx_ln", 4096, 4096, "B")
         a, b = fp8hg.fp8_quant_mx32(xa, E4), fp8hg.fp8_quant_mx32(xb, E4)
         y = torch.empty((M, 4096), dtype=bf, device=dev)
-        fn = lambda: fp8hg.fp8_gemm_scaled(fp8hg.FPROP, a, b, out=y)
+        fn = lambda: fp8hg.fp8_gemm_scaled(fp8hg.FPROP, a, b, out=y, tile=args.tile)
         work, unit = 2.0 * M * 4096 * 4096, "flop"
+    elif c == "quant_dual":
+        h = mk("act", M, MLP, "H")
+        n = h.numel()
+        o = fp8hg.alloc_token(M, MLP, 0, E4, False, dev)
+        ot = fp8hg.alloc_token(M, MLP, 128, E4, True, dev)
+        ws = fp8hg.dual_workspace(M, MLP, dev)
+        fn = lambda: fp8hg.fp8_quant_token_dual(h, E4, out=o, out_t=ot, workspace=ws)
+        work, unit = _dual_bytes(n, M), "bytes"
     elif c in ("quant_row", "quant_1x128", "quant_t", "requant"):
         h = mk("act", M, MLP, "H")
         n = h.numel()

@@ -9,6 +9,7 @@ missing or fails to load, every call raises.
 Tensor-level API (same names as the C entry points):
 
   fp8_quant_token(x, group=0|128, fmt, transpose=False) -> QTensor
+  fp8_quant_token_dual(x, fmt, fmt_t)                   -> QTensor, QTensor^T (one read)
   fp8_quant_block128(x, fmt, transposed_copy=False)     -> QTensor[, QTensor]
   fp8_quant_mx32(x, fmt, clamp_count=None)              -> QTensor
   fp8_quant_mx32_monitor(x, fmt, stats=None, row_saturated=None) -> QTensor, stats
@@ -100,6 +101,10 @@ def load_library(build_if_stale: bool = True):
         P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         lib.fp8_quant_token.argtypes = [P, I64, I64, I64, I, I, I, P, I64, P, I64, P]
         lib.fp8_quant_token_ex.argtypes = [P, I64, I64, I64, I, I, I, P, I64, P, I64, P, P]
+        lib.fp8_quant_token_dual.argtypes = [P, I64, I64, I64, I, P, I64, P, I64, I, P, I64, P,
+                                             I64, P, ctypes.c_size_t, P, P]
+        lib.fp8_quant_token_dual_workspace.argtypes = [I64, I64]
+        lib.fp8_quant_token_dual_workspace.restype = ctypes.c_size_t
         lib.fp8_requant_t_ex.argtypes = [P, I64, I64, I64, P, I64, I, I, I, P, I64, P, I64, P, P]
         lib.fp8_gemm_scaled_f32s_ex.argtypes = [I, ctypes.POINTER(Operand),
                                                 ctypes.POINTER(Operand), P, I64, I, P, P]
@@ -124,7 +129,8 @@ def load_library(build_if_stale: bool = True):
         lib.fp8hg_status_str.argtypes = [I]
         for fn in ("fp8_quant_token", "fp8_quant_block128", "fp8_quant_mx32", "fp8_gemm_scaled",
                    "fp8_gemm_scaled_ex", "fp8hg_get_device_error", "fp8hg_version",
-                   "fp8_quant_token_ex", "fp8_requant_t_ex", "fp8_gemm_scaled_f32s_ex"):
+                   "fp8_quant_token_ex", "fp8_requant_t_ex", "fp8_gemm_scaled_f32s_ex",
+                   "fp8_quant_token_dual"):
             getattr(lib, fn).restype = I
         _lib = lib
         return lib
@@ -199,6 +205,36 @@ def fp8_quant_token(x, group: int = 0, fmt: int = E4M3, transpose: bool = False,
                                   _stream(stream))
     _check(rc, "fp8_quant_token")
     return out
+
+
+def dual_workspace(rows: int, cols: int, device="cuda"):
+    """Scratch for fp8_quant_token_dual on [rows, cols] (a uint8 CUDA tensor)."""
+    import torch
+    n = int(lib().fp8_quant_token_dual_workspace(rows, cols))
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def fp8_quant_token_dual(x, fmt: int = E4M3, fmt_t: Optional[int] = None,
+                         out: Optional[QTensor] = None, out_t: Optional[QTensor] = None,
+                         workspace=None, stream=None, wait_limit_ns: int = 0,
+                         inject_fault: int = 0):
+    """Per-token codes (as fp8_quant_token(x, 0, fmt)) and transposed 1x128
+    codes along the tokens (as fp8_quant_token(x, 128, fmt_t, transpose=True))
+    from one read of x.  Returns (QTensor, QTensor).  workspace: optional
+    tensor from dual_workspace (allocated per call if None)."""
+    _check_bf16(x)
+    rows, cols = x.shape
+    fmt_t = fmt if fmt_t is None else fmt_t
+    out = out if out is not None else alloc_token(rows, cols, 0, fmt, False, x.device)
+    out_t = out_t if out_t is not None else alloc_token(rows, cols, 128, fmt_t, True, x.device)
+    ws = workspace if workspace is not None else dual_workspace(rows, cols, x.device)
+    rc = lib().fp8_quant_token_dual(
+        _ptr(x), rows, cols, x.stride(0), fmt, _ptr(out.codes), out.codes.stride(0),
+        _ptr(out.scale), out.scale.stride(0), fmt_t, _ptr(out_t.codes), out_t.codes.stride(0),
+        _ptr(out_t.scale), out_t.scale.stride(0), _ptr(ws), ws.numel() * ws.element_size(),
+        _wait_opts(wait_limit_ns, inject_fault), _stream(stream))
+    _check(rc, "fp8_quant_token_dual")
+    return out, out_t
 
 
 def fp8_quant_block128(x, fmt: int = E4M3, transposed_copy: bool = False, out=None,

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libfp8hg.so")
-SOURCES = ["api.cu", "quant.cu", "gemm.cu", "gemm_f32s.cu"]
+SOURCES = ["api.cu", "quant.cu", "quant_dual.cu", "gemm.cu", "gemm_f32s.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

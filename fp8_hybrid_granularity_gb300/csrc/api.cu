@@ -3,6 +3,7 @@
 // except fp8hg_get_device_error.
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <cstdint>
 
 #include "../../include/fp8hg.h"
@@ -163,6 +164,35 @@ int fp8_quant_token(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
                               nullptr, stream);
 }
 
+size_t fp8_quant_token_dual_workspace(int64_t rows, int64_t cols) {
+    if (rows <= 0 || cols <= 0) return 0;
+    return fp8hg::dual_workspace_bytes(rows, cols);
+}
+
+int fp8_quant_token_dual(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
+                         uint8_t *q, int64_t ld_q, uint8_t *scale, int64_t ld_s, int fmt_t,
+                         uint8_t *q_t, int64_t ld_qt, uint8_t *scale_t, int64_t ld_st,
+                         void *workspace, size_t workspace_bytes, const fp8hg_wait_opts *opts,
+                         void *stream) {
+    fp8hg::WaitOpts w;
+    int st = wait_opts(opts, w);
+    if (st != FP8HG_OK) return st;
+    st = check_quant_common(x, rows, cols, ld_x, fmt, q, ld_q, scale);
+    if (st != FP8HG_OK) return st;
+    if (!valid_fmt(fmt_t)) return FP8HG_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return FP8HG_OK;
+    if (!q_t || !scale_t || !workspace) return FP8HG_ERR_INVALID_ARG;
+    if (!aligned(q_t, 16) || ld_qt % 16 || !aligned(workspace, 16)) return FP8HG_ERR_ALIGNMENT;
+    if (rows % 128 || cols % 128) return FP8HG_ERR_SHAPE;
+    if (rows > (int64_t(1) << 31) || cols > (int64_t(1) << 31)) return FP8HG_ERR_SHAPE;
+    if (ld_x < cols || ld_q < cols || ld_s < 1 || ld_qt < rows || ld_st < rows / 128)
+        return FP8HG_ERR_INVALID_ARG;
+    if (workspace_bytes < fp8hg::dual_workspace_bytes(rows, cols)) return FP8HG_ERR_INVALID_ARG;
+    return status_from_cuda(fp8hg::launch_quant_dual(
+        x, rows, cols, ld_x, fmt, q, ld_q, scale, ld_s, fmt_t, q_t, ld_qt, scale_t, ld_st,
+        static_cast<unsigned int *>(workspace), w, static_cast<cudaStream_t>(stream)));
+}
+
 int fp8_quant_block128(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
                        uint8_t *q, int64_t ld_q, uint8_t *scale, int64_t ld_s, uint8_t *q_t,
                        int64_t ld_qt, uint8_t *scale_t, int64_t ld_st, void *stream) {
@@ -255,8 +285,8 @@ int fp8_gemm_scaled_ex(int op, const fp8hg_operand *a, const fp8hg_operand *b, v
     if (ldc < b->rows) return FP8HG_ERR_INVALID_ARG;
     if (ldc % (out == FP8HG_OUT_BF16 ? 8 : 4)) return FP8HG_ERR_ALIGNMENT;
     if (opts && (opts->inject_fault < 0 || opts->inject_fault > 1)) return FP8HG_ERR_INVALID_ARG;
-    if (opts && (opts->tile < 0 || opts->tile > 2)) return FP8HG_ERR_INVALID_ARG;
-    if (opts && opts->tile == 2 && a->rows % 256) return FP8HG_ERR_UNSUPPORTED;
+    if (opts && (opts->tile < 0 || opts->tile > 3)) return FP8HG_ERR_INVALID_ARG;
+    if (opts && opts->tile >= 2 && a->rows % 256) return FP8HG_ERR_UNSUPPORTED;
     g.c = c;
     g.ldc = ldc;
     g.out_fp32 = out == FP8HG_OUT_FP32;

@@ -954,6 +954,383 @@ __global__ void __launch_bounds__(W_THREADS, 1)
     }
 }
 
+// ---------------------------------------------------------- CTA-pair variant
+// Tile 256 x 256 computed by a pair of CTAs (a cluster of two) with
+// tcgen05.mma.cta_group::2: each CTA holds its 128 rows of A and its half
+// (128 rows) of B in its own shared memory, the MMA issued by the even CTA
+// reads both, and each CTA's tensor memory receives its 128 rows of the
+// accumulator.  A stage is then 32 KB per CTA for 128 x 256 x 128 MACs per
+// SM (the 128 x 256 kernel needs 48 KB for the same work), so six stages fit:
+// five stages of operand loads in flight while one is consumed, against two
+// in the 256 x 224 kernel, to hide the latency of a loaded L2.
+//   Both CTAs: warp 0 TMA producer (its own A and B halves; completion counted
+//   on the even CTA's stage barrier), warp 2 scale loader (its 128 A rows and
+//   all 256 B rows into its own shared memory; arrivals on the even CTA's
+//   barrier), warps 4-7 epilogue of its 128 rows.  Even CTA: warp 1 issues the
+//   scale-factor copies and MMAs for the pair and commits to both CTAs'
+//   barriers.  Tensor memory (both CTAs): accumulator columns 0-255, then per
+//   stage 4 columns of A scales and 8 of B scales.
+constexpr int PR_BM = 256, PR_BN = 256, PR_STAGES = 6;
+constexpr uint32_t PR_A_TILE = 128 * BK;   // per CTA
+constexpr uint32_t PR_B_TILE = 128 * BK;   // per CTA (its half of B)
+constexpr uint32_t PR_SFA_TILE = 512, PR_SFB_TILE = 1024;
+constexpr uint32_t PR_SFA_COL = 256;                     // + 4 * stage
+constexpr uint32_t PR_SFB_COL = 256 + 4 * PR_STAGES;     // + 8 * stage
+constexpr uint32_t PR_OFF_A = 0;
+constexpr uint32_t PR_OFF_B = PR_OFF_A + PR_STAGES * PR_A_TILE;
+constexpr uint32_t PR_OFF_SFA = PR_OFF_B + PR_STAGES * PR_B_TILE;
+constexpr uint32_t PR_OFF_SFB = PR_OFF_SFA + PR_STAGES * PR_SFA_TILE;
+constexpr uint32_t PR_OFF_BAR = PR_OFF_SFB + PR_STAGES * PR_SFB_TILE;
+// barriers from PR_OFF_BAR (8 bytes each): full[6] at 0 (operand bytes of both
+// CTAs; even CTA), empty[6] at 48 (each CTA), sf[6] at 96 (scale words of both
+// CTAs, one arrival per scale warp; even CTA), tfull 144 (each CTA), tempty
+// 152 (one arrival per epilogue warp of both CTAs; even CTA), drain 160.
+// Cross-CTA arrivals carry cluster-scope release semantics, so each warp
+// arrives once, after __syncwarp, rather than once per lane.
+constexpr uint32_t PR_BAR_EMPTY = 48, PR_BAR_SF = 96, PR_BAR_TFULL = 144, PR_BAR_TEMPTY = 152,
+                   PR_BAR_DRAIN = 160;
+constexpr uint32_t PR_OFF_TMEM_SLOT = PR_OFF_BAR + 168;
+constexpr uint32_t PR_OFF_ABORT = PR_OFF_BAR + 172;
+constexpr uint32_t PR_OFF_EPI = PR_OFF_BAR + 256;
+constexpr uint32_t PR_SMEM_BYTES = PR_OFF_EPI + 4 * EPI_WARP_BYTES + 1024;
+static_assert(PR_SFB_COL + 8 * PR_STAGES <= TMEM_COLS, "tensor memory overflow");
+static_assert(PR_SMEM_BYTES <= 232448, "shared memory overflow");
+
+// Wait on a barrier of this CTA whose arrivals may come from the other CTA of
+// the pair (acquire at cluster scope); bounded like wait_phase.
+__device__ bool wait_phase_pair(uint32_t bar, uint32_t parity, uint64_t limit,
+                                volatile uint32_t *abort_flag, unsigned int *err, uint32_t who,
+                                bool check_abort = true) {
+    if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    uint32_t it = 0;
+    while (true) {
+        if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
+        if ((++it & 15u) == 0) {
+            if (check_abort && *abort_flag) return false;
+            if (ptx::globaltimer() - t0 > limit) {
+                if (check_abort) {
+                    *abort_flag = 1u;
+                    atomicOr(err, 1u);
+                    atomicCAS(err + 1, 0u, who);
+                }
+                return false;
+            }
+        }
+    }
+}
+
+// Pair tile t -> (m-block of 256 rows, n-block of 256 columns); the same
+// grouped order as the other kernels.
+template <int G>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_gemm_pair(const __grid_constant__ CUtensorMap tmap_a,
+                const __grid_constant__ CUtensorMap tmap_b, const KParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    const uint32_t sA = base + PR_OFF_A, sB = base + PR_OFF_B;
+    const uint32_t sSFA = base + PR_OFF_SFA, sSFB = base + PR_OFF_SFB, sBAR = base + PR_OFF_BAR;
+    const uint32_t empty = sBAR + PR_BAR_EMPTY, sfbar = sBAR + PR_BAR_SF;
+    const uint32_t tfull = sBAR + PR_BAR_TFULL, tempty = sBAR + PR_BAR_TEMPTY,
+                   drain = sBAR + PR_BAR_DRAIN;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + PR_OFF_TMEM_SLOT);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + PR_OFF_ABORT);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_ctarank();   // 0: issues the pair's MMAs
+    const bool leader = rank == 0;
+    const int pair = static_cast<int>(blockIdx.x >> 1), npairs = static_cast<int>(gridDim.x >> 1);
+    const uint64_t limit = p.wait_limit_ns;
+    const uint64_t drain_limit = 2000000ull;
+    // the even CTA's barriers, as seen from either CTA
+    const uint32_t full_l = ptx::map_shared_rank(sBAR, 0);
+    const uint32_t sf_l = ptx::map_shared_rank(sfbar, 0);
+    const uint32_t tempty_l = ptx::map_shared_rank(tempty, 0);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < PR_STAGES; ++s) {
+            ptx::mbar_init(sBAR + 8 * s, 1);        // even CTA's expect_tx (both CTAs' bytes)
+            ptx::mbar_init(empty + 8 * s, 1);       // the pair's commit
+            ptx::mbar_init(sfbar + 8 * s, 2);       // one arrival per CTA's scale warp
+        }
+        ptx::mbar_init(tfull, 1);
+        ptx::mbar_init(tempty, 8);                  // one arrival per epilogue warp of both CTAs
+        ptx::mbar_init(drain, 1);
+        *abort_flag = 0u;
+        ptx::fence_mbar_init();
+        ptx::prefetch_tmap(&tmap_a);
+        ptx::prefetch_tmap(&tmap_b);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), TMEM_COLS);
+        ptx::tmem_relinquish_pair();
+    }
+    ptx::tc_fence_before();
+    ptx::cluster_sync();   // both CTAs' barriers and tensor memory exist
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = pair; tile < p.num_tiles && ok; tile += npairs) {
+            int mb, nb;
+            tile_coords(tile, p.num_mb, p.num_nb, mb, nb);
+            for (int kb = 0; kb < p.nk; ++kb) {
+                const uint32_t s = it % PR_STAGES, ph = (it / PR_STAGES) & 1u;
+                ok = wait_phase_pair(empty + 8 * s, ph ^ 1u, limit, abort_flag, p.err, WHO_PRODUCER);
+                ok = __all_sync(0xFFFFFFFFu, ok);
+                if (!ok) break;
+                if (lane == 0) {
+                    if (leader)
+                        ptx::mbar_arrive_expect_tx(sBAR + 8 * s, 2 * (PR_A_TILE + PR_B_TILE));
+                    ptx::tma_load_2d_pair(sA + s * PR_A_TILE, &tmap_a, full_l + 8 * s, kb * BK,
+                                          mb * PR_BM + static_cast<int>(rank) * 128);
+                    ptx::tma_load_2d_pair(sB + s * PR_B_TILE, &tmap_b, full_l + 8 * s, kb * BK,
+                                          nb * PR_BN + static_cast<int>(rank) * 128);
+                }
+                __syncwarp();
+                ++it;
+            }
+        }
+        // the even CTA waits until the last loads of both CTAs have landed; the
+        // cluster barrier below keeps the odd CTA resident until then
+        if (leader) {
+            const uint32_t nd = it < static_cast<uint32_t>(PR_STAGES) ? it : static_cast<uint32_t>(PR_STAGES);
+            for (uint32_t i = it - nd; i < it; ++i)
+                wait_phase_pair(sBAR + 8 * (i % PR_STAGES), (i / PR_STAGES) & 1u, drain_limit,
+                                abort_flag, p.err, WHO_PRODUCER, false);
+        }
+        // A CTA that stopped early cannot tell which of its last copies the
+        // even CTA's barriers have counted; it gives them the drain bound to
+        // land (copies take microseconds) before the pair may leave.
+        if (!ok || *abort_flag) {
+            const uint64_t t0 = ptx::globaltimer();
+            while (ptx::globaltimer() - t0 < drain_limit) {
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------- MMA issuer (even CTA)
+        if (leader) {
+            uint32_t it = 0, tcount = 0;
+            bool ok = true;
+            for (int tile = pair; tile < p.num_tiles && ok; tile += npairs) {
+                ok = wait_phase_pair(tempty, (tcount & 1u) ^ 1u, limit, abort_flag, p.err, WHO_MMA);
+                ok = __all_sync(0xFFFFFFFFu, ok);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                for (int kb = 0; kb < p.nk; ++kb) {
+                    const uint32_t s = it % PR_STAGES, ph = (it / PR_STAGES) & 1u;
+                    ok = wait_phase_pair(sBAR + 8 * s, ph, limit, abort_flag, p.err, WHO_MMA) &&
+                         wait_phase_pair(sfbar + 8 * s, ph, limit, abort_flag, p.err, WHO_MMA);
+                    ok = __all_sync(0xFFFFFFFFu, ok);
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t tsfa = tmem + PR_SFA_COL + 4 * s;
+                        const uint32_t tsfb = tmem + PR_SFB_COL + 8 * s;
+                        ptx::tc_cp_32x128b_warpx4_pair(tsfa, desc_sf(sSFA + s * PR_SFA_TILE));
+                        ptx::tc_cp_32x128b_warpx4_pair(tsfb, desc_sf(sSFB + s * PR_SFB_TILE));
+                        ptx::tc_cp_32x128b_warpx4_pair(tsfb + 4, desc_sf(sSFB + s * PR_SFB_TILE + 512));
+                        const uint64_t ad = desc_sw128(sA + s * PR_A_TILE);
+                        const uint64_t bd = desc_sw128(sB + s * PR_B_TILE);
+#pragma unroll
+                        for (int j = 0; j < BK / 32; ++j) {
+                            const uint32_t idesc = p.idesc | (sf_id(p.gran_a, kb, j) << 29) |
+                                                   (sf_id(p.gran_b, kb, j) << 4);
+                            ptx::tc_mma_mxf8_pair(tmem + ACC_COL, ad + 2 * j, bd + 2 * j, idesc, tsfa,
+                                                  tsfb, (kb | j) != 0 ? 1u : 0u);
+                        }
+                        ptx::tc_commit_pair(empty + 8 * s, 0x3);   // frees the stage in both CTAs
+                    }
+                    __syncwarp();
+                    ++it;
+                }
+                if (!ok) break;
+                if (lane == 0) ptx::tc_commit_pair(tfull, 0x3);
+                __syncwarp();
+                ++tcount;
+            }
+            if (lane == 0) ptx::tc_commit_pair(drain, 0x1);
+            __syncwarp();
+            wait_phase_pair(drain, 0u, drain_limit, abort_flag, p.err, WHO_MMA, false);
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------ scale loader
+        // this CTA's 128 A rows and all 256 B rows of the pair tile
+        uint32_t it = 0;
+        bool ok = true;
+        const int ngrp = (p.nk + G - 1) / G;
+        int tile = pair, grp = 0;
+        ScaleGroup cur, nxt;
+        KParams q = p;    // A rows offset to this CTA's half of the pair tile
+        auto load = [&](ScaleGroup &g, int t, int gr) {
+            int mb, nb;
+            tile_coords(t, p.num_mb, p.num_nb, mb, nb);
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const int64_t m = static_cast<int64_t>(mb) * PR_BM + rank * 128 + 32 * a + lane;
+                load_row_scales<G>(q.sa, q.ld_sa, q.gran_a, m, gr, q.nk, true, g.a[a]);
+            }
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                const int64_t n = static_cast<int64_t>(nb) * PR_BN + 32 * h + lane;
+                load_row_scales<G>(q.sb, q.ld_sb, q.gran_b, n, gr, q.nk, n < q.N, g.b[h]);
+            }
+        };
+        if (tile < p.num_tiles) load(cur, tile, 0);
+        while (tile < p.num_tiles && ok) {
+            int ntile = tile, ngrp_next = grp + 1;
+            if (ngrp_next == ngrp) {
+                ntile += npairs;
+                ngrp_next = 0;
+            }
+            if (ntile < p.num_tiles) load(nxt, ntile, ngrp_next);
+#pragma unroll
+            for (int t = 0; t < G; ++t) {
+                if (G * grp + t >= p.nk || !ok) break;
+                constexpr int kWordStep = G / 4;
+                const int wi = t / kWordStep;
+                const uint32_t s = it % PR_STAGES, ph = (it / PR_STAGES) & 1u;
+                ok = wait_phase_pair(empty + 8 * s, ph ^ 1u, limit, abort_flag, p.err, WHO_SCALES);
+                ok = __all_sync(0xFFFFFFFFu, ok);
+                if (!ok) break;
+                const uint32_t dA = sSFA + s * PR_SFA_TILE + lane * 16;
+                const uint32_t dB = sSFB + s * PR_SFB_TILE + lane * 16;
+                st_shared_v4(dA, cur.a[0][wi], cur.a[1][wi], cur.a[2][wi], cur.a[3][wi]);
+                st_shared_v4(dB, cur.b[0][wi], cur.b[1][wi], cur.b[2][wi], cur.b[3][wi]);
+                st_shared_v4(dB + 512, cur.b[4][wi], cur.b[5][wi], cur.b[6][wi], cur.b[7][wi]);
+                // every lane's words visible to the tensor core's copy, then
+                // one cluster-scope arrival for the warp
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && !(p.inject == 1 && it == 0 && leader))
+                    ptx::mbar_arrive_cluster(sf_l + 8 * s);
+                ++it;
+            }
+            cur = nxt;
+            tile = ntile;
+            grp = ngrp_next;
+        }
+    } else if (warp >= 4) {
+        // --------------------------------------------------------- epilogue
+        const int qw = warp & 3;
+        uint8_t *stage = gbase + PR_OFF_EPI + qw * EPI_WARP_BYTES;
+        uint32_t tcount = 0;
+        for (int tile = pair; tile < p.num_tiles; tile += npairs) {
+            int mb, nb;
+            tile_coords(tile, p.num_mb, p.num_nb, mb, nb);
+            bool ok = wait_phase_pair(tfull, tcount & 1u, limit, abort_flag, p.err, WHO_EPILOGUE);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const int64_t row0 = static_cast<int64_t>(mb) * PR_BM + rank * 128 + qw * 32;
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(qw * 32) << 16) + ACC_COL;
+            if (!p.out_fp32 && !p.accumulate) {
+                uint32_t packed[PR_BN / 2];
+#pragma unroll
+                for (int chunk = 0; chunk < PR_BN / 32; chunk += 2) {
+                    uint32_t r[32], r2[32];
+                    ptx::tmem_ld_32x32b_x32(taddr + chunk * 32, r);
+                    ptx::tmem_ld_32x32b_x32(taddr + chunk * 32 + 32, r2);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        packed[chunk * 16 + e] =
+                            ptx::cvt_bf16x2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+                        packed[chunk * 16 + 16 + e] =
+                            ptx::cvt_bf16x2(__uint_as_float(r2[2 * e]), __uint_as_float(r2[2 * e + 1]));
+                    }
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive_cluster(tempty_l);
+#pragma unroll
+                for (int pc = 0; pc < PR_BN / 64; ++pc) {
+                    const int64_t n0 = static_cast<int64_t>(nb) * PR_BN + pc * 64;
+                    if (n0 >= p.N) continue;
+                    uint4 v[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        v[c] = make_uint4(packed[pc * 32 + 4 * c], packed[pc * 32 + 4 * c + 1],
+                                          packed[pc * 32 + 4 * c + 2], packed[pc * 32 + 4 * c + 3]);
+                    store_piece(stage, v, lane,
+                                reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.c) + row0 * p.ldc + n0),
+                                p.ldc * 2);
+                }
+                ++tcount;
+                continue;
+            }
+            // FP32 out, or accumulation into C: 64 columns at a time
+#pragma unroll 1
+            for (int pc = 0; pc < PR_BN / 64; ++pc) {
+                uint32_t r0[32], r1[32];
+                ptx::tmem_ld_32x32b_x32(taddr + pc * 64, r0);
+                ptx::tmem_ld_32x32b_x32(taddr + pc * 64 + 32, r1);
+                ptx::tmem_wait_ld();
+                if (pc == PR_BN / 64 - 1) {
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive_cluster(tempty_l);
+                }
+                const int64_t n0 = static_cast<int64_t>(nb) * PR_BN + pc * 64;
+                if (n0 >= p.N) continue;
+                if (p.out_fp32) {
+                    auto piece = [&](const uint32_t(&rr)[32], int64_t col) {
+                        uint8_t *g = reinterpret_cast<uint8_t *>(static_cast<float *>(p.c) + row0 * p.ldc + col);
+                        uint4 v[8];
+                        if (p.accumulate) {
+                            load_piece(stage, v, lane, g, p.ldc * 4);
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                v[c] = make_uint4(__float_as_uint(__uint_as_float(rr[4 * c]) + __uint_as_float(v[c].x)),
+                                                  __float_as_uint(__uint_as_float(rr[4 * c + 1]) + __uint_as_float(v[c].y)),
+                                                  __float_as_uint(__uint_as_float(rr[4 * c + 2]) + __uint_as_float(v[c].z)),
+                                                  __float_as_uint(__uint_as_float(rr[4 * c + 3]) + __uint_as_float(v[c].w)));
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                v[c] = make_uint4(rr[4 * c], rr[4 * c + 1], rr[4 * c + 2], rr[4 * c + 3]);
+                        }
+                        store_piece(stage, v, lane, g, p.ldc * 4);
+                    };
+                    piece(r0, n0);
+                    piece(r1, n0 + 32);
+                } else {
+                    uint8_t *g = reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.c) + row0 * p.ldc + n0);
+                    uint4 v[8];
+                    load_piece(stage, v, lane, g, p.ldc * 2);
+                    auto add8 = [](const uint32_t *f32, const uint4 &old) {
+                        return make_uint4(
+                            ptx::cvt_bf16x2(__uint_as_float(f32[0]) + bf16_lo(old.x), __uint_as_float(f32[1]) + bf16_hi(old.x)),
+                            ptx::cvt_bf16x2(__uint_as_float(f32[2]) + bf16_lo(old.y), __uint_as_float(f32[3]) + bf16_hi(old.y)),
+                            ptx::cvt_bf16x2(__uint_as_float(f32[4]) + bf16_lo(old.z), __uint_as_float(f32[5]) + bf16_hi(old.z)),
+                            ptx::cvt_bf16x2(__uint_as_float(f32[6]) + bf16_lo(old.w), __uint_as_float(f32[7]) + bf16_hi(old.w)));
+                    };
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        v[c] = add8(r0 + 8 * c, v[c]);
+                        v[c + 4] = add8(r1 + 8 * c, v[c + 4]);
+                    }
+                    store_piece(stage, v, lane, g, p.ldc * 2);
+                }
+            }
+            ++tcount;
+        }
+    }
+
+    // neither CTA leaves (or frees its tensor memory) while the other may still
+    // read its shared memory, signal its barriers or write its tensor memory
+    ptx::tc_fence_before();
+    ptx::cluster_sync();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc_pair(tmem, TMEM_COLS);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -1018,6 +1395,11 @@ int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
                     kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(W_SMEM_BYTES));
                 if (e != cudaSuccess) return 2 + static_cast<int>(e);
             }
+            for (auto kern : {k_gemm_pair<16>, k_gemm_pair<4>}) {
+                const cudaError_t e = cudaFuncSetAttribute(
+                    kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(PR_SMEM_BYTES));
+                if (e != cudaSuccess) return 2 + static_cast<int>(e);
+            }
             int n = 0;
             cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
             g_sms[dev] = n > 0 ? n : 1;
@@ -1030,7 +1412,8 @@ int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
     // quantized epilogue, whose 1x128 groups must not straddle tiles), unless
     // its coarser tiles fill the last wave of SMs so much worse that its
     // ~8 % faster tiles do not make up for it.
-    bool wide = !g.out_q && g.M % WBM == 0 && g.tile != 1;
+    const bool paired = g.tile == 3 && !g.out_q && g.M % PR_BM == 0 && sms >= 2;
+    bool wide = !paired && !g.out_q && g.M % WBM == 0 && g.tile != 1;
     if (wide && g.tile != 2) {
         auto wave_eff = [&](int64_t tiles) {
             const int64_t waves = (tiles + sms - 1) / sms;
@@ -1043,14 +1426,14 @@ int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
     CUtensorMap ta, tb;
     std::memset(&ta, 0, sizeof(ta));
     std::memset(&tb, 0, sizeof(tb));
-    if (!make_tmap(&ta, g.a_codes, g.M, g.K, g.lda, wide ? WBM : BM)) return 1;
-    if (!make_tmap(&tb, g.b_codes, g.N, g.K, g.ldb, wide ? WBN : BN)) return 1;
+    if (!make_tmap(&ta, g.a_codes, g.M, g.K, g.lda, paired ? 128 : (wide ? WBM : BM))) return 1;
+    if (!make_tmap(&tb, g.b_codes, g.N, g.K, g.ldb, paired ? 128 : (wide ? WBN : BN))) return 1;
 
     KParams p;
     p.M = static_cast<int>(g.M);
     p.N = static_cast<int>(g.N);
     p.nk = static_cast<int>(g.K / BK);
-    const int tbn = wide ? WBN : BN, tbm = wide ? WBM : BM;
+    const int tbn = paired ? PR_BN : (wide ? WBN : BN), tbm = paired ? PR_BM : (wide ? WBM : BM);
     p.num_nb = static_cast<int>((g.N + tbn - 1) / tbn);
     p.num_mb = static_cast<int>(g.M / tbm);
     p.num_tiles = p.num_mb * p.num_nb;
@@ -1073,15 +1456,36 @@ int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
     // (E4M3 = 0, E5M2 = 1) in bits 7-9 / 10-12, K-major A and B, N >> 3 in
     // bits 17-22, UE8M0 scale type in bit 23, M >> 4 in bits 24-28; the
     // scale-factor byte ids (bits 4-5 for B, 29-30 for A) are set per MMA.
+    // (the pair kernel's MMA spans M = 256 rows of both CTAs)
     p.idesc = (1u << 23) | (static_cast<uint32_t>(tbn >> 3) << 17) |
-              (static_cast<uint32_t>(BM >> 4) << 24) | (static_cast<uint32_t>(g.fmt_a) << 7) |
-              (static_cast<uint32_t>(g.fmt_b) << 10);
+              (static_cast<uint32_t>((paired ? PR_BM : BM) >> 4) << 24) |
+              (static_cast<uint32_t>(g.fmt_a) << 7) | (static_cast<uint32_t>(g.fmt_b) << 10);
     p.wait_limit_ns = g.wait_limit_ns;
     p.err = g.err;
 
+    const bool mx = g.gran_a == GRAN_MX32;
+    if (paired) {
+        // one pair of CTAs (a cluster of two) per two SMs
+        int pairs = sms / 2;
+        if (pairs > p.num_tiles) pairs = p.num_tiles;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+        cfg.blockDim = dim3(NUM_THREADS);
+        cfg.dynamicSmemBytes = PR_SMEM_BYTES;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = mx ? cudaLaunchKernelEx(&cfg, k_gemm_pair<4>, ta, tb, p)
+                                 : cudaLaunchKernelEx(&cfg, k_gemm_pair<16>, ta, tb, p);
+        return e == cudaSuccess ? 0 : 2 + static_cast<int>(e);
+    }
     int grid = sms;
     if (grid > p.num_tiles) grid = p.num_tiles;
-    const bool mx = g.gran_a == GRAN_MX32;
     if (wide) {
         if (mx) k_gemm_wide<4><<<grid, W_THREADS, W_SMEM_BYTES, stream>>>(ta, tb, p);
         else k_gemm_wide<16><<<grid, W_THREADS, W_SMEM_BYTES, stream>>>(ta, tb, p);

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <cstdint>
 
 namespace fp8hg {
@@ -32,6 +33,15 @@ bool quant_token_waits(int64_t cols, int group, int transpose);
 cudaError_t launch_quant_token(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
                                int group, int transpose, int fmt, uint8_t *q, int64_t ld_q,
                                uint8_t *s, int64_t ld_s, const WaitOpts &w, cudaStream_t stream);
+
+// Both layouts of an activation from one read (per token, and 1x128 along
+// the tokens transposed); ws: dual_workspace_bytes(rows, cols) of device
+// memory (per-token maxima and per-stripe counters; zeroed by the launch).
+size_t dual_workspace_bytes(int64_t rows, int64_t cols);
+cudaError_t launch_quant_dual(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
+                              uint8_t *q, int64_t ld_q, uint8_t *s, int64_t ld_s, int fmt_t,
+                              uint8_t *qt, int64_t ld_qt, uint8_t *st, int64_t ld_st,
+                              unsigned int *ws, const WaitOpts &w, cudaStream_t stream);
 
 cudaError_t launch_quant_mx32(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
                               uint8_t *q, int64_t ld_q, uint8_t *s, int64_t ld_s,

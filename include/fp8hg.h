@@ -47,6 +47,7 @@
 #ifndef FP8HG_H
 #define FP8HG_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -75,6 +76,28 @@ typedef enum {
 typedef enum { FP8HG_FPROP = 0, FP8HG_DGRAD = 1, FP8HG_WGRAD = 2 } fp8hg_op;
 
 typedef enum { FP8HG_OUT_BF16 = 0, FP8HG_OUT_FP32 = 1 } fp8hg_out;
+
+/*
+ * Options of the quantizer and GEMM entry points whose kernels wait on
+ * copies or on each other (the per-token quantizer's row staging, the
+ * re-quantizer's tile ring, the FP32-scale GEMM's operand pipeline, the
+ * single-read quantizer's second pass).  No passage: these exist to
+ * bound and test the library's own waits.
+ *   wait_limit_ns  upper bound on any single wait for a copy (0 = the
+ *                  default, 2 s).  When it runs out the kernel records
+ *                  FP8HG_ERR_TIMEOUT in the device error word, waits (bounded)
+ *                  for the copies it still has in flight and returns; the
+ *                  outputs are then unspecified.
+ *   inject_fault   0 = none.  1 = the first CTA never issues its first copy,
+ *                  so the wait for it can only run out: a host-chosen,
+ *                  GPU-safe way to exercise the timeout path in tests.
+ *   reserved       must be 0.
+ */
+typedef struct {
+    uint64_t wait_limit_ns;
+    int32_t inject_fault;
+    int32_t reserved;
+} fp8hg_wait_opts;
 
 /*
  * fp8_quant_token — per-token (group = 0) or per-1x128-group (group = 128)
@@ -108,6 +131,45 @@ typedef enum { FP8HG_OUT_BF16 = 0, FP8HG_OUT_FP32 = 1 } fp8hg_out;
 int fp8_quant_token(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int group,
                     int transpose, int fmt, uint8_t *q, int64_t ld_q, uint8_t *scale,
                     int64_t ld_s, void *stream);
+
+/*
+ * fp8_quant_token_dual — both quantizations an activation needs, from one read
+ * of it: the per-token codes of fp8_quant_token(group = 0) and the transposed
+ * 1x128-along-tokens codes of fp8_quant_token(group = 128, transpose = 1),
+ * identical to what those two calls write.
+ *
+ * Passage: "A Comprehensive FP8 Training Recipe ...", "What carries the
+ * argument" (token-wise activation scales, E8M0 exponent-only scales rounded
+ * up); the forward and data-gradient GEMMs take the per-token operand, the
+ * weight-gradient GEMM (contraction over tokens) the transposed one.
+ *
+ *   x         [rows = tokens, cols] BF16 (ld_x elements)
+ *   fmt, q, scale      per-token codes [rows, cols] (ld_q bytes) in fmt,
+ *                      scale [rows] at scale[r * ld_s]
+ *   fmt_t, q_t, scale_t  transposed codes [cols, rows] (ld_qt bytes) in fmt_t,
+ *                      scale_t [cols, rows/128] (ld_st bytes)
+ *   workspace  device scratch of at least
+ *              fp8_quant_token_dual_workspace(rows, cols) bytes, 16-byte
+ *              aligned, owned by the caller; the call clears and uses it
+ *              (per-token maxima and per-128-token counters), so calls that
+ *              may overlap on the GPU need separate workspaces.
+ *   opts       NULL or wait options (fp8hg_wait_opts; inject_fault = 1
+ *              withholds one tile's completion so that the waits for it run
+ *              out, for tests of the timeout path)
+ * The kernel is a cooperative launch (every CTA resident at once).  Its
+ * second pass over a 128-token stripe waits (bounded) for the first pass of
+ * every tile of that stripe; an expired wait is FP8HG_ERR_TIMEOUT from
+ * fp8hg_get_device_error.
+ * Requirements: rows % 128 == 0, cols % 128 == 0; x, q, q_t 16-byte aligned;
+ * ld_x % 8 == 0, ld_q % 16 == 0, ld_qt % 16 == 0; ld_s >= 1,
+ * ld_st >= rows/128.
+ */
+size_t fp8_quant_token_dual_workspace(int64_t rows, int64_t cols);
+int fp8_quant_token_dual(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
+                         uint8_t *q, int64_t ld_q, uint8_t *scale, int64_t ld_s, int fmt_t,
+                         uint8_t *q_t, int64_t ld_qt, uint8_t *scale_t, int64_t ld_st,
+                         void *workspace, size_t workspace_bytes,
+                         const fp8hg_wait_opts *opts, void *stream);
 
 /*
  * fp8_quant_block128 — weight quantizer, one UE8M0 round-up scale per
@@ -364,9 +426,11 @@ int fp8_gemm_scaled_q(int op, const fp8hg_operand *a, const fp8hg_operand *b, ui
  *                  complete: a host-chosen, GPU-safe way to exercise the
  *                  timeout path in tests.
  *   tile           0 = the library's choice.  1 = 128 x 256 tiles.  2 = 256 x 224
- *                  tiles (two accumulators per B stage); honoured when M is a
- *                  multiple of 256, else FP8HG_ERR_UNSUPPORTED.  The result
- *                  does not depend on the tile beyond FP32 accumulation order.
+ *                  tiles (two accumulators per B stage).  3 = 256 x 256 tiles
+ *                  computed by a pair of CTAs (a two-CTA cluster sharing the
+ *                  MMA).  2 and 3 are honoured when M is a multiple of 256,
+ *                  else FP8HG_ERR_UNSUPPORTED.  The result does not depend on
+ *                  the tile beyond FP32 accumulation order.
  */
 typedef struct {
     uint64_t wait_limit_ns;
@@ -379,26 +443,6 @@ int fp8_gemm_scaled_ex(int op, const fp8hg_operand *a, const fp8hg_operand *b, v
                        int64_t ldc, int out, int accumulate, const fp8hg_gemm_opts *opts,
                        void *stream);
 
-/*
- * Options of the quantizer and GEMM entry points whose kernels wait on
- * copies (the per-token quantizer's row staging, the re-quantizer's tile
- * ring, the FP32-scale GEMM's operand pipeline).  No passage: these exist to
- * bound and test the library's own waits.
- *   wait_limit_ns  upper bound on any single wait for a copy (0 = the
- *                  default, 2 s).  When it runs out the kernel records
- *                  FP8HG_ERR_TIMEOUT in the device error word, waits (bounded)
- *                  for the copies it still has in flight and returns; the
- *                  outputs are then unspecified.
- *   inject_fault   0 = none.  1 = the first CTA never issues its first copy,
- *                  so the wait for it can only run out: a host-chosen,
- *                  GPU-safe way to exercise the timeout path in tests.
- *   reserved       must be 0.
- */
-typedef struct {
-    uint64_t wait_limit_ns;
-    int32_t inject_fault;
-    int32_t reserved;
-} fp8hg_wait_opts;
 
 /*
  * fp8_quant_token, fp8_requant_t and fp8_gemm_scaled_f32s with wait options
@@ -421,8 +465,8 @@ int fp8_gemm_scaled_f32s_ex(int op, const fp8hg_operand_f32s *a, const fp8hg_ope
 /*
  * fp8hg_get_device_error — synchronizes `stream`, then reads and clears the
  * device error word of the current device.  Returns FP8HG_OK,
- * FP8HG_ERR_TIMEOUT (a bounded wait in a GEMM, the per-token quantizer or
- * the re-quantizer expired since the last call) or FP8HG_ERR_CUDA (the
+ * FP8HG_ERR_TIMEOUT (a bounded wait in a GEMM, the per-token quantizer, the
+ * re-quantizer or the single-read quantizer expired since the last call) or FP8HG_ERR_CUDA (the
  * synchronization itself failed).
  */
 int fp8hg_get_device_error(void *stream);

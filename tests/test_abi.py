@@ -13,7 +13,8 @@ EXPECTED = {"fp8_quant_token", "fp8_quant_block128", "fp8_quant_mx32", "fp8_quan
             "fp8_quant_block128_f32s", "fp8_gemm_scaled_f32s",
             "fp8_gemm_scaled",
             "fp8_gemm_scaled_ex", "fp8hg_get_device_error", "fp8hg_status_str", "fp8hg_version",
-            "fp8_quant_token_ex", "fp8_requant_t_ex", "fp8_gemm_scaled_f32s_ex"}
+            "fp8_quant_token_ex", "fp8_requant_t_ex", "fp8_gemm_scaled_f32s_ex",
+            "fp8_quant_token_dual", "fp8_quant_token_dual_workspace"}
 
 OK, INVALID, ALIGN, SHAPE, UNSUP = 0, 1, 2, 3, 4
 FAKE = 0x10000  # never dereferenced: every call below fails validation first
@@ -151,9 +152,11 @@ def test_gemm_options_validation(lib):
         return g(0, ctypes.byref(a), ctypes.byref(_op(**blk)), FAKE, 256, 0, 0,
                  ctypes.byref(opts), None)
 
-    assert call(_op(), fp8hg.GemmOpts(0, 0, 3)) == INVALID        # tile selector
+    assert call(_op(), fp8hg.GemmOpts(0, 0, 4)) == INVALID        # tile selector
+    assert call(_op(), fp8hg.GemmOpts(0, 0, -1)) == INVALID
     assert call(_op(), fp8hg.GemmOpts(0, 2, 0)) == INVALID        # inject_fault
     assert call(_op(rows=128), fp8hg.GemmOpts(0, 0, 2)) == UNSUP  # 256-row tiles, M = 128
+    assert call(_op(rows=384), fp8hg.GemmOpts(0, 0, 3)) == UNSUP  # CTA pairs, M % 256 != 0
 
 
 def test_gemm_validation(lib):
@@ -209,3 +212,28 @@ def test_wait_options_validation(lib):
     blk = dict(gran=GRAN_128x128, lds=2)
     assert g(0, ctypes.byref(_op()), ctypes.byref(_op(**blk)), FAKE, 256, 0,
              ctypes.byref(W(0, -1, 0)), None) == INVALID
+
+
+def test_dual_quant_validation(lib):
+    d = lib.fp8_quant_token_dual
+    ws_need = lib.fp8_quant_token_dual_workspace(256, 256)
+    assert ws_need >= 4 * (256 + 2) and ws_need % 256 == 0
+    assert lib.fp8_quant_token_dual_workspace(0, 256) == 0
+
+    def call(rows=256, cols=256, fmt=E4M3, fmt_t=E4M3, ws=FAKE, wsb=None, qt=FAKE, ld_qt=256,
+             ld_st=2, st=FAKE, x=FAKE, opts=None):
+        wsb = ws_need if wsb is None else wsb
+        return d(x, rows, cols, cols, fmt, FAKE, cols, FAKE, 1, fmt_t, qt, ld_qt, st, ld_st, ws,
+                 wsb, opts, None)
+
+    assert call(fmt_t=4) == INVALID
+    assert call(ws=None) == INVALID
+    assert call(wsb=ws_need - 1) == INVALID
+    assert call(ws=FAKE + 4) == ALIGN
+    assert call(qt=FAKE + 8) == ALIGN
+    assert call(rows=200, ld_qt=208) == SHAPE
+    assert call(cols=192) == SHAPE
+    assert call(ld_st=1) == INVALID
+    assert call(st=None) == INVALID
+    assert call(rows=0) == OK
+    assert call(opts=ctypes.byref(fp8hg.WaitOpts(0, 7, 0))) == INVALID

@@ -162,11 +162,11 @@ def _gemm_operands(M, N, K):
     return to_qtensor(qa, sa, E4M3, GRAN_ROW), to_qtensor(qb, sb, E4M3, GRAN_128x128), ref
 
 
-@pytest.mark.parametrize("tile", [1, 2])
+@pytest.mark.parametrize("tile", [1, 2, 3])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("accumulate", [False, True])
 def test_gemm_output_canary(cuda_lib, tile, dtype, accumulate):
-    """N = 384 ends inside both tile shapes' last n-tile (256 + 128, 224 + 160)."""
+    """N = 384 ends inside every tile shape's last n-tile (256 + 128, 224 + 160)."""
     M, N, K = 256, 384, 256
     a, b, (c_ref, s_abs) = _gemm_operands(M, N, K)
     cbuf, c = canvas(M, N, N + 64, dtype=dtype)
