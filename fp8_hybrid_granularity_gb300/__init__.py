@@ -237,6 +237,28 @@ def fp8_quant_token_dual(x, fmt: int = E4M3, fmt_t: Optional[int] = None,
     return out, out_t
 
 
+def fp8_quant_token_dual_noalloc(x, fmt: int = E4M3, fmt_t: Optional[int] = None,
+                                 out: Optional[QTensor] = None, out_t: Optional[QTensor] = None,
+                                 stream=None):
+    """fp8_quant_token_dual for callers that cannot provide device scratch:
+    the library's fixed scratch is used instead (at most 65536 tokens; calls
+    that may overlap on the GPU must not use it concurrently)."""
+    _check_bf16(x)
+    rows, cols = x.shape
+    fmt_t = fmt if fmt_t is None else fmt_t
+    out = out if out is not None else alloc_token(rows, cols, 0, fmt, False, x.device)
+    out_t = out_t if out_t is not None else alloc_token(rows, cols, 128, fmt_t, True, x.device)
+    f = lib().fp8_quant_token_dual_noalloc
+    P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    f.argtypes = [P, I64, I64, I64, I, P, I64, P, I64, I, P, I64, P, I64, P, P]
+    f.restype = I
+    rc = f(_ptr(x), rows, cols, x.stride(0), fmt, _ptr(out.codes), out.codes.stride(0),
+           _ptr(out.scale), out.scale.stride(0), fmt_t, _ptr(out_t.codes), out_t.codes.stride(0),
+           _ptr(out_t.scale), out_t.scale.stride(0), None, _stream(stream))
+    _check(rc, "fp8_quant_token_dual_noalloc")
+    return out, out_t
+
+
 def fp8_quant_block128(x, fmt: int = E4M3, transposed_copy: bool = False, out=None,
                        out_t=None, stream=None):
     """Per-128x128-block UE8M0 quantization; with transposed_copy=True also

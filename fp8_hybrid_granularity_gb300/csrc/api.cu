@@ -193,6 +193,31 @@ int fp8_quant_token_dual(const uint16_t *x, int64_t rows, int64_t cols, int64_t 
         static_cast<unsigned int *>(workspace), w, static_cast<cudaStream_t>(stream)));
 }
 
+int fp8_quant_token_dual_noalloc(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
+                                 int fmt, uint8_t *q, int64_t ld_q, uint8_t *scale, int64_t ld_s,
+                                 int fmt_t, uint8_t *q_t, int64_t ld_qt, uint8_t *scale_t,
+                                 int64_t ld_st, const fp8hg_wait_opts *opts, void *stream) {
+    fp8hg::WaitOpts w;
+    int st = wait_opts(opts, w);
+    if (st != FP8HG_OK) return st;
+    st = check_quant_common(x, rows, cols, ld_x, fmt, q, ld_q, scale);
+    if (st != FP8HG_OK) return st;
+    if (!valid_fmt(fmt_t)) return FP8HG_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return FP8HG_OK;
+    if (!q_t || !scale_t) return FP8HG_ERR_INVALID_ARG;
+    if (!aligned(q_t, 16) || ld_qt % 16) return FP8HG_ERR_ALIGNMENT;
+    if (rows % 128 || cols % 128) return FP8HG_ERR_SHAPE;
+    if (rows > fp8hg::noalloc_dual_max_rows()) return FP8HG_ERR_SHAPE;   // beyond the fixed scratch
+    if (cols > (int64_t(1) << 31)) return FP8HG_ERR_SHAPE;
+    if (ld_x < cols || ld_q < cols || ld_s < 1 || ld_qt < rows || ld_st < rows / 128)
+        return FP8HG_ERR_INVALID_ARG;
+    unsigned int *ws = fp8hg::noalloc_dual_workspace();
+    if (!ws) return FP8HG_ERR_CUDA;
+    return status_from_cuda(fp8hg::launch_quant_dual(x, rows, cols, ld_x, fmt, q, ld_q, scale, ld_s,
+                                                     fmt_t, q_t, ld_qt, scale_t, ld_st, ws, w,
+                                                     static_cast<cudaStream_t>(stream)));
+}
+
 int fp8_quant_block128(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
                        uint8_t *q, int64_t ld_q, uint8_t *scale, int64_t ld_s, uint8_t *q_t,
                        int64_t ld_qt, uint8_t *scale_t, int64_t ld_st, void *stream) {

@@ -43,6 +43,12 @@ cudaError_t launch_quant_dual(const uint16_t *x, int64_t rows, int64_t cols, int
                               uint8_t *qt, int64_t ld_qt, uint8_t *st, int64_t ld_st,
                               unsigned int *ws, const WaitOpts &w, cudaStream_t stream);
 
+// The fixed scratch of the allocation-free dual quantizer: its device address
+// on the current device (looked up on the first call per device; null on
+// failure) and the largest row count it serves.
+unsigned int *noalloc_dual_workspace();
+int64_t noalloc_dual_max_rows();
+
 cudaError_t launch_quant_mx32(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt,
                               uint8_t *q, int64_t ld_q, uint8_t *s, int64_t ld_s,
                               unsigned long long *cnt, cudaStream_t stream);

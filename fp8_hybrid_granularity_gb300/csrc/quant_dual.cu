@@ -309,7 +309,34 @@ cudaError_t launch_dual_t(const uint16_t *x, int64_t rows, int64_t cols, int64_t
                                        smem, stream);
 }
 
+// Scratch of fp8_quant_token_dual_noalloc, for callers that cannot give the
+// library device memory: the per-token maxima (kParts partitions) and the
+// per-stripe counters for up to kNoallocMaxRows tokens, about 2 MB.  Every
+// device that loads the library holds it until the process exits; all calls
+// on a device share it.
+constexpr int64_t kNoallocMaxRows = 65536;
+__device__ __align__(256) unsigned int
+    g_dual_noalloc_ws[kParts * kNoallocMaxRows + kNoallocMaxRows / kDT];
+std::atomic<unsigned int *> g_dual_noalloc_ptr[64];
+
 }  // namespace
+
+int64_t noalloc_dual_max_rows() { return kNoallocMaxRows; }
+
+unsigned int *noalloc_dual_workspace() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    unsigned int *p = g_dual_noalloc_ptr[dev].load(std::memory_order_acquire);
+    if (p) return p;
+    // Set-up, once per device, with that device current.  In host code the
+    // array's name only stands in for it; its device address is asked for.
+    void *addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_dual_noalloc_ws) != cudaSuccess || addr == nullptr)
+        return nullptr;
+    p = static_cast<unsigned int *>(addr);
+    g_dual_noalloc_ptr[dev].store(p, std::memory_order_release);
+    return p;
+}
 
 size_t dual_workspace_bytes(int64_t rows, int64_t cols) {
     (void)cols;

@@ -172,6 +172,34 @@ int fp8_quant_token_dual(const uint16_t *x, int64_t rows, int64_t cols, int64_t 
                          const fp8hg_wait_opts *opts, void *stream);
 
 /*
+ * fp8_quant_token_dual_noalloc — fp8_quant_token_dual for callers that cannot
+ * hand the library any device memory of its own: code that runs inside a
+ * framework whose memory pool owns the device and gives extensions no way to
+ * call cudaMalloc, code that runs inside an allocator's own callbacks, or a
+ * hot path that must not take the device-wide synchronization cudaMalloc and
+ * cudaFree can cause.  It takes the same inputs and outputs, writes the same
+ * bytes, and allocates nothing: its scratch is a fixed array inside the
+ * library (about 2 MB, present on every device that loads the library until
+ * the process exits).
+ *
+ * No passage of the paper corresponds to this entry point; it exists only for
+ * the callers above.
+ *
+ *   arguments as fp8_quant_token_dual, without workspace / workspace_bytes
+ * Limit: rows <= 65536; more rows is FP8HG_ERR_SHAPE (the fixed scratch holds
+ * the per-token maxima of 65536 tokens).
+ * The first call on a device, with that device current, looks up the array's
+ * device address once; make that first call before any stream capture.
+ * Every call on a device uses the same array: each call clears it before it
+ * starts, and calls that can overlap on the GPU (different streams with no
+ * ordering between them) race on it and give wrong results.
+ */
+int fp8_quant_token_dual_noalloc(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
+                                 int fmt, uint8_t *q, int64_t ld_q, uint8_t *scale, int64_t ld_s,
+                                 int fmt_t, uint8_t *q_t, int64_t ld_qt, uint8_t *scale_t,
+                                 int64_t ld_st, const fp8hg_wait_opts *opts, void *stream);
+
+/*
  * fp8_quant_block128 — weight quantizer, one UE8M0 round-up scale per
  * 128x128 block (the whole block's amax is taken before any element is cast).
  *

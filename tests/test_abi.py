@@ -14,7 +14,8 @@ EXPECTED = {"fp8_quant_token", "fp8_quant_block128", "fp8_quant_mx32", "fp8_quan
             "fp8_gemm_scaled",
             "fp8_gemm_scaled_ex", "fp8hg_get_device_error", "fp8hg_status_str", "fp8hg_version",
             "fp8_quant_token_ex", "fp8_requant_t_ex", "fp8_gemm_scaled_f32s_ex",
-            "fp8_quant_token_dual", "fp8_quant_token_dual_workspace"}
+            "fp8_quant_token_dual", "fp8_quant_token_dual_workspace",
+            "fp8_quant_token_dual_noalloc"}
 
 OK, INVALID, ALIGN, SHAPE, UNSUP = 0, 1, 2, 3, 4
 FAKE = 0x10000  # never dereferenced: every call below fails validation first
