@@ -67,7 +67,8 @@ TENSOR_FLOP_PER_CYCLE_SM = 16384      # dense FP8 MMA rate of one SM (128x256x32
 # DRAM bytes per GEMM launch of the 7B step from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the gemm.cu
 # it was taken on; any other source gives traffic null.
-GEMM_TRAFFIC = {"gemm_sha256": None, "bytes_per_launch": None}
+GEMM_TRAFFIC = {"gemm_sha256": "5d032afd2ca85a696748a4e9f6591ca2f6dbc11d3d8ec0be52efbdb10a9a70c9",
+                "bytes_per_launch": 1.0969e9}
 
 
 def _parse(argv=None):

@@ -5,26 +5,29 @@
 // Models", "What carries the argument": token-wise activation scales), and the
 // weight-gradient GEMM contracts over tokens, so the same tensor is also needed
 // in 1x128 groups along the tokens, transposed.  Quantizing it twice reads it
-// from HBM twice.  This kernel reads it once from HBM:
+// from HBM twice.  This kernel reads it once.
 //
-//   first pass, per 128-token x 128-column tile: each column's amax over the
-//     tile's 128 tokens -> the transposed codes and their scale (the 1x128
-//     group is wholly inside the tile); each row's amax over the tile's
-//     columns is folded into a per-token maximum in a workspace (integer
-//     atomic max on BF16 magnitude patterns, spread over 8 partitions by tile
-//     column so that the ~150 tiles of a stripe do not all update the same
-//     128 words), and the stripe's counter is bumped once the tile's maxima
-//     are published;
-//   second pass, per tile, once every tile of its 128-token stripe has passed
-//     the first pass: the per-token scales from the workspace, and the tile
-//     read again (from L2: the stripe was read moments before) and cast.
-//
-// Persistent cooperative grid (every CTA resident), work taken in rounds of
-// one tile per CTA, first-pass and second-pass rounds alternating, the second
-// passes a few rounds behind the first (see dual_round): a second pass only
-// waits for first passes earlier in that order, so the waits cannot form a
-// cycle, and the data it re-reads is a few rounds old (~60-80 MB), inside L2.  Every wait is bounded; on expiry the kernel
-// records bit 8 in the device error word and its CTAs return.
+// Work unit: one 128-token x 128-column tile; a 128-token stripe is tiles
+// wide.  Each thread holds an 8-token x 8-column block of its tile in
+// registers for the whole unit:
+//   1. the token maxima over the tile's columns are folded into a workspace
+//      (integer atomic max on BF16 magnitude patterns, spread over 8
+//      partitions by tile column), and the stripe's counter is bumped;
+//   2. each column's amax over the tile's 128 tokens gives the transposed
+//      codes and their scale (the 1x128 group lies inside the tile), written
+//      through shared memory as whole 128-byte rows;
+//   3. once every tile of the stripe has been counted, the token scales come
+//      from the workspace and the same registers are cast per token.
+// Persistent cooperative grid (every CTA resident); CTA b takes tiles b,
+// b + G, ... (G = grid), so the tiles of a stripe are taken by neighbouring
+// CTAs in the same round of the grid, or in two consecutive rounds.  Each
+// CTA prefetches its next tile into a private shared-memory region by
+// cp.async while it works on steps 2 and 3 of the current one.  A CTA waits in step 3 only
+// for first steps of the same round or of the next round's first CTAs, which
+// never wait themselves on a later round while the stripe is at most G tiles
+// wide (checked by the launcher), so the waits cannot form a cycle.  Every
+// wait is bounded; on expiry the kernel records bit 8 in the device error
+// word and its CTAs return.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -40,15 +43,18 @@ namespace {
 constexpr int kDT = 128;          // tokens per stripe = the 1x128 group along tokens
 constexpr int kDC = 128;          // columns per tile
 constexpr int kDThreads = 256;
-constexpr int kParts = 8;         // the per-token maxima are kept in 8 partitions (by tile column)
+constexpr int kParts = 8;         // partitions of the per-token maxima (by tile column)
 constexpr uint64_t kDualWaitNs = 2000000000ull;  // 2 s
 
 struct DualSmem {
-    uint16_t tile[kDT][kDC + 8];   // first pass: the tile (rows padded: conflict-free columns)
-    uint8_t codes[kDC][kDT + 16];  // first pass: transposed codes, one row per column
-    uint32_t red[2][kDC];          // column amax of each half of the tokens
-    float mul[kDT];                // second pass: per-token multipliers 2^-e
-    uint32_t nan_row[kDT];         // second pass: the token holds a NaN or an infinity
+    uint4 pre[8][kDThreads];        // next tile: vector k of thread t at pre[k][t] (cp.async;
+                                    // consecutive threads, consecutive 16-byte slots)
+    uint2 codes[kDC][kDT / 8];      // transposed codes: column c, 8-token groups XOR-swizzled
+    uint32_t cred[8][8][16];        // per-warp column maxima: [warp][j][v] for column 8 v + j
+    float cmul[kDC];                // column multipliers 2^-e
+    uint32_t cnan[kDC];
+    float rmul[kDT];                // token multipliers 2^-e
+    uint32_t rnan[kDT];
     int ok;
 };
 
@@ -74,38 +80,25 @@ __device__ bool wait_count(const unsigned int *counter, uint32_t target, uint64_
     if (ld_acquire(counter) >= target) return true;
     const uint64_t t0 = ptx::globaltimer();
     while (true) {
-        __nanosleep(128);
+        __nanosleep(64);
         if (ld_acquire(counter) >= target) return true;
         if (ptx::globaltimer() - t0 > limit) return false;
     }
 }
 
-// The work is cut into rounds of one item per CTA: first-pass rounds P1_j
-// (tiles j*G .. j*G + G - 1 of the first pass, G = the grid) and second-pass
-// rounds P2_j, in the order P1_0 .. P1_{lag-1}, then P2_m, P1_{m+lag} for
-// m = 0, 1, ..., then the remaining P2 rounds.  Every CTA thus alternates
-// between reading HBM (first pass) and L2 (second pass).  The second pass of
-// round m needs first-pass tiles up to (m+1) G + T - 1, which lie in rounds
-// P1_0 .. P1_{m+lag-1} when lag >= 1 + ceil(T / G): all of them come earlier
-// in the order, so the waits cannot form a cycle.
-__device__ __forceinline__ void dual_round(int r, int lag, int nrounds1, bool &first, int &block) {
-    const int pre = min(lag, nrounds1);
-    if (r < pre) {
-        first = true;
-        block = r;
-        return;
-    }
-    const int t = r - pre, pairs = max(nrounds1 - lag, 0);
-    if (t < 2 * pairs) {
-        first = (t & 1) != 0;
-        block = first ? t / 2 + lag : t / 2;
-        return;
-    }
-    first = false;
-    block = pairs + (t - 2 * pairs);
+// |x| pattern of BF16 element j (0..7) of a 16-byte vector
+__device__ __forceinline__ uint32_t abs_el(const uint4 &v, int j) {
+    const uint32_t w = j < 2 ? v.x : (j < 4 ? v.y : (j < 6 ? v.z : v.w));
+    return ((j & 1) ? (w >> 16) : w) & 0x7FFFu;
+}
+__device__ __forceinline__ float f32_el(const uint4 &v, int j) {
+    const uint32_t w = j < 2 ? v.x : (j < 4 ? v.y : (j < 6 ? v.z : v.w));
+    return __uint_as_float((j & 1) ? (w & 0xFFFF0000u) : (w << 16));
 }
 
-// F1: per-token codes; F2: transposed 1x128 codes.
+// F1: per-token codes; F2: transposed 1x128 codes.  Thread tid holds tokens
+// 8 g .. 8 g + 7 (g = tid / 16) and columns 8 v .. 8 v + 7 (v = tid % 16) of
+// the tile: vector k is token 8 g + k.
 template <int F1, int F2>
 __global__ void __launch_bounds__(kDThreads, 4)
     k_quant_dual(const uint16_t *__restrict__ x, int64_t ld_x, int stripes, int tiles,
@@ -115,154 +108,130 @@ __global__ void __launch_bounds__(kDThreads, 4)
                  uint64_t wait_ns, int inject, unsigned int *err) {
     extern __shared__ __align__(16) uint8_t dual_smem[];
     DualSmem &sm = *reinterpret_cast<DualSmem *>(dual_smem);
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = tid >> 4, v = tid & 15;
     const int64_t n1 = static_cast<int64_t>(stripes) * tiles;
     const int64_t rows = static_cast<int64_t>(stripes) * kDT;
-    const int64_t G = gridDim.x;
-    const int nrounds1 = static_cast<int>((n1 + G - 1) / G);
-    const int lag = 2 + static_cast<int>((tiles + G - 1) / G);
-    // inject = 1 (a test of the timeout path): CTA 0 never reports its first
-    // tile, so the second passes of that stripe can only run out of time.
+    // inject = 1 (a test of the timeout path): CTA 0 never counts its first
+    // tile, so the cast of that stripe can only run out of time.
     bool withhold = inject == 1 && blockIdx.x == 0;
-    // The first-pass tile is copied into sm.tile by cp.async as soon as the
-    // buffer is free (after the previous first pass), so that its HBM latency
-    // overlaps the second-pass item in between.  Thread tid copies vectors
-    // e = tid + 256k: token e / 16, columns 8 (e % 16) .. +7.
-    auto issue_tile = [&](int64_t tidx) {
-        const int64_t rr0 = (tidx / tiles) * kDT, cc0 = (tidx % tiles) * kDC;
+    auto issue = [&](int64_t t) {
+        const int64_t rr0 = (t / tiles) * kDT, cc0 = (t % tiles) * kDC;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int e = tid + kDThreads * k, r = e >> 4, cv = e & 15;
-            cp_async16(ptx::smem_u32(&sm.tile[r][cv * 8]), x + (rr0 + r) * ld_x + cc0 + cv * 8);
-        }
+        for (int k = 0; k < 8; ++k)
+            cp_async16(ptx::smem_u32(&sm.pre[k][tid]), x + (rr0 + 8 * g + k) * ld_x + cc0 + 8 * v);
         cp_async_commit();
     };
-    // this CTA's next first-pass tile after round r (-1 if none)
-    auto next_first = [&](int r) -> int64_t {
-        for (int r2 = r + 1; r2 < 2 * nrounds1; ++r2) {
-            bool f;
-            int b;
-            dual_round(r2, lag, nrounds1, f, b);
-            const int64_t t = static_cast<int64_t>(b) * G + blockIdx.x;
-            if (f && t < n1) return t;
-        }
-        return -1;
-    };
-    int64_t prefetched = -1;   // tile whose copy into sm.tile is in flight
-    for (int r = 0; r < 2 * nrounds1; ++r) {
-        bool first;
-        int block;
-        dual_round(r, lag, nrounds1, first, block);
-        const int64_t idx = static_cast<int64_t>(block) * G + blockIdx.x;
-        if (idx >= n1) continue;
-        const int stripe = static_cast<int>(idx / tiles), tcol = static_cast<int>(idx % tiles);
+    if (static_cast<int64_t>(blockIdx.x) < n1) issue(blockIdx.x);
+    for (int64_t t = blockIdx.x; t < n1; t += gridDim.x) {
+        const int stripe = static_cast<int>(t / tiles), tcol = static_cast<int>(t % tiles);
         const int64_t r0 = static_cast<int64_t>(stripe) * kDT, c0 = static_cast<int64_t>(tcol) * kDC;
-        if (first) {
-            // --------------------------------------------------- first pass
-            if (prefetched != idx) issue_tile(idx);
-            cp_async_wait_all();
-            __syncthreads();
-            // the 16 lanes of a token reduce its maximum over the tile
+        // this thread's block (its own copies), then the next tile's copies
+        cp_async_wait_all();
+        uint4 a[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int e = tid + kDThreads * k, r = e >> 4, cv = e & 15;
-                const uint4 v = *reinterpret_cast<const uint4 *>(&sm.tile[r][cv * 8]);
-                uint32_t m = bf16_abs_max8(v);
+        for (int k = 0; k < 8; ++k) a[k] = sm.pre[k][tid];
+
+        // 1. token maxima: the 16 threads of a token group reduce over 128 columns
 #pragma unroll
-                for (int o = 8; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-                if ((tid & 15) == 0) atomicMax(rowmax + (tcol % kParts) * rows + r0 + r, m);
-            }
-            // column c over tokens 64 h .. 64 h + 63
-            const int c = tid & (kDC - 1), h = tid >> 7;
-            uint32_t vals[32];
+        for (int k = 0; k < 8; ++k) {
+            uint32_t m = bf16_abs_max8(a[k]);
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+            if (v == 0) atomicMax(rowmax + (tcol % kParts) * rows + r0 + 8 * g + k, m);
+        }
+        // column maxima over this thread's 8 tokens, then over the two token
+        // groups of the warp
+        uint32_t cm[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
             uint32_t m = 0;
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                const uint32_t lo = sm.tile[h * 64 + 2 * k][c];
-                const uint32_t hi = sm.tile[h * 64 + 2 * k + 1][c];
-                vals[k] = lo | (hi << 16);
-                m = max(m, max(lo & 0x7FFFu, hi & 0x7FFFu));
-            }
-            sm.red[h][c] = m;
-            // publish the tile's token maxima (the atomics above) before the
-            // cast and the stores, so that no fence waits for those stores
-            __threadfence();
-            __syncthreads();
-            if (tid == 0) {
-                if (!withhold) atomicAdd(done + stripe, 1u);
-                withhold = false;
-            }
-            m = max(sm.red[0][c], sm.red[1][c]);
-            float mul;
-            const uint32_t sbyte = group_scale<F2, false>(m, mul);
-            uint32_t w[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                if (sbyte == 0xFFu) {
-                    w[k] = kNanCodes;
-                } else {
-                    const uint32_t a = vals[2 * k], b = vals[2 * k + 1];
-                    const uint32_t p0 = cvt2<F2>(__uint_as_float(a << 16) * mul,
-                                                 __uint_as_float(a & 0xFFFF0000u) * mul);
-                    const uint32_t p1 = cvt2<F2>(__uint_as_float(b << 16) * mul,
-                                                 __uint_as_float(b & 0xFFFF0000u) * mul);
-                    w[k] = p0 | (p1 << 16);
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                *reinterpret_cast<uint4 *>(&sm.codes[c][h * 64 + 16 * k]) =
-                    make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-            if (h == 0) st[(c0 + c) * ld_st + stripe] = static_cast<uint8_t>(sbyte);
-            __syncthreads();
-            // transposed rows: 128 columns x 128 tokens, whole 128-byte rows
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int e = tid + kDThreads * k, row = e >> 3, ch = e & 7;
-                *reinterpret_cast<uint4 *>(qt + (c0 + row) * ld_qt + r0 + ch * 16) =
-                    *reinterpret_cast<const uint4 *>(&sm.codes[row][ch * 16]);
-            }
-            __syncthreads();   // sm.tile / sm.codes are free again
-            prefetched = next_first(r);
-            if (prefetched >= 0) issue_tile(prefetched);
-        } else {
-            // -------------------------------------------------- second pass
-            // the tile's re-read (from L2) is issued before the wait
-            uint4 v[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int e = tid + kDThreads * k, r = e >> 4, cv = e & 15;
-                v[k] = ptx::ld_stream_v4(x + (r0 + r) * ld_x + c0 + cv * 8);
-            }
-            if (tid == 0) sm.ok = wait_count(done + stripe, static_cast<uint32_t>(tiles), wait_ns);
-            __syncthreads();
-            if (!sm.ok) {
-                if (tid == 0) atomicOr(err, 8u);
-                cp_async_wait_all();   // no copy into this CTA's shared memory outlives it
-                return;
-            }
-            if (tid < kDT) {
-                uint32_t m = 0;
-#pragma unroll
-                for (int pt = 0; pt < kParts; ++pt)
-                    m = max(m, ld_acquire(rowmax + pt * rows + r0 + tid));
-                const GroupScale<F1, SCALE_UE8M0> gs(m);
-                sm.mul[tid] = gs.mul;
-                sm.nan_row[tid] = gs.nan;
-                if (tcol == 0) gs.store(s, (r0 + tid) * ld_s);
-            }
-            __syncthreads();
-            uint32_t unused = 0;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int e = tid + kDThreads * k, r = e >> 4, cv = e & 15;
-                const uint2 code = sm.nan_row[r] ? make_uint2(kNanCodes, kNanCodes)
-                                                 : quant8<F1, false>(v[k], sm.mul[r], unused);
-                *reinterpret_cast<uint2 *>(q + (r0 + r) * ld_q + c0 + cv * 8) = code;
-            }
-            __syncthreads();   // sm.mul / nan_row are rewritten by the next item
+            for (int k = 0; k < 8; ++k) m = max(m, abs_el(a[k], j));
+            cm[j] = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
         }
+        if (lane < 16) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) sm.cred[warp][j][v] = cm[j];
+        }
+        __syncthreads();
+        // 2. column scales and the transposed codes (staged in shared memory;
+        // this work lets the atomics above complete before the fence below)
+        uint32_t cbyte = 0;   // column tid's scale byte (tid < 128), stored after the count
+        if (tid < kDC) {
+            uint32_t m = 0;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) m = max(m, sm.cred[w][tid & 7][tid >> 3]);
+            float mul;
+            cbyte = group_scale<F2, false>(m, mul);
+            sm.cmul[tid] = mul;
+            sm.cnan[tid] = cbyte == 0xFFu;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int c = 8 * v + j;
+            const float mul = sm.cmul[c];
+            uint2 w;
+            if (sm.cnan[c]) {
+                w = make_uint2(kNanCodes, kNanCodes);
+            } else {
+                const uint32_t p0 = cvt2<F2>(f32_el(a[0], j) * mul, f32_el(a[1], j) * mul);
+                const uint32_t p1 = cvt2<F2>(f32_el(a[2], j) * mul, f32_el(a[3], j) * mul);
+                const uint32_t p2 = cvt2<F2>(f32_el(a[4], j) * mul, f32_el(a[5], j) * mul);
+                const uint32_t p3 = cvt2<F2>(f32_el(a[6], j) * mul, f32_el(a[7], j) * mul);
+                w = make_uint2(p0 | (p1 << 16), p2 | (p3 << 16));
+            }
+            sm.codes[c][(g ^ (c >> 3)) & 15] = w;   // token group g of column c
+        }
+        __threadfence();       // the token maxima are visible before the count
+        __syncthreads();
+        if (tid == 0) {
+            if (!withhold) atomicAdd(done + stripe, 1u);
+            withhold = false;
+        }
+        // the next tile's copies, issued after the fence so that it does not
+        // wait for them
+        if (t + gridDim.x < n1) issue(t + gridDim.x);
+        if (tid < kDC) st[(c0 + tid) * ld_st + stripe] = static_cast<uint8_t>(cbyte);
+        // transposed rows: column c, tokens 16 h .. 16 h + 15 (two token groups)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int e = tid + kDThreads * i, c = e >> 3, h = e & 7;
+            const uint2 lo = sm.codes[c][(2 * h ^ (c >> 3)) & 15];
+            const uint2 hi = sm.codes[c][((2 * h + 1) ^ (c >> 3)) & 15];
+            *reinterpret_cast<uint4 *>(qt + (c0 + c) * ld_qt + r0 + 16 * h) =
+                make_uint4(lo.x, lo.y, hi.x, hi.y);
+        }
+        // 3. per-token codes once the whole stripe has been counted
+        if (tid == 0) sm.ok = wait_count(done + stripe, static_cast<uint32_t>(tiles), wait_ns);
+        __syncthreads();
+        if (!sm.ok) {
+            if (tid == 0) atomicOr(err, 8u);
+            cp_async_wait_all();   // no copy into this CTA's shared memory outlives it
+            return;
+        }
+        if (tid < kDT) {
+            uint32_t m = 0;
+#pragma unroll
+            for (int pt = 0; pt < kParts; ++pt) m = max(m, ld_acquire(rowmax + pt * rows + r0 + tid));
+            const GroupScale<F1, SCALE_UE8M0> gs(m);
+            sm.rmul[tid] = gs.mul;
+            sm.rnan[tid] = gs.nan;
+            if (tcol == 0) gs.store(s, (r0 + tid) * ld_s);
+        }
+        __syncthreads();
+        uint32_t unused = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int r = 8 * g + k;
+            const uint2 code = sm.rnan[r] ? make_uint2(kNanCodes, kNanCodes)
+                                          : quant8<F1, false>(a[k], sm.rmul[r], unused);
+            *reinterpret_cast<uint2 *>(q + (r0 + r) * ld_q + c0 + 8 * v) = code;
+        }
+        __syncthreads();   // sm.cred / codes / rmul are rewritten by the next tile
     }
+    cp_async_wait_all();
 }
 
 std::atomic<int> g_dual_sms[64];
@@ -299,7 +268,15 @@ cudaError_t launch_dual_t(const uint16_t *x, int64_t rows, int64_t cols, int64_t
     e = cudaMemsetAsync(ws, 0, dual_workspace_bytes(rows, cols), stream);
     if (e != cudaSuccess) return e;
     int64_t grid = static_cast<int64_t>(sms) * per_sm;
-    if (grid > 2 * static_cast<int64_t>(stripes) * tiles) grid = 2 * static_cast<int64_t>(stripes) * tiles;
+    if (grid > static_cast<int64_t>(stripes) * tiles) grid = static_cast<int64_t>(stripes) * tiles;
+    if (tiles > grid) {
+        // a stripe wider than one round of the grid (more than ~77k columns
+        // on GB300): the two quantizers, one read each
+        const WaitOpts none{};
+        e = launch_quant_token(x, rows, cols, ld_x, 0, 0, F1, q, ld_q, s, ld_s, none, stream);
+        if (e != cudaSuccess) return e;
+        return launch_quant_token(x, rows, cols, ld_x, 128, 1, F2, qt, ld_qt, st, ld_st, none, stream);
+    }
     uint64_t wait_ns = w.limit_ns ? w.limit_ns : kDualWaitNs;
     int inject = w.inject;
     void *args[] = {&x, &ld_x, &stripes, &tiles, &q, &ld_q, &s, &ld_s, &qt, &ld_qt, &st, &ld_st,
