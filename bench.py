@@ -31,7 +31,7 @@ quantization pass inside the timed region); the sweep's is the quantizers'
 algorithmic bytes over their time (GB/s).  Inputs are seeded synthetic BF16
 tensors resident in HBM.  The JSON line carries the roofline of the dominant
 kernel against a dense FP8 peak measured in the same run (cuBLAS E4M3 8192^3
-through torch._scaled_mm, best of 20), the quantizers' GB/s against the
+through torch._scaled_mm, best single launch), the quantizers' GB/s against the
 measured HBM copy rate, an end-to-end figure with host buffers, the SM clocks
 seen, and the CPU oracle's rate on a bounded sample of the same work.
 
@@ -436,7 +436,8 @@ STEPS = {"linear_step_7b": LinearStep7B, "fprop_1p5b": Fprop1p5B, "tiny_fprop": 
 def fp8_peak_probe(torch, dev, n=8192, sustain_s=4.0):
     """Dense FP8 peak of this GPU, measured: cuBLAS E4M3 x E4M3 -> BF16 at
     n^3 through torch._scaled_mm (tensor-wise unit scales).  Burst = best of
-    20 single launches; sustained = back-to-back launches for ~sustain_s
+    the single launches timed over ~0.4 s (at least 20); sustained =
+    back-to-back launches for ~sustain_s
     seconds, with the SM clocks sampled meanwhile.  None if unavailable."""
     try:
         a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
@@ -448,15 +449,19 @@ def fp8_peak_probe(torch, dev, n=8192, sustain_s=4.0):
             f()
         torch.cuda.synchronize()
         flop = 2.0 * n ** 3
+        # burst: single launches, each timed alone, for ~0.4 s (at least 20)
+        # so that the clock sampler sees the same interval
         clk = ClockSampler(dev.index or 0, period_ms=20).start()
-        best = float("inf")
-        for _ in range(20):
+        time.sleep(0.1)
+        best, count, t0 = float("inf"), 0, time.perf_counter()
+        while count < 20 or time.perf_counter() - t0 < 0.4:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             f()
             e1.record()
             e1.synchronize()
             best = min(best, e0.elapsed_time(e1))
+            count += 1
         burst_clk = clk.stop()
         iters = max(10, int(sustain_s * 1e3 / best))
         clk = ClockSampler(dev.index or 0).start()
@@ -469,10 +474,12 @@ def fp8_peak_probe(torch, dev, n=8192, sustain_s=4.0):
         sus_clk = clk.stop()
         del a, b
         return {"burst_tflops": flop / best / 1e9, "sustained_tflops": flop * iters / e0.elapsed_time(e1) / 1e9,
-                "burst_ms": best, "sustained_launches": iters, "burst_clocks": burst_clk,
+                "burst_ms": best, "burst_launches": count, "sustained_launches": iters,
+                "burst_clocks": burst_clk,
                 "sustained_clocks": sus_clk,
                 "how": f"cuBLAS E4M3 x E4M3 -> BF16, {n}^3, torch._scaled_mm with tensor-wise unit "
-                       f"scales: best of 20 launches (burst) and {iters} back-to-back launches (sustained)"}
+                       f"scales: best of {count} single launches over ~0.4 s (burst) and {iters} "
+                       f"back-to-back launches (sustained)"}
     except Exception as e:   # reported in the line; the fallback denominator is used
         return {"error": repr(e)}
 
