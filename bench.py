@@ -776,10 +776,25 @@ def spawn_replicas(n, argv, script=None, env=None):
         e = dict(base, RANK=str(r), LOCAL_RANK=str(r), WORLD_SIZE=str(n),
                  LOCAL_WORLD_SIZE=str(n), MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
         procs.append(subprocess.Popen([sys.executable, script] + list(argv), env=e))
+    # A rank that fails would leave the others waiting in a collective: once
+    # any rank exits non-zero, the remaining ones are stopped.
     rc = 0
+    while None in [p.poll() for p in procs]:      # poll every rank each pass
+        failed = [p.returncode for p in procs if p.returncode not in (None, 0)]
+        if failed:
+            rc = failed[0]
+            for p in procs:
+                if p.poll() is None:
+                    p.terminate()
+            for p in procs:
+                try:
+                    p.wait(timeout=30)
+                except subprocess.TimeoutExpired:
+                    p.kill()
+            break
+        time.sleep(0.1)
     for p in procs:
-        r = p.wait()
-        rc = rc or r
+        rc = rc or (p.wait() or 0)
     return rc
 
 

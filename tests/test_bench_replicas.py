@@ -42,3 +42,19 @@ def test_a_rank_under_torchrun_does_not_spawn(monkeypatch):
     monkeypatch.setattr(bench, "spawn_replicas", lambda *a: (_ for _ in ()).throw(AssertionError))
     monkeypatch.setattr(bench, "run_reference", lambda args: None)
     assert bench.main(["--gpus", "2", "--impl", "reference"]) == 0
+
+
+def test_a_failing_rank_stops_the_others(tmp_path):
+    """Rank 1 exits with an error before the collective; rank 0 would wait in
+    it forever, so the launcher stops it and returns the failure."""
+    worker = tmp_path / "fail_worker.py"
+    worker.write_text(
+        "import os, sys, time\n"
+        "if os.environ['RANK'] == '1':\n"
+        "    sys.exit(3)\n"
+        "time.sleep(600)\n")
+    code = ("import sys, bench; sys.exit(bench.spawn_replicas(2, [], "
+            f"script={str(worker)!r}))")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
+                       timeout=120)
+    assert r.returncode == 3
