@@ -78,6 +78,10 @@ def _parse(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--launch", default="eager", choices=["eager", "graph"],
+                    help="timed steps replayed from one CUDA graph, or launched one by one")
+    ap.add_argument("--act-quant", default="dual", choices=["dual", "separate"],
+                    help="7B step: both activation layouts from one read, or one call each")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-peak-probe", action="store_true")
@@ -185,18 +189,20 @@ class StepBase:
         self.out_bytes = sum(t.numel() * t.element_size() for t in self.out.values())
         self.flop = float(sum(self.gemm_flop))
 
-    def run(self, ev=None, ready=None, done=None):
+    def run(self, ev=None, ready=None, done=None, external=False):
         """Enqueue one step on the current stream.  ev: optional list that
         receives (kind, start_event, end_event) per launch.  ready: optional
         {input name: event}, waited on before the first launch that reads the
         input.  done: optional dict that receives {output name: event},
-        recorded after the output's last write."""
-        self.launches(_Launcher(self.torch, ev, ready, done))
+        recorded after the output's last write.  external: the timing events
+        are recorded as event nodes of a graph being captured."""
+        self.launches(_Launcher(self.torch, ev, ready, done, external))
 
 
 class _Launcher:
-    def __init__(self, torch, ev, ready, done):
+    def __init__(self, torch, ev, ready, done, external=False):
         self.torch, self.ev, self.ready, self.done, self.waited = torch, ev, ready, done, set()
+        self.ekw = {"enable_timing": True, "external": True} if external else {"enable_timing": True}
 
     def need(self, *names):
         if self.ready is None:
@@ -218,8 +224,8 @@ class _Launcher:
         if self.ev is None:
             fn()
             return
-        a = self.torch.cuda.Event(enable_timing=True)
-        b = self.torch.cuda.Event(enable_timing=True)
+        a = self.torch.cuda.Event(**self.ekw)
+        b = self.torch.cuda.Event(**self.ekw)
         a.record()
         fn()
         b.record()
@@ -238,6 +244,10 @@ def _dual_bytes(n_el, rows):       # one read, both outputs: 2 + 1 + 1 B per ele
     return 4.0 * n_el + rows + n_el / 128.0
 
 
+def _dual_bytes(n_el, rows):        # both layouts from one read: 2 B read + 2 x 1 B written
+    return 4.0 * n_el + rows + n_el / 128.0
+
+
 def _blk_bytes(n_el, transposed):  # 128x128 blocks (+ transposed copy and its scales)
     return (4.0 if transposed else 3.0) * n_el + (2.0 if transposed else 1.0) * n_el / 16384.0
 
@@ -246,8 +256,14 @@ class LinearStep7B(StepBase):
     INPUT_ORDER = ["W_gate", "W_up", "W_down", "X", "H", "dY_gate", "dY_up", "dY_down"]
     GEMM_NAMES = ["fprop_gate", "fprop_up", "fprop_down", "dgrad_gate", "dgrad_up", "dgrad_down",
                   "wgrad_gate", "wgrad_up", "wgrad_down"]
-    QUANT_NAMES = ["W_gate_blk", "W_up_blk", "W_down_blk", "X_tok", "H_tok", "dYg_tok", "dYu_tok",
-                   "dYd_tok", "X_t", "H_t", "dYg_t", "dYu_t", "dYd_t"]
+    ACTS = ("X", "H", "dY_gate", "dY_up", "dY_down")
+    # dual: each activation's per-token and transposed 1x128 codes from one
+    # read (fp8_quant_token_dual); separate: one quantizer call per layout
+    QUANT_NAMES_DUAL = ["W_gate_blk", "W_up_blk", "W_down_blk", "X_dual", "H_dual", "dYg_dual",
+                        "dYu_dual", "dYd_dual"]
+    QUANT_NAMES_SEPARATE = ["W_gate_blk", "W_up_blk", "W_down_blk", "X_tok", "H_tok", "dYg_tok",
+                            "dYu_tok", "dYd_tok", "X_t", "H_t", "dYg_t", "dYu_t", "dYd_t"]
+    ACT_QUANT = "dual"
     WORKLOAD = (f"linear_step_7b: Qwen2.5-7B MLP block (gate/up/down) fprop+dgrad+wgrad, "
                 f"M={M_TOK} tokens, hidden {HID}, MLP {MLP}; per-token E4M3 activations, "
                 f"128x128-block E4M3 weights, per-token E5M2 output grads, 1x128 wgrad re-quant")
@@ -282,9 +298,15 @@ class LinearStep7B(StepBase):
                     "dH": e((M_TOK, MLP), bf), "dW_gate": e((MLP, HID), f32),
                     "dW_up": e((MLP, HID), f32), "dW_down": e((HID, MLP), f32)}
         i = self.inp
+        self.dual = self.ACT_QUANT == "dual"
+        self.QUANT_NAMES = self.QUANT_NAMES_DUAL if self.dual else self.QUANT_NAMES_SEPARATE
+        self.ws = f.dual_workspace(M_TOK, MLP, device) if self.dual else None
         qb = sum(_blk_bytes(i[n].numel(), True) for n in ("W_gate", "W_up", "W_down"))
-        for n in ("X", "H", "dY_gate", "dY_up", "dY_down"):
-            qb += _tok_bytes(i[n].numel(), i[n].shape[0]) + _g128_bytes(i[n].numel())
+        for n in self.ACTS:
+            if self.dual:
+                qb += _dual_bytes(i[n].numel(), i[n].shape[0])
+            else:
+                qb += _tok_bytes(i[n].numel(), i[n].shape[0]) + _g128_bytes(i[n].numel())
         self.quant_bytes = qb
         self.gemm_flop = [2.0 * M_TOK * HID * MLP] * 9
         self._sizes()
@@ -296,17 +318,22 @@ class LinearStep7B(StepBase):
             w, wt = W[n]
             L.need(n)
             L.timed("quant", lambda: f.fp8_quant_block128(i[n], E4, True, out=w, out_t=wt))
-        L.need("X")
-        L.timed("quant", lambda: f.fp8_quant_token(i["X"], 0, E4, out=self.xq))
-        L.need("H")
-        L.timed("quant", lambda: f.fp8_quant_token(i["H"], 0, E4, out=self.hq))
-        for n in ("dY_gate", "dY_up", "dY_down"):
-            L.need(n)
-            L.timed("quant", lambda: f.fp8_quant_token(i[n], 0, E5, out=self.dyq[n]))
-        L.timed("quant", lambda: f.fp8_quant_token(i["X"], 128, E4, True, out=self.xt))
-        L.timed("quant", lambda: f.fp8_quant_token(i["H"], 128, E4, True, out=self.ht))
-        for n in ("dY_gate", "dY_up", "dY_down"):
-            L.timed("quant", lambda: f.fp8_quant_token(i[n], 128, E5, True, out=self.dyt[n]))
+        tok = {"X": (self.xq, self.xt, E4), "H": (self.hq, self.ht, E4)}
+        tok.update({n: (self.dyq[n], self.dyt[n], E5) for n in ("dY_gate", "dY_up", "dY_down")})
+        if self.dual:
+            for n in self.ACTS:
+                q, qt, fmt = tok[n]
+                L.need(n)
+                L.timed("quant", lambda: f.fp8_quant_token_dual(i[n], fmt, out=q, out_t=qt,
+                                                                workspace=self.ws))
+        else:
+            for n in self.ACTS:
+                q, _, fmt = tok[n]
+                L.need(n)
+                L.timed("quant", lambda: f.fp8_quant_token(i[n], 0, fmt, out=q))
+            for n in self.ACTS:
+                _, qt, fmt = tok[n]
+                L.timed("quant", lambda: f.fp8_quant_token(i[n], 128, fmt, True, out=qt))
         g = f.fp8_gemm_scaled
         L.timed("gemm", lambda: g(f.FPROP, self.xq, W["W_gate"][0], out=o["Y_gate"]))
         L.finished("Y_gate")
@@ -862,6 +889,8 @@ def _pipelined_e2e(torch, make_step, step, nsets, nsteps_warm, nsteps, barrier):
 def run_step_config(args, torch, dist, fp8hg, workloads, ri, dev, peaks):
     world, rank = ri.world, ri.rank
     cls = STEPS[args.config]
+    if hasattr(cls, "ACT_QUANT"):
+        cls.ACT_QUANT = args.act_quant
     step = cls(torch, fp8hg, workloads, dev, seed_offset=rank)
     torch.cuda.synchronize()
 
@@ -881,31 +910,55 @@ def run_step_config(args, torch, dist, fp8hg, workloads, ri, dev, peaks):
     # after a 512 MB write that flushes L2 and outside the step's own events.
     flush = (torch.empty(512 * 2 ** 20 // 4, dtype=torch.float32, device=dev)
              if args.config in L2_FLUSHED else None)
+
+    def enqueue_timed(events, per_step, external):
+        for _ in range(args.steps):
+            if flush is not None:
+                flush.fill_(1.0)
+                a = torch.cuda.Event(enable_timing=True, external=external)
+                b = torch.cuda.Event(enable_timing=True, external=external)
+                a.record()
+                step.run(events, external=external)
+                b.record()
+                per_step.append((a, b))
+            else:
+                step.run(events, external=external)
+
+    # Graph launch: the K timed steps are captured once, with each launch's
+    # timing events as event nodes, and the timed region is one replay.
+    launch = args.launch
+    graph = None
+    if launch == "graph":
+        try:
+            events, per_step = [], []
+            graph = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.graph(graph, stream=side):
+                enqueue_timed(events, per_step, True)
+            graph.replay()                      # untimed: uploads the graph
+            barrier()
+        except (TypeError, RuntimeError) as e:  # no external events in this torch
+            graph, launch = None, f"eager (graph capture failed: {type(e).__name__})"
+    if graph is None:
+        events, per_step = [], []
     clocks = ClockSampler(ri.local).start()
     time.sleep(0.2)
-    events = []
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
+    t_start.record()
+    if graph is not None:
+        graph.replay()
+    else:
+        enqueue_timed(events, per_step, False)
+    t_end.record()
+    barrier()
     if flush is None:
-        t_start.record()
-        for _ in range(args.steps):
-            step.run(events)
-        t_end.record()
-        barrier()
         ms = t_start.elapsed_time(t_end) / args.steps
     else:
-        per_step = []
-        for _ in range(args.steps):
-            flush.fill_(1.0)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            step.run(events)
-            b.record()
-            per_step.append((a, b))
-        barrier()
         ms = sum(a.elapsed_time(b) for a, b in per_step) / args.steps
-        del flush
     clk = clocks.stop()
+    del flush
     status = fp8hg.fp8hg_get_device_error()
     if status != 0:
         raise RuntimeError(f"device error: {fp8hg.fp8hg_status_str(status)}")
@@ -958,7 +1011,8 @@ def run_step_config(args, torch, dist, fp8hg, workloads, ri, dev, peaks):
         "dtype": "fp8", "data": "synthetic (seeded; recipe distributions)",
         "config": dict({"workload": cls.WORKLOAD, "name": args.config,
                         "gemms_per_step": ng, "quant_launches_per_step": nq,
-                        "l2": L2_NOTE[args.config],
+                        "l2": L2_NOTE[args.config], "launch": launch,
+                        "act_quant": getattr(cls, "ACT_QUANT", None),
                         "parallelism": "replicas" if world > 1 else "single GPU"}, **cls.DESC),
         "roofline": {"bound": "tensor", "kernel": gemm_kernel, "achieved": gemm_tf,
                      "peak": fp8_peak, "unit": "TFLOP/s", "frac": gemm_tf / fp8_peak,

@@ -64,6 +64,12 @@ __device__ __forceinline__ uint32_t ld_acquire(const unsigned int *p) {
     return v;
 }
 
+__device__ __forceinline__ uint32_t ld_relaxed(const unsigned int *p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // 16-byte asynchronous copy global -> shared (completion by wait_group).
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -155,8 +161,7 @@ __global__ void __launch_bounds__(kDThreads, 4)
             for (int j = 0; j < 8; ++j) sm.cred[warp][j][v] = cm[j];
         }
         __syncthreads();
-        // 2. column scales and the transposed codes (staged in shared memory;
-        // this work lets the atomics above complete before the fence below)
+        // 2. column scales and the transposed codes (staged in shared memory)
         uint32_t cbyte = 0;   // column tid's scale byte (tid < 128), stored after the count
         if (tid < kDC) {
             uint32_t m = 0;
@@ -184,9 +189,12 @@ __global__ void __launch_bounds__(kDThreads, 4)
             }
             sm.codes[c][(g ^ (c >> 3)) & 15] = w;   // token group g of column c
         }
-        __threadfence();       // the token maxima are visible before the count
         __syncthreads();
         if (tid == 0) {
+            // release: one fence, after the barrier, orders every thread's
+            // token maxima of this tile before the count (a fence in every
+            // thread would stall each of them on its own outstanding stores)
+            __threadfence();
             if (!withhold) atomicAdd(done + stripe, 1u);
             withhold = false;
         }
@@ -212,9 +220,12 @@ __global__ void __launch_bounds__(kDThreads, 4)
             return;
         }
         if (tid < kDT) {
+            // thread 0 read the count with acquire and the barrier orders these
+            // loads after it: independent relaxed loads, one round trip (a
+            // chain of acquire loads would cost one round trip each)
             uint32_t m = 0;
 #pragma unroll
-            for (int pt = 0; pt < kParts; ++pt) m = max(m, ld_acquire(rowmax + pt * rows + r0 + tid));
+            for (int pt = 0; pt < kParts; ++pt) m = max(m, ld_relaxed(rowmax + pt * rows + r0 + tid));
             const GroupScale<F1, SCALE_UE8M0> gs(m);
             sm.rmul[tid] = gs.mul;
             sm.rnan[tid] = gs.nan;

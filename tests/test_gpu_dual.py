@@ -41,6 +41,21 @@ def test_dual_matches_oracle(cuda_lib, rows, cols, fmt, fmt_t):
     _check(x, tok, tr, fmt, fmt_t)
 
 
+@pytest.mark.parametrize("rows,cols", [(8192, 1024), (2560, 2560), (256, 18944), (128, 19584)])
+def test_dual_many_tiles_per_cta(cuda_lib, rows, cols):
+    """More tiles than the grid has CTAs, so each CTA streams several tiles
+    and casts each per token a few tiles after its first pass: 16 to 296
+    tiles per stripe (18944 columns: a stripe nearly one round of the grid
+    wide), and 19584 columns (306 tiles, wider than a round: the two
+    quantizers run instead).  A NaN and a zero token included."""
+    x = workloads.make_tensor("act", rows, cols, rows + cols, "dual-many")
+    x[rows - 1, :] = 0.0
+    x[rows // 3, cols - 1] = float("nan")
+    tok, tr = fp8hg.fp8_quant_token_dual(x.cuda(), E4M3, E5M2)
+    assert fp8hg.fp8hg_get_device_error() == 0
+    _check(x, tok, tr, E4M3, E5M2, f"{rows}x{cols}")
+
+
 def test_dual_equals_the_two_quantizers(cuda_lib):
     """[4096, 3584] (the 7B hidden size): the same bytes as the per-token
     quantizer and the transposed 1x128 quantizer, called separately."""
