@@ -50,11 +50,11 @@ struct DualSmem {
     uint4 pre[8][kDThreads];        // next tile: vector k of thread t at pre[k][t] (cp.async;
                                     // consecutive threads, consecutive 16-byte slots)
     uint2 codes[kDC][kDT / 8];      // transposed codes: column c, 8-token groups XOR-swizzled
-    uint32_t cred[8][8][16];        // per-warp column maxima: [warp][j][v] for column 8 v + j
+    uint32_t cred[8][4][16];        // per-warp column maxima, two columns per word:
+                                    // [warp][p][v] holds columns 8 v + 2 p (low), + 1 (high)
     float cmul[kDC];                // column multipliers 2^-e
     uint32_t cnan[kDC];
-    float rmul[kDT];                // token multipliers 2^-e
-    uint32_t rnan[kDT];
+    float rmul[kDT];                // token multipliers 2^-e (NaN: a non-finite token)
     int ok;
 };
 
@@ -92,11 +92,42 @@ __device__ bool wait_count(const unsigned int *counter, uint32_t target, uint64_
     }
 }
 
-// |x| pattern of BF16 element j (0..7) of a 16-byte vector
-__device__ __forceinline__ uint32_t abs_el(const uint4 &v, int j) {
-    const uint32_t w = j < 2 ? v.x : (j < 4 ? v.y : (j < 6 ? v.z : v.w));
-    return ((j & 1) ? (w >> 16) : w) & 0x7FFFu;
+// 32-bit word p (BF16 elements 2 p, 2 p + 1) of a 16-byte vector
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int p) {
+    return p == 0 ? v.x : (p == 1 ? v.y : (p == 2 ? v.z : v.w));
 }
+
+// Two FP32 values times one factor with the packed FP32 multiply (each half
+// correctly rounded, as two separate multiplies; by a power of two, exact).
+__device__ __forceinline__ void mul2(float &a, float &b, float m) {
+    uint64_t x, mm, r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a), "f"(b));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(mm) : "f"(m));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(mm));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+
+// Two BF16 values (lo, hi) scaled by m -> two FP8 codes (lo in the low byte);
+// a NaN multiplier gives the NaN code for both.
+template <int FMT>
+__device__ __forceinline__ uint32_t cast_pair(float lo, float hi, float m) {
+    mul2(lo, hi, m);
+    return cvt2<FMT>(lo, hi);
+}
+
+// One token's 8 consecutive BF16 values -> 8 codes.
+template <int FMT>
+__device__ __forceinline__ uint2 cast_row8(const uint4 &v, float m) {
+    uint32_t c[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const uint32_t w = word_of(v, p);
+        c[p] = cast_pair<FMT>(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u), m);
+    }
+    return make_uint2(__byte_perm(c[0], c[1], 0x5410), __byte_perm(c[2], c[3], 0x5410));
+}
+
+// FP32 value of BF16 element j (0..7) of a 16-byte vector
 __device__ __forceinline__ float f32_el(const uint4 &v, int j) {
     const uint32_t w = j < 2 ? v.x : (j < 4 ? v.y : (j < 6 ? v.z : v.w));
     return __uint_as_float((j & 1) ? (w & 0xFFFF0000u) : (w << 16));
@@ -138,27 +169,30 @@ __global__ void __launch_bounds__(kDThreads, 4)
 #pragma unroll
         for (int k = 0; k < 8; ++k) a[k] = sm.pre[k][tid];
 
-        // 1. token maxima: the 16 threads of a token group reduce over 128 columns
+        // 1. token maxima and column maxima in one pass over the |x| patterns
+        // (two columns per word, sign bits cleared): the 16 threads of a
+        // token group reduce its maximum over 128 columns; each column's over
+        // this thread's 8 tokens, then over the two token groups of the warp
+        uint32_t cp[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            uint32_t m = bf16_abs_max8(a[k]);
+            uint32_t am[4];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                am[p] = word_of(a[k], p) & 0x7FFF7FFFu;
+                cp[p] = __vmaxu2(cp[p], am[p]);
+            }
+            const uint32_t t2 = __vmaxu2(__vmaxu2(am[0], am[1]), __vmaxu2(am[2], am[3]));
+            uint32_t m = max(t2 & 0xFFFFu, t2 >> 16);
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
             if (v == 0) atomicMax(rowmax + (tcol % kParts) * rows + r0 + 8 * g + k, m);
         }
-        // column maxima over this thread's 8 tokens, then over the two token
-        // groups of the warp
-        uint32_t cm[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            uint32_t m = 0;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) m = max(m, abs_el(a[k], j));
-            cm[j] = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
-        }
+        for (int p = 0; p < 4; ++p) cp[p] = __vmaxu2(cp[p], __shfl_xor_sync(0xFFFFFFFFu, cp[p], 16));
         if (lane < 16) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) sm.cred[warp][j][v] = cm[j];
+            for (int p = 0; p < 4; ++p) sm.cred[warp][p][v] = cp[p];
         }
         __syncthreads();
         // 2. column scales and the transposed codes (staged in shared memory)
@@ -166,7 +200,8 @@ __global__ void __launch_bounds__(kDThreads, 4)
         if (tid < kDC) {
             uint32_t m = 0;
 #pragma unroll
-            for (int w = 0; w < 8; ++w) m = max(m, sm.cred[w][tid & 7][tid >> 3]);
+            for (int w = 0; w < 8; ++w) m = __vmaxu2(m, sm.cred[w][(tid & 7) >> 1][tid >> 3]);
+            m = (tid & 1) ? (m >> 16) : (m & 0xFFFFu);
             float mul;
             cbyte = group_scale<F2, false>(m, mul);
             sm.cmul[tid] = mul;
@@ -181,11 +216,11 @@ __global__ void __launch_bounds__(kDThreads, 4)
             if (sm.cnan[c]) {
                 w = make_uint2(kNanCodes, kNanCodes);
             } else {
-                const uint32_t p0 = cvt2<F2>(f32_el(a[0], j) * mul, f32_el(a[1], j) * mul);
-                const uint32_t p1 = cvt2<F2>(f32_el(a[2], j) * mul, f32_el(a[3], j) * mul);
-                const uint32_t p2 = cvt2<F2>(f32_el(a[4], j) * mul, f32_el(a[5], j) * mul);
-                const uint32_t p3 = cvt2<F2>(f32_el(a[6], j) * mul, f32_el(a[7], j) * mul);
-                w = make_uint2(p0 | (p1 << 16), p2 | (p3 << 16));
+                const uint32_t p0 = cast_pair<F2>(f32_el(a[0], j), f32_el(a[1], j), mul);
+                const uint32_t p1 = cast_pair<F2>(f32_el(a[2], j), f32_el(a[3], j), mul);
+                const uint32_t p2 = cast_pair<F2>(f32_el(a[4], j), f32_el(a[5], j), mul);
+                const uint32_t p3 = cast_pair<F2>(f32_el(a[6], j), f32_el(a[7], j), mul);
+                w = make_uint2(__byte_perm(p0, p1, 0x5410), __byte_perm(p2, p3, 0x5410));
             }
             sm.codes[c][(g ^ (c >> 3)) & 15] = w;   // token group g of column c
         }
@@ -226,18 +261,16 @@ __global__ void __launch_bounds__(kDThreads, 4)
             uint32_t m = 0;
 #pragma unroll
             for (int pt = 0; pt < kParts; ++pt) m = max(m, ld_relaxed(rowmax + pt * rows + r0 + tid));
+            // a non-finite token's multiplier is NaN, which casts to NaN codes
             const GroupScale<F1, SCALE_UE8M0> gs(m);
-            sm.rmul[tid] = gs.mul;
-            sm.rnan[tid] = gs.nan;
+            sm.rmul[tid] = gs.nan ? __uint_as_float(0x7FFFFFFFu) : gs.mul;
             if (tcol == 0) gs.store(s, (r0 + tid) * ld_s);
         }
         __syncthreads();
-        uint32_t unused = 0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const int r = 8 * g + k;
-            const uint2 code = sm.rnan[r] ? make_uint2(kNanCodes, kNanCodes)
-                                          : quant8<F1, false>(a[k], sm.rmul[r], unused);
+            const uint2 code = cast_row8<F1>(a[k], sm.rmul[r]);
             *reinterpret_cast<uint2 *>(q + (r0 + r) * ld_q + c0 + 8 * v) = code;
         }
         __syncthreads();   // sm.cred / codes / rmul are rewritten by the next tile
