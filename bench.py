@@ -886,6 +886,51 @@ def _pipelined_e2e(torch, make_step, step, nsets, nsteps_warm, nsteps, barrier):
     return ms
 
 
+def host_link_probe(torch, dev, nbytes=1 << 30, reps=3):
+    """Copy rates between pinned host memory and the device on this machine: host
+    -> device alone, device -> host alone, and both at once (half the bytes
+    each way on two streams), best of `reps`, GB/s."""
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    h.fill_(1)
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    rates = {}
+    for name in ("h2d", "d2h", "both"):
+        best = float("inf")
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            if name == "h2d":
+                d.copy_(h, non_blocking=True)
+            elif name == "d2h":
+                h.copy_(d, non_blocking=True)
+            else:
+                half = nbytes // 2
+                for st_ in (s1, s2):
+                    st_.wait_event(a)
+                with torch.cuda.stream(s1):
+                    d[:half].copy_(h[:half], non_blocking=True)
+                with torch.cuda.stream(s2):
+                    h[half:].copy_(d[half:], non_blocking=True)
+                torch.cuda.current_stream().wait_stream(s1)
+                torch.cuda.current_stream().wait_stream(s2)
+            b.record()
+            torch.cuda.synchronize()
+            best = min(best, a.elapsed_time(b))
+        rates[name] = nbytes / (best * 1e-3) / 1e9
+    del h, d
+    return rates
+
+
+def link_floor_ms(in_bytes, out_bytes, rates):
+    """Lower bound on a step whose inputs cross the host link in and whose
+    outputs cross it out: each direction at its own rate, and all bytes at
+    the rate of both directions together."""
+    return 1e3 * max(in_bytes / (rates["h2d"] * 1e9), out_bytes / (rates["d2h"] * 1e9),
+                     (in_bytes + out_bytes) / (rates["both"] * 1e9))
+
+
 def run_step_config(args, torch, dist, fp8hg, workloads, ri, dev, peaks):
     world, rank = ri.world, ri.rank
     cls = STEPS[args.config]
@@ -981,9 +1026,13 @@ def run_step_config(args, torch, dist, fp8hg, workloads, ri, dev, peaks):
         n_e2e = max(4, min(args.steps, 30))
         e_ms = _pipelined_e2e(torch, make, step, 3, max(args.warmup, 3), n_e2e, barrier)
         e_ms = replicas.max_over_ranks(e_ms, dist, dev)
+        link = host_link_probe(torch, dev)
+        floor = link_floor_ms(step.in_bytes, step.out_bytes, link)
         e2e = {"value": replicas.job_throughput(world, step.flop, e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": step.in_bytes, "d2h_bytes_per_step": step.out_bytes,
                "ms_per_step": e_ms, "steps": n_e2e,
+               "host_link_gbs": {k: round(v, 1) for k, v in link.items()},
+               "link_floor_ms": floor, "frac_of_link_floor": floor / e_ms,
                "note": ("pinned host buffers; three device buffer sets; each input copied in the "
                         "order the step reads it and each output copied back once final, "
                         "overlapped with compute")}

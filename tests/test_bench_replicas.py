@@ -58,3 +58,15 @@ def test_a_failing_rank_stops_the_others(tmp_path):
     r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
                        timeout=120)
     assert r.returncode == 3
+
+
+def test_link_floor_takes_the_binding_term():
+    """The end-to-end floor is the slowest of: inputs at the host->device
+    rate, outputs at the device->host rate, everything at the combined
+    rate."""
+    import bench
+    rates = {"h2d": 200.0, "d2h": 100.0, "both": 250.0}
+    gb = 1e9
+    assert abs(bench.link_floor_ms(2 * gb, 1 * gb, rates) - 12.0) < 1e-9      # combined: 3 / 250
+    assert abs(bench.link_floor_ms(0.5 * gb, 2 * gb, rates) - 20.0) < 1e-9    # out: 2 / 100
+    assert abs(bench.link_floor_ms(4 * gb, 0.1 * gb, rates) - 20.0) < 1e-9    # in: 4 / 200
