@@ -89,6 +89,8 @@ def _parse(argv=None):
     ap.add_argument("--m", type=int, default=4096, help="tokens of a --kernel case")
     ap.add_argument("--n", type=int, default=HID, help="N of the gemm_shape case")
     ap.add_argument("--k", type=int, default=MLP, help="K of the gemm_shape case")
+    ap.add_argument("--split", type=int, default=1,
+                    help="K parts of the gemm_shape case (1 = no split, 0 = the library's choice)")
     ap.add_argument("--tile", type=int, default=0,
                     help="GEMM tile of a --kernel case (0 = the library's choice; see fp8hg_gemm_opts)")
     return ap.parse_args(argv)
@@ -1283,7 +1285,12 @@ def run_kernel_case(args):
         x, w = mk("act", M, args.k, "X"), mk("weight", args.n, args.k, "W")
         a, b = fp8hg.fp8_quant_token(x, 0, E4), fp8hg.fp8_quant_block128(w, E4)
         y = torch.empty((M, args.n), dtype=bf, device=dev)
-        fn = lambda: fp8hg.fp8_gemm_scaled(fp8hg.FPROP, a, b, out=y, tile=args.tile)
+        if args.split == 1:
+            fn = lambda: fp8hg.fp8_gemm_scaled(fp8hg.FPROP, a, b, out=y, tile=args.tile)
+        else:
+            ws = fp8hg.splitk_workspace(M, args.n, args.k, args.split, dev)
+            fn = lambda: fp8hg.fp8_gemm_scaled_splitk(fp8hg.FPROP, a, b, out=y, split_k=args.split,
+                                                      workspace=ws, tile=args.tile)
         work, unit = 2.0 * M * args.n * args.k, "flop"
     elif c == "gemm_mx":
         xa, xb = mk("mx_ln", M, 4096, "A"), mk("mx_ln", 4096, 4096, "B")

@@ -124,13 +124,18 @@ def load_library(build_if_stale: bool = True):
                                         I64, I, I, P]
         lib.fp8_gemm_scaled_ex.argtypes = [I, ctypes.POINTER(Operand), ctypes.POINTER(Operand), P,
                                            I64, I, I, ctypes.POINTER(GemmOpts), P]
+        lib.fp8_gemm_scaled_splitk.argtypes = [I, ctypes.POINTER(Operand), ctypes.POINTER(Operand),
+                                               P, I64, I, I, I, P, ctypes.c_size_t,
+                                               ctypes.POINTER(GemmOpts), P]
+        lib.fp8_gemm_splitk_workspace.argtypes = [I64, I64, I64, I]
+        lib.fp8_gemm_splitk_workspace.restype = ctypes.c_size_t
         lib.fp8hg_get_device_error.argtypes = [P]
         lib.fp8hg_status_str.restype = ctypes.c_char_p
         lib.fp8hg_status_str.argtypes = [I]
         for fn in ("fp8_quant_token", "fp8_quant_block128", "fp8_quant_mx32", "fp8_gemm_scaled",
                    "fp8_gemm_scaled_ex", "fp8hg_get_device_error", "fp8hg_version",
                    "fp8_quant_token_ex", "fp8_requant_t_ex", "fp8_gemm_scaled_f32s_ex",
-                   "fp8_quant_token_dual"):
+                   "fp8_quant_token_dual", "fp8_gemm_scaled_splitk"):
             getattr(lib, fn).restype = I
         _lib = lib
         return lib
@@ -486,6 +491,44 @@ def fp8_gemm_scaled(op: int, a: QTensor, b: QTensor, out=None, out_dtype=None,
         rc = lib().fp8_gemm_scaled(op, ctypes.byref(oa), ctypes.byref(ob), _ptr(out),
                                    out.stride(0), kind, 1 if accumulate else 0, _stream(stream))
     _check(rc, "fp8_gemm_scaled")
+    return out
+
+
+def splitk_workspace(M: int, N: int, K: int, split_k: int = 0, device="cuda"):
+    """Zero-filled scratch for fp8_gemm_scaled_splitk on an [M, K] x [N, K]^T
+    product with split_k parts (0 = what the library's choice needs); None
+    when that choice would not split."""
+    import torch
+    n = int(lib().fp8_gemm_splitk_workspace(M, N, K, split_k))
+    if n == 0:
+        return None
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def fp8_gemm_scaled_splitk(op: int, a: QTensor, b: QTensor, out=None, out_dtype=None,
+                           accumulate: bool = False, split_k: int = 0, workspace=None,
+                           wait_limit_ns: int = 0, inject_fault: int = 0, tile: int = 0,
+                           stream=None):
+    """fp8_gemm_scaled with each tile's K range split over split_k CTAs (0 =
+    the library's choice, given a workspace from splitk_workspace)."""
+    import torch
+    if out is None:
+        dt = out_dtype if out_dtype is not None else torch.bfloat16
+        out = torch.empty((a.codes.shape[0], b.codes.shape[0]), dtype=dt, device=a.codes.device)
+    if out.dtype == torch.bfloat16:
+        kind = OUT_BF16
+    elif out.dtype == torch.float32:
+        kind = OUT_FP32
+    else:
+        raise ValueError("out must be bfloat16 or float32")
+    oa, ob = a.operand(), b.operand()
+    opts = GemmOpts(wait_limit_ns, inject_fault, tile)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib().fp8_gemm_scaled_splitk(op, ctypes.byref(oa), ctypes.byref(ob), _ptr(out),
+                                      out.stride(0), kind, 1 if accumulate else 0, split_k,
+                                      _ptr(workspace), ws_bytes, ctypes.byref(opts),
+                                      _stream(stream))
+    _check(rc, "fp8_gemm_scaled_splitk")
     return out
 
 

@@ -319,6 +319,48 @@ int fp8_gemm_scaled_ex(int op, const fp8hg_operand *a, const fp8hg_operand *b, v
     return run_gemm(g, opts, stream);
 }
 
+size_t fp8_gemm_splitk_workspace(int64_t M, int64_t N, int64_t K, int split_k) {
+    if (M <= 0 || N <= 0 || K <= 0 || M % 256 || N % 128 || K % 128) return 0;
+    if (split_k < 0 || split_k > 8 || split_k > K / 128) return 0;
+    return fp8hg::gemm_splitk_workspace(M, N, K, split_k);
+}
+
+int fp8_gemm_scaled_splitk(int op, const fp8hg_operand *a, const fp8hg_operand *b, void *c,
+                           int64_t ldc, int out, int accumulate, int split_k, void *workspace,
+                           size_t workspace_bytes, const fp8hg_gemm_opts *opts, void *stream) {
+    if (out != FP8HG_OUT_BF16 && out != FP8HG_OUT_FP32) return FP8HG_ERR_INVALID_ARG;
+    if (accumulate != 0 && accumulate != 1) return FP8HG_ERR_INVALID_ARG;
+    if (split_k < 0 || split_k > 8) return FP8HG_ERR_INVALID_ARG;
+    if (opts && (opts->inject_fault < 0 || opts->inject_fault > 2)) return FP8HG_ERR_INVALID_ARG;
+    if (opts && (opts->tile < 0 || opts->tile > 3)) return FP8HG_ERR_INVALID_ARG;
+    fp8hg::GemmArgs g;
+    int st = prepare_gemm(op, a, b, g);
+    if (st != FP8HG_OK) return st;
+    if (!c) return FP8HG_ERR_INVALID_ARG;
+    if (!aligned(c, 16)) return FP8HG_ERR_ALIGNMENT;
+    if (ldc < b->rows) return FP8HG_ERR_INVALID_ARG;
+    if (ldc % (out == FP8HG_OUT_BF16 ? 8 : 4)) return FP8HG_ERR_ALIGNMENT;
+    if (workspace && !aligned(workspace, 256)) return FP8HG_ERR_ALIGNMENT;
+    if (split_k > a->k / 128) return FP8HG_ERR_SHAPE;              // every part >= 1 k-block
+    if (split_k >= 2) {
+        // the split runs on the 256 x 224 tiles
+        if (a->rows % 256 || (opts && opts->tile != 0 && opts->tile != 2))
+            return FP8HG_ERR_UNSUPPORTED;
+        if (!workspace ||
+            workspace_bytes < fp8hg::gemm_splitk_workspace(a->rows, b->rows, a->k, split_k))
+            return FP8HG_ERR_INVALID_ARG;
+    }
+    if (opts && opts->inject_fault == 2 && split_k < 2) return FP8HG_ERR_UNSUPPORTED;
+    g.c = c;
+    g.ldc = ldc;
+    g.out_fp32 = out == FP8HG_OUT_FP32;
+    g.accumulate = accumulate;
+    g.split_k = split_k;
+    g.ws = workspace;
+    g.ws_bytes = workspace ? workspace_bytes : 0;
+    return run_gemm(g, opts, stream);
+}
+
 int fp8_gemm_scaled_q(int op, const fp8hg_operand *a, const fp8hg_operand *b, uint8_t *c_codes,
                       int64_t ld_c, uint8_t *c_scale, int64_t ld_cs, int fmt_c, void *stream) {
     if (!valid_fmt(fmt_c)) return FP8HG_ERR_INVALID_ARG;

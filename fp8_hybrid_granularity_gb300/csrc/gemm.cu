@@ -103,7 +103,43 @@ struct KParams {
     uint32_t idesc;
     uint64_t wait_limit_ns;
     unsigned int *err;
+    // split-K (256 x 224 kernel only): each tile's K range in `split` parts,
+    // work unit u = tile * split + j computing part split - 1 - j; parts >= 1
+    // leave FP32 partial tiles in `ws`, part 0 adds them in part order.
+    int split, num_units;
+    float *ws;               // [num_tiles][split - 1][256][224] FP32
+    unsigned int *flags;     // [num_tiles][8]: partial pieces written, per epilogue warp
 };
+
+// Bounded wait until *flag >= target, read with acquire.  Returns false if
+// the CTA is aborting or the limit ran out (then the abort flag and the
+// device error word are set, as by wait_phase).
+__device__ bool wait_flag(const unsigned int *flag, uint32_t target, uint64_t limit,
+                          volatile uint32_t *abort_flag, unsigned int *err) {
+    const uint64_t t0 = ptx::globaltimer();
+    while (true) {
+        uint32_t v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (v >= target) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer() - t0 > limit) {
+            *abort_flag = 1u;
+            atomicOr(err, 1u);
+            atomicCAS(err + 1, 0u, static_cast<unsigned int>(WHO_EPILOGUE));
+            return false;
+        }
+        __nanosleep(256);
+    }
+}
+
+// Work unit -> (tile, part, k-block range [kb0, kb1)).
+__device__ __forceinline__ void unit_of(int u, const KParams &p, int &tile, int &part, int &kb0,
+                                        int &kb1) {
+    tile = u / p.split;
+    part = p.split - 1 - (u - tile * p.split);
+    kb0 = part * p.nk / p.split;
+    kb1 = (part + 1) * p.nk / p.split;
+}
 
 // Descriptor of a 32-row x 16-byte scale tile (no swizzle; 8-row core
 // matrices of 128 contiguous bytes).
@@ -706,10 +742,11 @@ __global__ void __launch_bounds__(W_THREADS, 1)
         // ------------------------------------------------------ TMA producer
         uint32_t it = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
-            int mb, nb;
+        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+            int tile, part, kb0, kb1, mb, nb;
+            unit_of(u, p, tile, part, kb0, kb1);
             tile_coords(tile, p.num_mb, p.num_nb, mb, nb);
-            for (int kb = 0; kb < p.nk; ++kb) {
+            for (int kb = kb0; kb < kb1; ++kb) {
                 const uint32_t s = it % WSTAGES, ph = (it / WSTAGES) & 1u;
                 ok = wait_phase(sBAR + 32 + 8 * s, ph ^ 1u, limit, abort_flag, p.err, WHO_PRODUCER);
                 ok = __all_sync(0xFFFFFFFFu, ok);
@@ -731,12 +768,14 @@ __global__ void __launch_bounds__(W_THREADS, 1)
         // ------------------------------------------------------- MMA issuer
         uint32_t it = 0, tcount = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+            int tile, part, kb0, kb1;
+            unit_of(u, p, tile, part, kb0, kb1);
             ok = wait_phase(tempty, (tcount & 1u) ^ 1u, limit, abort_flag, p.err, WHO_MMA);
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) break;
             ptx::tc_fence_after();
-            for (int kb = 0; kb < p.nk; ++kb) {
+            for (int kb = kb0; kb < kb1; ++kb) {
                 const uint32_t s = it % WSTAGES, ph = (it / WSTAGES) & 1u;
                 ok = wait_phase(sBAR + 8 * s, ph, limit, abort_flag, p.err, WHO_MMA) &&
                      wait_phase(sBAR + BAR_SF + 8 * s, ph, limit, abort_flag, p.err, WHO_MMA);
@@ -757,7 +796,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
                     for (int j = 0; j < BK / 32; ++j) {
                         const uint32_t idesc = p.idesc | (sf_id(p.gran_a, kb, j) << 29) |
                                                (sf_id(p.gran_b, kb, j) << 4);
-                        const uint32_t acc = (kb | j) != 0 ? 1u : 0u;
+                        const uint32_t acc = (kb != kb0 || j != 0) ? 1u : 0u;
                         ptx::tc_mma_mxf8(tmem, ad0 + 2 * j, bd + 2 * j, idesc, tsfa, tsfb, acc);
                         ptx::tc_mma_mxf8(tmem + WACC1, ad1 + 2 * j, bd + 2 * j, idesc, tsfa + 4, tsfb, acc);
                     }
@@ -779,28 +818,37 @@ __global__ void __launch_bounds__(W_THREADS, 1)
         // warp 2: A's 256 rows, warp 3: B's 224 rows (padded to 256); each
         // keeps its rows' words for one group of G k-blocks in registers with
         // the next group's loads in flight, and arrives on the stage.
+        // A work unit covers k-blocks [kb0, kb1), which may start and end
+        // inside a group.
         const bool is_a = warp == 2;
         uint32_t it = 0;
         bool ok = true;
-        const int ngrp = (p.nk + G - 1) / G;
-        int tile = blockIdx.x, grp = 0;
+        int u = blockIdx.x, tile = 0, part = 0, kb0 = 0, kb1 = 0;
+        if (u < p.num_units) unit_of(u, p, tile, part, kb0, kb1);
+        int grp = kb0 / G;
         WScaleRows cur, nxt;
         auto load = [&](WScaleRows &dst, int t, int gr) {
             if (is_a) load_rows_wide<G, true>(dst, p, t, gr, lane);
             else load_rows_wide<G, false>(dst, p, t, gr, lane);
         };
-        if (tile < p.num_tiles) load(cur, tile, 0);
+        if (u < p.num_units) load(cur, tile, grp);
         const uint32_t sbase = is_a ? sSFA : sSFB;
-        while (tile < p.num_tiles && ok) {
-            int ntile = tile, ngrp_next = grp + 1;
-            if (ngrp_next == ngrp) {
-                ntile += gridDim.x;
-                ngrp_next = 0;
+        while (u < p.num_units && ok) {
+            int nu = u, ntile = tile, nkb0 = kb0, nkb1 = kb1, ngrp_next = grp + 1;
+            if (ngrp_next * G >= kb1) {
+                nu = u + gridDim.x;
+                if (nu < p.num_units) {
+                    int npart;
+                    unit_of(nu, p, ntile, npart, nkb0, nkb1);
+                    ngrp_next = nkb0 / G;
+                }
             }
-            if (ntile < p.num_tiles) load(nxt, ntile, ngrp_next);
+            if (nu < p.num_units) load(nxt, ntile, ngrp_next);
+            const int t_lo = kb0 - G * grp, t_hi = kb1 - G * grp;
 #pragma unroll
             for (int t = 0; t < G; ++t) {
-                if (G * grp + t >= p.nk || !ok) break;
+                if (t < t_lo) continue;
+                if (t >= t_hi || !ok) break;
                 constexpr int kWordStep = G / 4;
                 const int wi = t / kWordStep;
                 const uint32_t s = it % WSTAGES, ph = (it / WSTAGES) & 1u;
@@ -817,16 +865,21 @@ __global__ void __launch_bounds__(W_THREADS, 1)
                 ++it;
             }
             cur = nxt;
+            u = nu;
             tile = ntile;
+            kb0 = nkb0;
+            kb1 = nkb1;
             grp = ngrp_next;
         }
     } else if (warp >= 4) {
         // --------------------------------------------------------- epilogue
-        const int q = warp & 3, half = (warp - 4) >> 2;
-        uint8_t *stage = gbase + WOFF_EPI + (warp - 4) * EPI_WARP_BYTES;
+        const int q = warp & 3, half = (warp - 4) >> 2, ew = warp - 4;
+        uint8_t *stage = gbase + WOFF_EPI + ew * EPI_WARP_BYTES;
         uint32_t tcount = 0;
-        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
-            int mb, nb;
+        bool withhold = p.inject == 2 && blockIdx.x == 0 && ew == 0;
+        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+            int tile, part, kb0, kb1, mb, nb;
+            unit_of(u, p, tile, part, kb0, kb1);
             tile_coords(tile, p.num_mb, p.num_nb, mb, nb);
             bool ok = wait_phase(tfull, tcount & 1u, limit, abort_flag, p.err, WHO_EPILOGUE);
             ok = __all_sync(0xFFFFFFFFu, ok);
@@ -834,6 +887,65 @@ __global__ void __launch_bounds__(W_THREADS, 1)
             ptx::tc_fence_after();
             const int64_t row0 = static_cast<int64_t>(mb) * WBM + half * 128 + q * 32;
             const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + half * WACC1;
+            // this warp's 32 rows of a partial tile of part `pt` (>= 1)
+            auto partial_rows = [&](int pt) {
+                return reinterpret_cast<uint8_t *>(
+                    p.ws + ((static_cast<int64_t>(tile) * (p.split - 1) + (pt - 1)) * WBM +
+                            half * 128 + q * 32) * WBN);
+            };
+            if (part > 0) {
+                // a K part other than the first: its FP32 partial tile goes to
+                // the workspace; the accumulator is free after its last read
+#pragma unroll 1
+                for (int chunk = 0; chunk < WBN / 32; ++chunk) {
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32(taddr + chunk * 32, r);
+                    ptx::tmem_wait_ld();
+                    if (chunk == WBN / 32 - 1) {
+                        ptx::tc_fence_before();
+                        ptx::mbar_arrive(tempty);
+                    }
+                    uint4 v[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        v[c] = make_uint4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
+                    store_piece(stage, v, lane, partial_rows(part) + chunk * 128, WBN * 4);
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    // release: the warp's partial rows before the count
+                    __threadfence();
+                    if (!withhold) atomicAdd(p.flags + tile * 8 + ew, 1u);
+                }
+                withhold = false;
+                ++tcount;
+                continue;
+            }
+            if (p.split > 1) {
+                // the first K part: wait until every other part has written
+                // this warp's rows (bounded), then add them chunk by chunk
+                if (lane == 0)
+                    ok = wait_flag(p.flags + tile * 8 + ew, static_cast<uint32_t>(p.split - 1),
+                                   limit, abort_flag, p.err);
+                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                __syncwarp();              // lane 0's acquire orders every lane's reads below
+                if (!ok) break;
+            }
+            // FP32 partials of parts 1 .. split-1 added to a 32-column chunk of
+            // the accumulator, in part order
+            auto add_partials = [&](uint32_t (&r)[32], int chunk) {
+                for (int pt = 1; pt < p.split; ++pt) {
+                    uint4 v[8];
+                    load_piece(stage, v, lane, partial_rows(pt) + chunk * 128, WBN * 4);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        r[4 * c] = __float_as_uint(__uint_as_float(r[4 * c]) + __uint_as_float(v[c].x));
+                        r[4 * c + 1] = __float_as_uint(__uint_as_float(r[4 * c + 1]) + __uint_as_float(v[c].y));
+                        r[4 * c + 2] = __float_as_uint(__uint_as_float(r[4 * c + 2]) + __uint_as_float(v[c].z));
+                        r[4 * c + 3] = __float_as_uint(__uint_as_float(r[4 * c + 3]) + __uint_as_float(v[c].w));
+                    }
+                }
+            };
             if (p.out_fp32 || p.accumulate) {
                 // FP32 out or accumulation into C: 32 columns at a time, old
                 // values read and new ones written as row
@@ -848,6 +960,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
                         ptx::tc_fence_before();
                         ptx::mbar_arrive(tempty);
                     }
+                    if (p.split > 1) add_partials(r, chunk);
                     auto emit = [&](const uint32_t(&rr)[32], int cc) {
                         const int64_t n0 = static_cast<int64_t>(nb) * WBN + cc * 32;
                         if (n0 >= p.N) return;
@@ -890,6 +1003,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
                     };
                     emit(r, chunk);
                 }
+                if (p.split > 1 && lane == 0) p.flags[tile * 8 + ew] = 0u;   // clean for the next call
                 ++tcount;
                 continue;
             }
@@ -899,6 +1013,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
                 uint32_t r[32];
                 ptx::tmem_ld_32x32b_x32(taddr + chunk * 32, r);
                 ptx::tmem_wait_ld();
+                if (p.split > 1) add_partials(r, chunk);
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
                     packed[chunk * 16 + e] =
@@ -906,6 +1021,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(tempty);
+            if (p.split > 1 && lane == 0) p.flags[tile * 8 + ew] = 0u;   // clean for the next call
             // N is a multiple of 128 and the tile starts at a multiple of 224,
             // so a 64-column piece can straddle N by exactly 32 columns: it is
             // then written as a 32-column half piece.
@@ -1369,7 +1485,52 @@ int g_sms[64] = {0};
 bool g_attr_set[64] = {false};
 std::mutex g_mu;
 
+// Split-K workspace: per-tile flags (8 words per tile, padded to 256 bytes),
+// then the FP32 partial tiles of parts 1 .. split-1.
+size_t splitk_flag_bytes(int64_t tiles) { return (static_cast<size_t>(tiles) * 32 + 255) / 256 * 256; }
+size_t splitk_bytes(int64_t tiles, int split) {
+    if (split <= 1) return 0;
+    return splitk_flag_bytes(tiles) +
+           static_cast<size_t>(tiles) * (split - 1) * WBM * WBN * sizeof(float);
+}
+
+int device_sms() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+
 }  // namespace
+
+int64_t gemm_wide_tiles(int64_t M, int64_t N) { return (M / WBM) * ((N + WBN - 1) / WBN); }
+
+// The library's split for a 256 x 224-tile GEMM.  Cost in k-block times:
+// rounds of units x (k-blocks per unit + 13 per extra part), the exchange
+// cost measured on GB300 (about 10 us per partial tile read by the first
+// part's CTA while it holds its accumulator).  A split is taken only when it
+// is estimated at least 20 % faster: shapes with few tiles and a long K.
+int gemm_auto_split(int64_t M, int64_t N, int64_t K, int sms) {
+    const int64_t tiles = gemm_wide_tiles(M, N), nk = K / BK;
+    const double base = static_cast<double>((tiles + sms - 1) / sms) * static_cast<double>(nk);
+    int best = 1;
+    double best_cost = 0.8 * base;
+    for (int sp = 2; sp <= 8; ++sp) {
+        if (nk / sp < 8) break;
+        const double cost = static_cast<double>((tiles * sp + sms - 1) / sms) *
+                            (static_cast<double>(nk) / sp + 13.0 * (sp - 1));
+        if (cost < best_cost) {
+            best = sp;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
+size_t gemm_splitk_workspace(int64_t M, int64_t N, int64_t K, int split) {
+    if (split == 0) split = gemm_auto_split(M, N, K, device_sms());
+    return splitk_bytes(gemm_wide_tiles(M, N), split);
+}
 
 unsigned int *device_error_word() {
     void *p = nullptr;
@@ -1414,7 +1575,17 @@ int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
     // ~8 % faster tiles do not make up for it.
     const bool paired = g.tile == 3 && !g.out_q && g.M % PR_BM == 0 && sms >= 2;
     bool wide = !paired && !g.out_q && g.M % WBM == 0 && g.tile != 1;
-    if (wide && g.tile != 2) {
+    // split-K: forced (split_k >= 2, wide tiles) or chosen (split_k = 0) when
+    // the workspace holds what the split needs
+    int split = 1;
+    if (wide && g.ws && g.split_k != 1) {
+        split = g.split_k >= 2 ? g.split_k : gemm_auto_split(g.M, g.N, g.K, sms);
+        if (split > 1 && g.ws_bytes < splitk_bytes(gemm_wide_tiles(g.M, g.N), split)) {
+            if (g.split_k >= 2) return 1;
+            split = 1;
+        }
+    }
+    if (wide && g.tile != 2 && split == 1) {
         auto wave_eff = [&](int64_t tiles) {
             const int64_t waves = (tiles + sms - 1) / sms;
             return static_cast<double>(tiles) / static_cast<double>(waves * sms);
@@ -1462,6 +1633,12 @@ int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
               (static_cast<uint32_t>(g.fmt_a) << 7) | (static_cast<uint32_t>(g.fmt_b) << 10);
     p.wait_limit_ns = g.wait_limit_ns;
     p.err = g.err;
+    p.split = split;
+    p.num_units = p.num_tiles * split;
+    p.flags = split > 1 ? static_cast<unsigned int *>(g.ws) : nullptr;
+    p.ws = split > 1 ? reinterpret_cast<float *>(static_cast<uint8_t *>(g.ws) +
+                                                 splitk_flag_bytes(p.num_tiles))
+                     : nullptr;
 
     const bool mx = g.gran_a == GRAN_MX32;
     if (paired) {
@@ -1485,7 +1662,24 @@ int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
         return e == cudaSuccess ? 0 : 2 + static_cast<int>(e);
     }
     int grid = sms;
-    if (grid > p.num_tiles) grid = p.num_tiles;
+    if (grid > p.num_units) grid = p.num_units;
+    if (wide && split > 1) {
+        // a unit of the first K part waits for the other parts of its tile,
+        // which run on other CTAs: every CTA must be resident (cooperative)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(W_THREADS);
+        cfg.dynamicSmemBytes = W_SMEM_BYTES;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = mx ? cudaLaunchKernelEx(&cfg, k_gemm_wide<4>, ta, tb, p)
+                                 : cudaLaunchKernelEx(&cfg, k_gemm_wide<16>, ta, tb, p);
+        return e == cudaSuccess ? 0 : 2 + static_cast<int>(e);
+    }
     if (wide) {
         if (mx) k_gemm_wide<4><<<grid, W_THREADS, W_SMEM_BYTES, stream>>>(ta, tb, p);
         else k_gemm_wide<16><<<grid, W_THREADS, W_SMEM_BYTES, stream>>>(ta, tb, p);

@@ -93,7 +93,15 @@ struct GemmArgs {
     int inject_fault;
     int tile;           // 0 = choose, 1 = 128 x 256, 2 = 256 x 224
     unsigned int *err;  // device error word
+    int split_k = 1;    // 1 = no split, 0 = the library's choice, >= 2 forced
+    void *ws = nullptr; // split-K workspace
+    size_t ws_bytes = 0;
 };
+
+// Split-K (256 x 224 tiles): the library's number of K parts for a shape on
+// `sms` SMs, and the workspace bytes for `split` parts (0 = the library's).
+int gemm_auto_split(int64_t M, int64_t N, int64_t K, int sms);
+size_t gemm_splitk_workspace(int64_t M, int64_t N, int64_t K, int split);
 
 // Returns 0 on success, 1 if the tensor maps could not be encoded, or a
 // cudaError_t + 2 on a launch failure.

@@ -473,6 +473,45 @@ int fp8_gemm_scaled_ex(int op, const fp8hg_operand *a, const fp8hg_operand *b, v
 
 
 /*
+ * fp8_gemm_scaled_splitk — fp8_gemm_scaled with the K range of each output
+ * tile divided into split_k parts that run on different CTAs, for shapes
+ * whose tiles fill only a few waves of SMs (few tiles, long K).  The parts
+ * other than the first write FP32 partial tiles into the workspace; the first
+ * part's CTA waits for them (bounded) and adds them to its accumulator in
+ * part order before the output conversion, so the result is deterministic
+ * (it differs from fp8_gemm_scaled only in FP32 summation order).
+ *
+ * Passage: the same C as fp8_gemm_scaled ("A Comprehensive FP8 Training
+ * Recipe ...", "What carries the argument"); splitting K is this library's
+ * execution strategy and changes no rule of the recipe.
+ *
+ *   op, a, b, c, ldc, out, accumulate   as fp8_gemm_scaled
+ *   split_k    0 = the library's choice (no split where it would not pay,
+ *              or where the workspace is missing or too small), 1 = no
+ *              split, 2..8 = that many parts (at most K/128)
+ *   workspace  device scratch of fp8_gemm_splitk_workspace(M, N, K, split_k)
+ *              bytes (for split_k = 0: what the library's choice needs on
+ *              the current device; 0 bytes means it would not split),
+ *              256-byte aligned, owned by the caller.  Its first bytes are
+ *              per-tile counters that must be ZERO before the first call;
+ *              every call that completes leaves them zero, so the workspace
+ *              can be reused without clearing.  After FP8HG_ERR_TIMEOUT it
+ *              must be cleared again.  Calls that may overlap on the GPU
+ *              need separate workspaces.
+ *   opts       as fp8_gemm_scaled_ex; tile must be 0 or 2 when split_k >= 2;
+ *              inject_fault = 2 (split_k >= 2 only) makes one part withhold
+ *              its completion count, so the first part's wait for it runs
+ *              out (tests of the timeout path)
+ * A split launch is cooperative (every CTA resident at once).
+ * Requirements: as fp8_gemm_scaled; split_k >= 2 also needs M % 256 == 0
+ * (else FP8HG_ERR_UNSUPPORTED).
+ */
+size_t fp8_gemm_splitk_workspace(int64_t M, int64_t N, int64_t K, int split_k);
+int fp8_gemm_scaled_splitk(int op, const fp8hg_operand *a, const fp8hg_operand *b, void *c,
+                           int64_t ldc, int out, int accumulate, int split_k, void *workspace,
+                           size_t workspace_bytes, const fp8hg_gemm_opts *opts, void *stream);
+
+/*
  * fp8_quant_token, fp8_requant_t and fp8_gemm_scaled_f32s with wait options
  * (opts may be NULL = defaults; an inject_fault outside {0, 1} is
  * FP8HG_ERR_INVALID_ARG).  For fp8_quant_token_ex only the per-token

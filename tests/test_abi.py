@@ -15,7 +15,8 @@ EXPECTED = {"fp8_quant_token", "fp8_quant_block128", "fp8_quant_mx32", "fp8_quan
             "fp8_gemm_scaled_ex", "fp8hg_get_device_error", "fp8hg_status_str", "fp8hg_version",
             "fp8_quant_token_ex", "fp8_requant_t_ex", "fp8_gemm_scaled_f32s_ex",
             "fp8_quant_token_dual", "fp8_quant_token_dual_workspace",
-            "fp8_quant_token_dual_noalloc"}
+            "fp8_quant_token_dual_noalloc", "fp8_gemm_scaled_splitk",
+            "fp8_gemm_splitk_workspace"}
 
 OK, INVALID, ALIGN, SHAPE, UNSUP = 0, 1, 2, 3, 4
 FAKE = 0x10000  # never dereferenced: every call below fails validation first
@@ -158,6 +159,42 @@ def test_gemm_options_validation(lib):
     assert call(_op(), fp8hg.GemmOpts(0, 2, 0)) == INVALID        # inject_fault
     assert call(_op(rows=128), fp8hg.GemmOpts(0, 0, 2)) == UNSUP  # 256-row tiles, M = 128
     assert call(_op(rows=384), fp8hg.GemmOpts(0, 0, 3)) == UNSUP  # CTA pairs, M % 256 != 0
+
+
+def test_splitk_validation(lib):
+    """fp8_gemm_scaled_splitk: split_k in 0..8 and at most K/128, forced
+    splits only on 256-row tiles with a large enough, 256-byte aligned
+    workspace, inject_fault 2 only with a split; the workspace size
+    function's layout (flags padded to 256 bytes, then FP32 partial tiles)."""
+    g = lib.fp8_gemm_scaled_splitk
+    W = 1 << 40                      # "large enough" (never touched)
+
+    def sc(k):                        # scale columns, padded to four
+        return (k // 128 + 3) // 4 * 4
+
+    def call(a=None, split=2, ws=FAKE * 256, wsb=W, opts=None, k=1024):
+        a = a or _op(rows=512, k=k, lds=sc(k))
+        b = _op(rows=384, k=k, gran=GRAN_128x128, lds=sc(k))
+        return g(0, ctypes.byref(a), ctypes.byref(b), FAKE, 384, 0, 0,
+                 split, ws, wsb, ctypes.byref(opts) if opts else None, None)
+
+    assert call(split=9) == INVALID
+    assert call(split=-1) == INVALID
+    assert call(split=4, k=384) == SHAPE                          # more parts than k-blocks
+    assert call(a=_op(rows=384, k=1024, lds=8)) == UNSUP          # M % 256
+    assert call(opts=fp8hg.GemmOpts(0, 0, 1)) == UNSUP            # forced 128 x 256 tiles
+    assert call(ws=None) == INVALID
+    assert call(wsb=1000) == INVALID
+    assert call(ws=FAKE * 256 + 16) == ALIGN
+    assert call(opts=fp8hg.GemmOpts(0, 3, 0)) == INVALID          # inject_fault
+    assert call(split=1, opts=fp8hg.GemmOpts(0, 2, 0)) == UNSUP   # injection needs a split
+    ws = lib.fp8_gemm_splitk_workspace
+    tiles = 2 * 2                                                  # 512 / 256 x ceil(384 / 224)
+    assert ws(512, 384, 2048, 2) == 256 + tiles * 1 * 256 * 224 * 4
+    assert ws(512, 384, 2048, 3) == 256 + tiles * 2 * 256 * 224 * 4
+    assert ws(512, 384, 2048, 1) == 0
+    assert ws(384, 384, 2048, 2) == 0                             # M % 256
+    assert ws(512, 384, 256, 3) == 0                              # more parts than k-blocks
 
 
 def test_gemm_validation(lib):
