@@ -132,13 +132,22 @@ __device__ bool wait_flag(const unsigned int *flag, uint32_t target, uint64_t li
     }
 }
 
-// Work unit -> (tile, part, k-block range [kb0, kb1)).
+// Work unit -> (tile, part, k-block range [kb0, kb1)); without SPLIT a unit
+// is a whole tile.
+template <bool SPLIT>
 __device__ __forceinline__ void unit_of(int u, const KParams &p, int &tile, int &part, int &kb0,
                                         int &kb1) {
-    tile = u / p.split;
-    part = p.split - 1 - (u - tile * p.split);
-    kb0 = part * p.nk / p.split;
-    kb1 = (part + 1) * p.nk / p.split;
+    if constexpr (SPLIT) {
+        tile = u / p.split;
+        part = p.split - 1 - (u - tile * p.split);
+        kb0 = part * p.nk / p.split;
+        kb1 = (part + 1) * p.nk / p.split;
+    } else {
+        tile = u;
+        part = 0;
+        kb0 = 0;
+        kb1 = p.nk;
+    }
 }
 
 // Descriptor of a 32-row x 16-byte scale tile (no swizzle; 8-row core
@@ -698,7 +707,8 @@ __device__ __forceinline__ void load_piece64(uint8_t *stage, uint4 (&v)[4], int 
     __syncwarp();
 }
 
-template <int G>
+// SPLIT: the split-K instantiation (work units of one K part of a tile).
+template <int G, bool SPLIT>
 __global__ void __launch_bounds__(W_THREADS, 1)
     k_gemm_wide(const __grid_constant__ CUtensorMap tmap_a,
                 const __grid_constant__ CUtensorMap tmap_b, const KParams p) {
@@ -744,7 +754,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
         bool ok = true;
         for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
             int tile, part, kb0, kb1, mb, nb;
-            unit_of(u, p, tile, part, kb0, kb1);
+            unit_of<SPLIT>(u, p, tile, part, kb0, kb1);
             tile_coords(tile, p.num_mb, p.num_nb, mb, nb);
             for (int kb = kb0; kb < kb1; ++kb) {
                 const uint32_t s = it % WSTAGES, ph = (it / WSTAGES) & 1u;
@@ -770,7 +780,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
         bool ok = true;
         for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
             int tile, part, kb0, kb1;
-            unit_of(u, p, tile, part, kb0, kb1);
+            unit_of<SPLIT>(u, p, tile, part, kb0, kb1);
             ok = wait_phase(tempty, (tcount & 1u) ^ 1u, limit, abort_flag, p.err, WHO_MMA);
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) break;
@@ -824,7 +834,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
         uint32_t it = 0;
         bool ok = true;
         int u = blockIdx.x, tile = 0, part = 0, kb0 = 0, kb1 = 0;
-        if (u < p.num_units) unit_of(u, p, tile, part, kb0, kb1);
+        if (u < p.num_units) unit_of<SPLIT>(u, p, tile, part, kb0, kb1);
         int grp = kb0 / G;
         WScaleRows cur, nxt;
         auto load = [&](WScaleRows &dst, int t, int gr) {
@@ -839,7 +849,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
                 nu = u + gridDim.x;
                 if (nu < p.num_units) {
                     int npart;
-                    unit_of(nu, p, ntile, npart, nkb0, nkb1);
+                    unit_of<SPLIT>(nu, p, ntile, npart, nkb0, nkb1);
                     ngrp_next = nkb0 / G;
                 }
             }
@@ -847,7 +857,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
             const int t_lo = kb0 - G * grp, t_hi = kb1 - G * grp;
 #pragma unroll
             for (int t = 0; t < G; ++t) {
-                if (t < t_lo) continue;
+                if (SPLIT && t < t_lo) continue;
                 if (t >= t_hi || !ok) break;
                 constexpr int kWordStep = G / 4;
                 const int wi = t / kWordStep;
@@ -876,10 +886,10 @@ __global__ void __launch_bounds__(W_THREADS, 1)
         const int q = warp & 3, half = (warp - 4) >> 2, ew = warp - 4;
         uint8_t *stage = gbase + WOFF_EPI + ew * EPI_WARP_BYTES;
         uint32_t tcount = 0;
-        bool withhold = p.inject == 2 && blockIdx.x == 0 && ew == 0;
+        bool withhold = SPLIT && p.inject == 2 && blockIdx.x == 0 && ew == 0;
         for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
             int tile, part, kb0, kb1, mb, nb;
-            unit_of(u, p, tile, part, kb0, kb1);
+            unit_of<SPLIT>(u, p, tile, part, kb0, kb1);
             tile_coords(tile, p.num_mb, p.num_nb, mb, nb);
             bool ok = wait_phase(tfull, tcount & 1u, limit, abort_flag, p.err, WHO_EPILOGUE);
             ok = __all_sync(0xFFFFFFFFu, ok);
@@ -893,7 +903,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
                     p.ws + ((static_cast<int64_t>(tile) * (p.split - 1) + (pt - 1)) * WBM +
                             half * 128 + q * 32) * WBN);
             };
-            if (part > 0) {
+            if (SPLIT && part > 0) {
                 // a K part other than the first: its FP32 partial tile goes to
                 // the workspace; the accumulator is free after its last read
 #pragma unroll 1
@@ -921,7 +931,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
                 ++tcount;
                 continue;
             }
-            if (p.split > 1) {
+            if (SPLIT && p.split > 1) {
                 // the first K part: wait until every other part has written
                 // this warp's rows (bounded), then add them chunk by chunk
                 if (lane == 0)
@@ -946,11 +956,12 @@ __global__ void __launch_bounds__(W_THREADS, 1)
                     }
                 }
             };
-            if (p.out_fp32 || p.accumulate) {
-                // FP32 out or accumulation into C: 32 columns at a time, old
-                // values read and new ones written as row
-                // segments through the staging area; the accumulator is
-                // released after its last columns are read.
+            if (p.out_fp32 || p.accumulate || (SPLIT && p.split > 1)) {
+                // FP32 out, accumulation into C, or a split tile's first part:
+                // 32 columns at a time, old values (and partial tiles) read
+                // and new ones written as row segments through the staging
+                // area; the accumulator is released after its last columns
+                // are read.
 #pragma unroll 1
                 for (int chunk = 0; chunk < WBN / 32; ++chunk) {
                     uint32_t r[32];
@@ -960,7 +971,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
                         ptx::tc_fence_before();
                         ptx::mbar_arrive(tempty);
                     }
-                    if (p.split > 1) add_partials(r, chunk);
+                    if constexpr (SPLIT) add_partials(r, chunk);
                     auto emit = [&](const uint32_t(&rr)[32], int cc) {
                         const int64_t n0 = static_cast<int64_t>(nb) * WBN + cc * 32;
                         if (n0 >= p.N) return;
@@ -981,6 +992,18 @@ __global__ void __launch_bounds__(W_THREADS, 1)
                                     v[c] = make_uint4(rr[4 * c], rr[4 * c + 1], rr[4 * c + 2], rr[4 * c + 3]);
                             }
                             store_piece(stage, v, lane, g, p.ldc * 4);
+                        } else if (!p.accumulate) {
+                            // BF16 (a split tile's first part): round once
+                            uint8_t *g = reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.c) + row0 * p.ldc + n0);
+                            uint4 v[4];
+#pragma unroll
+                            for (int c = 0; c < 4; ++c)
+                                v[c] = make_uint4(
+                                    ptx::cvt_bf16x2(__uint_as_float(rr[8 * c]), __uint_as_float(rr[8 * c + 1])),
+                                    ptx::cvt_bf16x2(__uint_as_float(rr[8 * c + 2]), __uint_as_float(rr[8 * c + 3])),
+                                    ptx::cvt_bf16x2(__uint_as_float(rr[8 * c + 4]), __uint_as_float(rr[8 * c + 5])),
+                                    ptx::cvt_bf16x2(__uint_as_float(rr[8 * c + 6]), __uint_as_float(rr[8 * c + 7])));
+                            store_piece64(stage, v, lane, g, p.ldc * 2);
                         } else {
                             // BF16 with accumulation: add in FP32, round once
                             uint8_t *g = reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.c) + row0 * p.ldc + n0);
@@ -1003,7 +1026,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
                     };
                     emit(r, chunk);
                 }
-                if (p.split > 1 && lane == 0) p.flags[tile * 8 + ew] = 0u;   // clean for the next call
+                if (SPLIT && lane == 0) p.flags[tile * 8 + ew] = 0u;   // clean for the next call
                 ++tcount;
                 continue;
             }
@@ -1013,7 +1036,6 @@ __global__ void __launch_bounds__(W_THREADS, 1)
                 uint32_t r[32];
                 ptx::tmem_ld_32x32b_x32(taddr + chunk * 32, r);
                 ptx::tmem_wait_ld();
-                if (p.split > 1) add_partials(r, chunk);
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
                     packed[chunk * 16 + e] =
@@ -1021,7 +1043,6 @@ __global__ void __launch_bounds__(W_THREADS, 1)
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(tempty);
-            if (p.split > 1 && lane == 0) p.flags[tile * 8 + ew] = 0u;   // clean for the next call
             // N is a multiple of 128 and the tile starts at a multiple of 224,
             // so a 64-column piece can straddle N by exactly 32 columns: it is
             // then written as a 32-column half piece.
@@ -1551,7 +1572,8 @@ int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
                     kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_BYTES));
                 if (e != cudaSuccess) return 2 + static_cast<int>(e);
             }
-            for (auto kern : {k_gemm_wide<16>, k_gemm_wide<4>}) {
+            for (auto kern : {k_gemm_wide<16, false>, k_gemm_wide<4, false>, k_gemm_wide<16, true>,
+                              k_gemm_wide<4, true>}) {
                 const cudaError_t e = cudaFuncSetAttribute(
                     kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(W_SMEM_BYTES));
                 if (e != cudaSuccess) return 2 + static_cast<int>(e);
@@ -1676,13 +1698,13 @@ int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
         attr[0].val.cooperative = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        const cudaError_t e = mx ? cudaLaunchKernelEx(&cfg, k_gemm_wide<4>, ta, tb, p)
-                                 : cudaLaunchKernelEx(&cfg, k_gemm_wide<16>, ta, tb, p);
+        const cudaError_t e = mx ? cudaLaunchKernelEx(&cfg, k_gemm_wide<4, true>, ta, tb, p)
+                                 : cudaLaunchKernelEx(&cfg, k_gemm_wide<16, true>, ta, tb, p);
         return e == cudaSuccess ? 0 : 2 + static_cast<int>(e);
     }
     if (wide) {
-        if (mx) k_gemm_wide<4><<<grid, W_THREADS, W_SMEM_BYTES, stream>>>(ta, tb, p);
-        else k_gemm_wide<16><<<grid, W_THREADS, W_SMEM_BYTES, stream>>>(ta, tb, p);
+        if (mx) k_gemm_wide<4, false><<<grid, W_THREADS, W_SMEM_BYTES, stream>>>(ta, tb, p);
+        else k_gemm_wide<16, false><<<grid, W_THREADS, W_SMEM_BYTES, stream>>>(ta, tb, p);
     } else if (g.out_q) {
         if (mx) k_gemm_mxf8<4, true><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
         else k_gemm_mxf8<16, true><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
