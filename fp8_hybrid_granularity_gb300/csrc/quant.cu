@@ -258,7 +258,8 @@ __device__ __forceinline__ uint32_t top_codes(const uint2 &c) {
 // 256*U consecutive vectors of a row (blockIdx.x) for the rows blockIdx.y,
 // blockIdx.y + gridDim.y, ...; lanes [g*GV, g*GV + GV) of a warp hold one
 // group, and every lane reaches the shuffles.
-template <int FMT, int GV, int SM, bool COUNT, bool MON, int U>
+// D: rows in flight ahead of the one being cast (1 or 2).
+template <int FMT, int GV, int SM, bool COUNT, bool MON, int U, int D>
 __global__ void __launch_bounds__(256) k_quant_groups(const uint16_t *__restrict__ x, int64_t rows,
                                                       int vpr, int64_t ld_x,
                                                       uint8_t *__restrict__ q, int64_t ld_q,
@@ -268,7 +269,7 @@ __global__ void __launch_bounds__(256) k_quant_groups(const uint16_t *__restrict
     const int lane = threadIdx.x & 31;
     const int cv0 = blockIdx.x * (256 * U) + threadIdx.x;
     uint32_t nsat = 0, ntop = 0, nbsat = 0, ncoll = 0;
-    uint4 v[U], nxt[U];
+    uint4 v[U], nxt[U], nxt2[U];
     auto load = [&](int64_t r, uint4 (&dst)[U]) {
         const uint16_t *xr = x + r * ld_x;
 #pragma unroll
@@ -277,11 +278,22 @@ __global__ void __launch_bounds__(256) k_quant_groups(const uint16_t *__restrict
             if (cv < vpr) dst[u] = ptx::ld_stream_v4(xr + static_cast<int64_t>(cv) * 8);
         }
     };
+    // D rows in flight ahead of the one being cast (with few rows per CTA,
+    // each would otherwise wait a full round trip)
+    const int64_t gy = gridDim.y;
     if (static_cast<int64_t>(blockIdx.y) < rows) load(blockIdx.y, nxt);
-    for (int64_t row = blockIdx.y; row < rows; row += gridDim.y) {
+    if (D == 2 && static_cast<int64_t>(blockIdx.y) + gy < rows) load(blockIdx.y + gy, nxt2);
+    for (int64_t row = blockIdx.y; row < rows; row += gy) {
 #pragma unroll
-        for (int u = 0; u < U; ++u) v[u] = nxt[u];
-        if (row + gridDim.y < rows) load(row + gridDim.y, nxt);  // next row in flight
+        for (int u = 0; u < U; ++u) {
+            v[u] = nxt[u];
+            if (D == 2) nxt[u] = nxt2[u];
+        }
+        if (D == 2) {
+            if (row + 2 * gy < rows) load(row + 2 * gy, nxt2);
+        } else if (row + gy < rows) {
+            load(row + gy, nxt);
+        }
         uint32_t row_nsat = 0;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -832,20 +844,37 @@ cudaError_t launch_row(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld
     return cudaGetLastError();
 }
 
+template <int FMT, int GV, int SM, bool COUNT, bool MON, int U, int D>
+cudaError_t launch_groups_ud(const uint16_t *x, int64_t rows, int vpr, int64_t ld_x, uint8_t *q,
+                             int64_t ld_q, uint8_t *s, int64_t ld_s, MxCounters cnt,
+                             cudaStream_t stream, int64_t gx, int64_t gy) {
+    k_quant_groups<FMT, GV, SM, COUNT, MON, U, D>
+        <<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), 256, 0, stream>>>(
+            x, rows, vpr, ld_x, q, ld_q, s, ld_s, cnt);
+    return cudaGetLastError();
+}
+
+// Grid: enough CTAs for every SM's resident slots.  Two rows in flight per
+// CTA, except for the monitor variant when its CTAs have many rows each (its
+// extra registers cost more occupancy than the deeper prefetch gains there).
 template <int FMT, int GV, int SM, bool COUNT, bool MON, int U>
 cudaError_t launch_groups_u(const uint16_t *x, int64_t rows, int vpr, int64_t ld_x, uint8_t *q,
                             int64_t ld_q, uint8_t *s, int64_t ld_s, MxCounters cnt,
                             cudaStream_t stream) {
     const int gx = (vpr + 256 * U - 1) / (256 * U);
-    const int64_t target = static_cast<int64_t>(num_sms()) *
-                           resident_blocks(k_quant_groups<FMT, GV, SM, COUNT, MON, U>, 256);
-    int64_t gy = (target + gx - 1) / gx;
-    if (gy > rows) gy = rows;
-    if (gy > 65535) gy = 65535;
-    if (gy < 1) gy = 1;
-    k_quant_groups<FMT, GV, SM, COUNT, MON, U><<<dim3(gx, static_cast<unsigned>(gy)), 256, 0, stream>>>(
-        x, rows, vpr, ld_x, q, ld_q, s, ld_s, cnt);
-    return cudaGetLastError();
+    auto grid_y = [&](int res) {
+        int64_t gy = (static_cast<int64_t>(num_sms()) * res + gx - 1) / gx;
+        if (gy > rows) gy = rows;
+        if (gy > 65535) gy = 65535;
+        return gy < 1 ? int64_t(1) : gy;
+    };
+    const int64_t gy2 = grid_y(resident_blocks(k_quant_groups<FMT, GV, SM, COUNT, MON, U, 2>, 256));
+    if (!MON || (rows + gy2 - 1) / gy2 <= 16)
+        return launch_groups_ud<FMT, GV, SM, COUNT, MON, U, 2>(x, rows, vpr, ld_x, q, ld_q, s, ld_s,
+                                                             cnt, stream, gx, gy2);
+    const int64_t gy1 = grid_y(resident_blocks(k_quant_groups<FMT, GV, SM, COUNT, MON, U, 1>, 256));
+    return launch_groups_ud<FMT, GV, SM, COUNT, MON, U, 1>(x, rows, vpr, ld_x, q, ld_q, s, ld_s, cnt,
+                                                         stream, gx, gy1);
 }
 
 template <int FMT, int GV, int SM, bool COUNT, bool MON = false>
