@@ -64,11 +64,13 @@ M_TOK, HID, MLP = 16384, 3584, 18944
 GEMM_SRC = os.path.join(ROOT, "fp8_hybrid_granularity_gb300", "csrc", "gemm.cu")
 TENSOR_FLOP_PER_CYCLE_SM = 16384      # dense FP8 MMA rate of one SM (128x256x32 per 128 cycles)
 
-# DRAM bytes per GEMM launch of the 7B step from one ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the gemm.cu
-# it was taken on; any other source gives traffic null.
-GEMM_TRAFFIC = {"gemm_sha256": "5d032afd2ca85a696748a4e9f6591ca2f6dbc11d3d8ec0be52efbdb10a9a70c9",
-                "bytes_per_launch": 1.0969e9}
+# DRAM bytes per GEMM launch of the 7B step (dram__bytes_read.sum +
+# dram__bytes_write.sum): the mean of one full-size launch of each of the
+# step's three GEMM classes (gate-like, down-like, weight gradient; three
+# launches each), captured with ncu; valid only for the gemm.cu it was taken
+# on; any other source gives traffic null.
+GEMM_TRAFFIC = {"gemm_sha256": "f2c8108ac136b78c06071e77b794a987291afe312c4526b76993eb2864c6e319",
+                "bytes_per_launch": 1.1172e9}
 
 
 def _parse(argv=None):
