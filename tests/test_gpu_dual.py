@@ -134,3 +134,15 @@ def test_dual_canary(cuda_lib):
     for buf, r, c, what in ((qb, rows, cols, "codes"), (sb, rows, 1, "scales"),
                             (qtb, cols, rows, "codes^T"), (stb, cols, rows // 128, "scales^T")):
         assert_canary(buf, r, c, what)
+
+
+def test_dual_strided_input(cuda_lib):
+    """x a view into a wider buffer (ld_x = cols + 64): the copies follow the
+    row stride."""
+    rows, cols = 384, 512
+    full = workloads.make_tensor("act", rows, cols + 64, 17, "dual-strided")
+    x = full.cuda()[:, :cols]
+    assert x.stride(0) == cols + 64
+    tok, tr = fp8hg.fp8_quant_token_dual(x, E4M3, E5M2)
+    assert fp8hg.fp8hg_get_device_error() == 0
+    _check(full[:, :cols].contiguous(), tok, tr, E4M3, E5M2, "strided")

@@ -143,3 +143,29 @@ def test_gemm_timeout_path(cuda_lib, tile):
     assert fp8hg.fp8hg_get_device_error() == 0
     c_ref, s_abs = _ref(qa, sa, GRAN_1x128, E4M3, qb, sb, GRAN_128x128, E4M3)
     check_gemm(c.cpu().numpy(), c_ref, s_abs, "after timeout")
+
+
+@pytest.mark.parametrize("tile", TILES)
+def test_gemm_strided_operands(cuda_lib, tile):
+    """Operands and scales that are views into wider buffers (row strides
+    ld > K and ld_scale > the scale columns): the tensor maps and the scale
+    reads follow the strides."""
+    M, N, K = 256, 384, 640
+    qa, sa = _operand("act", M, K, GRAN_1x128, E4M3, 41)
+    qb, sb = _operand("weight", N, K, GRAN_128x128, E4M3, 42)
+
+    def strided(q, s, fmt, gran, pad_k, pad_s):
+        cb = torch.zeros((q.shape[0], q.shape[1] + pad_k), dtype=torch.uint8, device="cuda")
+        cb[:, :q.shape[1]] = torch.from_numpy(np.ascontiguousarray(q)).cuda()
+        ncs = s.shape[1]
+        sbuf = torch.full((s.shape[0], ncs + pad_s), 0x7F, dtype=torch.uint8, device="cuda")
+        sbuf[:, :ncs] = torch.from_numpy(np.ascontiguousarray(s)).cuda()
+        return fp8hg.QTensor(cb[:, :q.shape[1]], sbuf, fmt, gran, ncs)
+
+    a = strided(qa, sa, E4M3, GRAN_1x128, 256, 15)          # ld = K + 256, ld_scale = 5 + 15
+    b = strided(qb, sb, E4M3, GRAN_128x128, 128, 11)        # ld = K + 128, ld_scale = 5 + 11
+    assert a.codes.stride(0) == K + 256 and b.codes.stride(0) == K + 128
+    c = fp8hg.fp8_gemm_scaled(FPROP, a, b, out_dtype=torch.float32, tile=tile)
+    assert fp8hg.fp8hg_get_device_error() == 0
+    c_ref, s_abs = _ref(qa, sa, GRAN_1x128, E4M3, qb, sb, GRAN_128x128, E4M3)
+    check_gemm(c.cpu().numpy(), c_ref, s_abs, "strided operands")
