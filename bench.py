@@ -1082,7 +1082,12 @@ def run_step_config(args, torch, dist, fp8hg, workloads, ri, dev, peaks):
         "gemm_only_tflops": gemm_tf,
         "quant": {"gbs": quant_gbs, "frac_hbm": quant_gbs / peaks["hbm"],
                   "hbm_peak_gbs": peaks["hbm"], "bytes_per_step": step.quant_bytes,
-                  "ms_per_step": quant_step_ms},
+                  "ms_per_step": quant_step_ms,
+                  "bytes_counted": ("dual activation quantizer: 2 B read + 2 B written per "
+                                    "element (both layouts from one read); block weights: "
+                                    "3-4 B per element; + scales"
+                                    if getattr(step, "dual", False) else
+                                    "per call: 2 B read + 1 B written per element + scales")},
         "per_launch_ms": {"gemm": dict(zip(step.GEMM_NAMES, [round(x, 4) for x in per_gemm])),
                           "quant": dict(zip(step.QUANT_NAMES, [round(x, 4) for x in per_quant]))},
         "gpu_launches": (ng + nq) * args.steps,
