@@ -793,12 +793,19 @@ __global__ void __launch_bounds__(W_THREADS, 1)
                 if (!ok) break;
                 ptx::tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t tsfa = tmem + WSFA_COL + 8 * s;
-                    const uint32_t tsfb = tmem + WSFB_COL + 8 * s;
-                    ptx::tc_cp_32x128b_warpx4(tsfa, desc_sf(sSFA + s * WSF_TILE));
-                    ptx::tc_cp_32x128b_warpx4(tsfa + 4, desc_sf(sSFA + s * WSF_TILE + 512));
-                    ptx::tc_cp_32x128b_warpx4(tsfb, desc_sf(sSFB + s * WSF_TILE));
-                    ptx::tc_cp_32x128b_warpx4(tsfb + 4, desc_sf(sSFB + s * WSF_TILE + 512));
+                    // scale words: with 1x128 / 128x128 scales a row's word holds
+                    // the bytes of four consecutive k-blocks, so it is copied into
+                    // tensor memory once per four stages (two slots, alternating);
+                    // MX words change every k-block and are copied every stage
+                    const uint32_t slot = G == 16 ? static_cast<uint32_t>((kb >> 2) & 1) : s;
+                    const uint32_t tsfa = tmem + WSFA_COL + 8 * slot;
+                    const uint32_t tsfb = tmem + WSFB_COL + 8 * slot;
+                    if (G != 16 || (kb & 3) == 0 || kb == kb0) {
+                        ptx::tc_cp_32x128b_warpx4(tsfa, desc_sf(sSFA + s * WSF_TILE));
+                        ptx::tc_cp_32x128b_warpx4(tsfa + 4, desc_sf(sSFA + s * WSF_TILE + 512));
+                        ptx::tc_cp_32x128b_warpx4(tsfb, desc_sf(sSFB + s * WSF_TILE));
+                        ptx::tc_cp_32x128b_warpx4(tsfb + 4, desc_sf(sSFB + s * WSF_TILE + 512));
+                    }
                     const uint64_t ad0 = desc_sw128(sA + s * WA_TILE);
                     const uint64_t ad1 = desc_sw128(sA + s * WA_TILE + WA_TILE / 2);
                     const uint64_t bd = desc_sw128(sB + s * WB_TILE);
