@@ -364,11 +364,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!ok) break;
                 ptx::tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t tsfa = tmem + SFA_COL + 4 * s;
-                    const uint32_t tsfb = tmem + SFB_COL + 8 * s;
-                    ptx::tc_cp_32x128b_warpx4(tsfa, desc_sf(sSFA + s * SFA_TILE));
-                    ptx::tc_cp_32x128b_warpx4(tsfb, desc_sf(sSFB + s * SFB_TILE));
-                    ptx::tc_cp_32x128b_warpx4(tsfb + 4, desc_sf(sSFB + s * SFB_TILE + 512));
+                    // scale words copied once per four k-blocks for 1x128 /
+                    // 128x128 scales (two alternating slots), every stage for MX
+                    const uint32_t slot = G == 16 ? static_cast<uint32_t>((kb >> 2) & 1) : s;
+                    const uint32_t tsfa = tmem + SFA_COL + 4 * slot;
+                    const uint32_t tsfb = tmem + SFB_COL + 8 * slot;
+                    if (G != 16 || (kb & 3) == 0) {
+                        ptx::tc_cp_32x128b_warpx4(tsfa, desc_sf(sSFA + s * SFA_TILE));
+                        ptx::tc_cp_32x128b_warpx4(tsfb, desc_sf(sSFB + s * SFB_TILE));
+                        ptx::tc_cp_32x128b_warpx4(tsfb + 4, desc_sf(sSFB + s * SFB_TILE + 512));
+                    }
                     const uint64_t ad = desc_sw128(sA + s * A_TILE);
                     const uint64_t bd = desc_sw128(sB + s * B_TILE);
 #pragma unroll
@@ -1273,11 +1278,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (!ok) break;
                     ptx::tc_fence_after();
                     if (lane == 0) {
-                        const uint32_t tsfa = tmem + PR_SFA_COL + 4 * s;
-                        const uint32_t tsfb = tmem + PR_SFB_COL + 8 * s;
-                        ptx::tc_cp_32x128b_warpx4_pair(tsfa, desc_sf(sSFA + s * PR_SFA_TILE));
-                        ptx::tc_cp_32x128b_warpx4_pair(tsfb, desc_sf(sSFB + s * PR_SFB_TILE));
-                        ptx::tc_cp_32x128b_warpx4_pair(tsfb + 4, desc_sf(sSFB + s * PR_SFB_TILE + 512));
+                        // scale words copied once per four k-blocks for 1x128 /
+                        // 128x128 scales (two alternating slots), every stage for MX
+                        const uint32_t slot = G == 16 ? static_cast<uint32_t>((kb >> 2) & 1) : s;
+                        const uint32_t tsfa = tmem + PR_SFA_COL + 4 * slot;
+                        const uint32_t tsfb = tmem + PR_SFB_COL + 8 * slot;
+                        if (G != 16 || (kb & 3) == 0) {
+                            ptx::tc_cp_32x128b_warpx4_pair(tsfa, desc_sf(sSFA + s * PR_SFA_TILE));
+                            ptx::tc_cp_32x128b_warpx4_pair(tsfb, desc_sf(sSFB + s * PR_SFB_TILE));
+                            ptx::tc_cp_32x128b_warpx4_pair(tsfb + 4, desc_sf(sSFB + s * PR_SFB_TILE + 512));
+                        }
                         const uint64_t ad = desc_sw128(sA + s * PR_A_TILE);
                         const uint64_t bd = desc_sw128(sB + s * PR_B_TILE);
 #pragma unroll
