@@ -645,11 +645,12 @@ constexpr uint32_t WSFB_COL = 2 * WBN + 8 * WSTAGES;   // + 8 * stage
 constexpr int W_THREADS = 384;
 constexpr uint32_t WOFF_A = 0;
 constexpr uint32_t WOFF_B = WOFF_A + WSTAGES * WA_TILE;
+constexpr int WNSF = 4;              // scale-word buffers, one per scale group
 constexpr uint32_t WOFF_SFA = WOFF_B + WSTAGES * WB_TILE;
-constexpr uint32_t WOFF_SFB = WOFF_SFA + WSTAGES * WSF_TILE;
-constexpr uint32_t WOFF_BAR = WOFF_SFB + WSTAGES * WSF_TILE;
+constexpr uint32_t WOFF_SFB = WOFF_SFA + WNSF * WSF_TILE;
+constexpr uint32_t WOFF_BAR = WOFF_SFB + WNSF * WSF_TILE;
 // barriers as in the 128 x 256 kernel: tma[3] at 0, empty[3] at 32, tfull 64,
-// tempty 72, drain 80, sf[3] at BAR_SF
+// tempty 72, drain 80; scale words: full[4] at BAR_SF, empty[4] at BAR_SF + 32
 constexpr uint32_t WOFF_TMEM_SLOT = WOFF_BAR + 96;
 constexpr uint32_t WOFF_ABORT = WOFF_BAR + 100;
 constexpr uint32_t WOFF_EPI = WOFF_BAR + 256;
@@ -712,6 +713,12 @@ __device__ __forceinline__ void load_piece64(uint8_t *stage, uint4 (&v)[4], int 
     __syncwarp();
 }
 
+// k-blocks that share one 32-bit scale word per row: four for 1x128 / 128x128
+// scales (G = 16: a word holds four k-blocks' bytes), one for MX (G = 4: a
+// word holds the four 32-K slots of one k-block).
+template <int G>
+__device__ __forceinline__ constexpr int kScaleGroupKb() { return G == 16 ? 4 : 1; }
+
 // SPLIT: the split-K instantiation (work units of one K part of a tile).
 template <int G, bool SPLIT>
 __global__ void __launch_bounds__(W_THREADS, 1)
@@ -733,8 +740,11 @@ __global__ void __launch_bounds__(W_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < WSTAGES; ++s) {
             ptx::mbar_init(sBAR + 8 * s, 1);            // TMA expect_tx
-            ptx::mbar_init(sBAR + BAR_SF + 8 * s, 64);  // both scale warps' lanes
             ptx::mbar_init(sBAR + 32 + 8 * s, 1);       // tcgen05.commit
+        }
+        for (int i = 0; i < WNSF; ++i) {
+            ptx::mbar_init(sBAR + BAR_SF + 8 * i, 64);      // words written: both scale warps' lanes
+            ptx::mbar_init(sBAR + BAR_SF + 32 + 8 * i, 1);  // words copied: tcgen05.commit
         }
         ptx::mbar_init(tfull, 1);
         ptx::mbar_init(tempty, 256);
@@ -781,7 +791,15 @@ __global__ void __launch_bounds__(W_THREADS, 1)
                        WHO_PRODUCER, false);
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
-        uint32_t it = 0, tcount = 0;
+        // With 1x128 / 128x128 scales a row's 32-bit scale word holds four
+        // k-blocks' bytes: the words come in groups of four k-blocks through
+        // their own ring of WNSF buffers (the scale warps run up to WNSF
+        // groups ahead of the MMAs, independently of the operand stages) and
+        // each group is copied into one of three tensor-memory slots once,
+        // when its first k-block comes up.  MX words change every k-block:
+        // they ride with the operand stage (buffer and slot = stage), freed by
+        // the stage's own commit.
+        uint32_t it = 0, tcount = 0, sfi = 0, tslot = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
             int tile, part, kb0, kb1;
@@ -792,24 +810,25 @@ __global__ void __launch_bounds__(W_THREADS, 1)
             ptx::tc_fence_after();
             for (int kb = kb0; kb < kb1; ++kb) {
                 const uint32_t s = it % WSTAGES, ph = (it / WSTAGES) & 1u;
+                const bool new_group = kb == kb0 || kb % kScaleGroupKb<G>() == 0;
+                const uint32_t sl = G == 16 ? sfi % WNSF : s;
+                const uint32_t sph = G == 16 ? (sfi / WNSF) & 1u : ph;
                 ok = wait_phase(sBAR + 8 * s, ph, limit, abort_flag, p.err, WHO_MMA) &&
-                     wait_phase(sBAR + BAR_SF + 8 * s, ph, limit, abort_flag, p.err, WHO_MMA);
+                     (!new_group ||
+                      wait_phase(sBAR + BAR_SF + 8 * sl, sph, limit, abort_flag, p.err, WHO_MMA));
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) break;
                 ptx::tc_fence_after();
+                if (new_group) tslot = G == 16 ? sfi % 3 : s;
                 if (lane == 0) {
-                    // scale words: with 1x128 / 128x128 scales a row's word holds
-                    // the bytes of four consecutive k-blocks, so it is copied into
-                    // tensor memory once per four stages (two slots, alternating);
-                    // MX words change every k-block and are copied every stage
-                    const uint32_t slot = G == 16 ? static_cast<uint32_t>((kb >> 2) & 1) : s;
-                    const uint32_t tsfa = tmem + WSFA_COL + 8 * slot;
-                    const uint32_t tsfb = tmem + WSFB_COL + 8 * slot;
-                    if (G != 16 || (kb & 3) == 0 || kb == kb0) {
-                        ptx::tc_cp_32x128b_warpx4(tsfa, desc_sf(sSFA + s * WSF_TILE));
-                        ptx::tc_cp_32x128b_warpx4(tsfa + 4, desc_sf(sSFA + s * WSF_TILE + 512));
-                        ptx::tc_cp_32x128b_warpx4(tsfb, desc_sf(sSFB + s * WSF_TILE));
-                        ptx::tc_cp_32x128b_warpx4(tsfb + 4, desc_sf(sSFB + s * WSF_TILE + 512));
+                    const uint32_t tsfa = tmem + WSFA_COL + 8 * tslot;
+                    const uint32_t tsfb = tmem + WSFB_COL + 8 * tslot;
+                    if (new_group) {
+                        ptx::tc_cp_32x128b_warpx4(tsfa, desc_sf(sSFA + sl * WSF_TILE));
+                        ptx::tc_cp_32x128b_warpx4(tsfa + 4, desc_sf(sSFA + sl * WSF_TILE + 512));
+                        ptx::tc_cp_32x128b_warpx4(tsfb, desc_sf(sSFB + sl * WSF_TILE));
+                        ptx::tc_cp_32x128b_warpx4(tsfb + 4, desc_sf(sSFB + sl * WSF_TILE + 512));
+                        if (G == 16) ptx::tc_commit(sBAR + BAR_SF + 32 + 8 * sl);   // buffer free
                     }
                     const uint64_t ad0 = desc_sw128(sA + s * WA_TILE);
                     const uint64_t ad1 = desc_sw128(sA + s * WA_TILE + WA_TILE / 2);
@@ -825,6 +844,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
                     ptx::tc_commit(sBAR + 32 + 8 * s);
                 }
                 __syncwarp();
+                if (new_group) ++sfi;
                 ++it;
             }
             if (!ok) break;
@@ -839,7 +859,8 @@ __global__ void __launch_bounds__(W_THREADS, 1)
         // ------------------------------------------------- scale loaders
         // warp 2: A's 256 rows, warp 3: B's 224 rows (padded to 256); each
         // keeps its rows' words for one group of G k-blocks in registers with
-        // the next group's loads in flight, and arrives on the stage.
+        // the next group's loads in flight, and writes one buffer of the
+        // scale-word ring per scale group.
         // A work unit covers k-blocks [kb0, kb1), which may start and end
         // inside a group.
         const bool is_a = warp == 2;
@@ -871,18 +892,25 @@ __global__ void __launch_bounds__(W_THREADS, 1)
             for (int t = 0; t < G; ++t) {
                 if (SPLIT && t < t_lo) continue;
                 if (t >= t_hi || !ok) break;
+                // one buffer per scale group: its first k-block (or the unit's)
+                const int kb = G * grp + t;
+                if (!(kb == kb0 || kb % kScaleGroupKb<G>() == 0)) continue;
                 constexpr int kWordStep = G / 4;
                 const int wi = t / kWordStep;
-                const uint32_t s = it % WSTAGES, ph = (it / WSTAGES) & 1u;
-                ok = wait_phase(sBAR + 32 + 8 * s, ph ^ 1u, limit, abort_flag, p.err, WHO_SCALES);
+                // the buffer is free once the MMA warp's copy of its previous
+                // group is done (its own commit; MX: the operand stage's)
+                const uint32_t sl = G == 16 ? it % WNSF : it % WSTAGES;
+                const uint32_t sph = G == 16 ? (it / WNSF) & 1u : (it / WSTAGES) & 1u;
+                ok = wait_phase(sBAR + (G == 16 ? BAR_SF + 32 : 32) + 8 * sl, sph ^ 1u, limit,
+                                abort_flag, p.err, WHO_SCALES);
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) break;
-                const uint32_t d = sbase + s * WSF_TILE + lane * 16;
+                const uint32_t d = sbase + sl * WSF_TILE + lane * 16;
                 st_shared_v4(d, cur.w[0][wi], cur.w[1][wi], cur.w[2][wi], cur.w[3][wi]);
                 st_shared_v4(d + 512, cur.w[4][wi], cur.w[5][wi], cur.w[6][wi], cur.w[7][wi]);
                 if (!(p.inject == 1 && it == 0)) {
                     ptx::fence_proxy_async_smem();
-                    ptx::mbar_arrive(sBAR + BAR_SF + 8 * s);
+                    ptx::mbar_arrive(sBAR + BAR_SF + 8 * sl);
                 }
                 ++it;
             }
