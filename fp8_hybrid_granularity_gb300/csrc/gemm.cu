@@ -278,6 +278,12 @@ __device__ __forceinline__ uint32_t sf_id(int gran, int kb, int j) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// k-blocks that share one 32-bit scale word per row: four for 1x128 / 128x128
+// scales (G = 16: a word holds four k-blocks' bytes), one for MX (G = 4: a
+// word holds the four 32-K slots of one k-block).
+template <int G>
+__device__ __forceinline__ constexpr int kScaleGroupKb() { return G == 16 ? 4 : 1; }
+
 // G: k-blocks per scale group (16, or 4 when the operands are MX32).
 // OUTQ: the epilogue quantizes C (FP8, 1x128 along N) instead of storing it.
 template <int G, bool OUTQ>
@@ -300,8 +306,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(sBAR + 8 * s, 1);            // TMA expect_tx
-            ptx::mbar_init(sBAR + BAR_SF + 8 * s, 32);  // one arrival per scale-warp lane
+
             ptx::mbar_init(sBAR + 32 + 8 * s, 1);       // tcgen05.commit
+        }
+        for (int i = 0; i < STAGES; ++i) {
+            ptx::mbar_init(sBAR + BAR_SF + 8 * i, 32);      // words written: one per scale-warp lane
+            ptx::mbar_init(sBAR + BAR_SF + 32 + 8 * i, 1);  // words copied: tcgen05.commit
         }
         ptx::mbar_init(tfull, 1);
         ptx::mbar_init(tempty, 128);
@@ -349,7 +359,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                        WHO_PRODUCER, false);
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
-        uint32_t it = 0, tcount = 0;
+        // scale words as in the 256 x 224 kernel: with 1x128 / 128x128 scales
+        // one buffer of their own ring per four k-blocks, copied into one of
+        // three tensor-memory slots once; MX words ride with the stage
+        uint32_t it = 0, tcount = 0, sfi = 0, tslot = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
             ok = wait_phase(tempty, (tcount & 1u) ^ 1u, limit, abort_flag, p.err, WHO_MMA);
@@ -358,21 +371,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::tc_fence_after();
             for (int kb = 0; kb < p.nk; ++kb) {
                 const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                const bool new_group = kb % kScaleGroupKb<G>() == 0;
+                const uint32_t sl = G == 16 ? sfi % STAGES : s;
+                const uint32_t sph = G == 16 ? (sfi / STAGES) & 1u : ph;
                 ok = wait_phase(sBAR + 8 * s, ph, limit, abort_flag, p.err, WHO_MMA) &&
-                     wait_phase(sBAR + BAR_SF + 8 * s, ph, limit, abort_flag, p.err, WHO_MMA);
+                     (!new_group ||
+                      wait_phase(sBAR + BAR_SF + 8 * sl, sph, limit, abort_flag, p.err, WHO_MMA));
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) break;
                 ptx::tc_fence_after();
+                if (new_group) tslot = G == 16 ? sfi % 3 : s;
                 if (lane == 0) {
-                    // scale words copied once per four k-blocks for 1x128 /
-                    // 128x128 scales (two alternating slots), every stage for MX
-                    const uint32_t slot = G == 16 ? static_cast<uint32_t>((kb >> 2) & 1) : s;
-                    const uint32_t tsfa = tmem + SFA_COL + 4 * slot;
-                    const uint32_t tsfb = tmem + SFB_COL + 8 * slot;
-                    if (G != 16 || (kb & 3) == 0) {
-                        ptx::tc_cp_32x128b_warpx4(tsfa, desc_sf(sSFA + s * SFA_TILE));
-                        ptx::tc_cp_32x128b_warpx4(tsfb, desc_sf(sSFB + s * SFB_TILE));
-                        ptx::tc_cp_32x128b_warpx4(tsfb + 4, desc_sf(sSFB + s * SFB_TILE + 512));
+                    const uint32_t tsfa = tmem + SFA_COL + 4 * tslot;
+                    const uint32_t tsfb = tmem + SFB_COL + 8 * tslot;
+                    if (new_group) {
+                        ptx::tc_cp_32x128b_warpx4(tsfa, desc_sf(sSFA + sl * SFA_TILE));
+                        ptx::tc_cp_32x128b_warpx4(tsfb, desc_sf(sSFB + sl * SFB_TILE));
+                        ptx::tc_cp_32x128b_warpx4(tsfb + 4, desc_sf(sSFB + sl * SFB_TILE + 512));
+                        if (G == 16) ptx::tc_commit(sBAR + BAR_SF + 32 + 8 * sl);   // buffer free
                     }
                     const uint64_t ad = desc_sw128(sA + s * A_TILE);
                     const uint64_t bd = desc_sw128(sB + s * B_TILE);
@@ -387,6 +403,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ptx::tc_commit(sBAR + 32 + 8 * s);  // frees the smem stage when done
                 }
                 __syncwarp();
+                if (new_group) ++sfi;
                 ++it;
             }
             if (!ok) break;
@@ -418,10 +435,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int t = 0; t < G; ++t) {
                 if (G * grp + t >= p.nk || !ok) break;
+                // one buffer per scale group (four k-blocks; MX: one)
+                if ((G * grp + t) % kScaleGroupKb<G>() != 0) continue;
                 constexpr int kWordStep = G / 4;  // k-blocks per scale word
                 const int wi = t / kWordStep;
+                // free once the MMA warp's copy of its previous group is done
+                // (its own commit; MX: the operand stage's)
                 const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-                ok = wait_phase(sBAR + 32 + 8 * s, ph ^ 1u, limit, abort_flag, p.err, WHO_SCALES);
+                ok = wait_phase(sBAR + (G == 16 ? BAR_SF + 32 : 32) + 8 * s, ph ^ 1u, limit,
+                                abort_flag, p.err, WHO_SCALES);
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) break;
                 // Row r = 32a + lane of a 128-row chunk goes to byte offset
@@ -712,12 +734,6 @@ __device__ __forceinline__ void load_piece64(uint8_t *stage, uint4 (&v)[4], int 
         v[c] = *reinterpret_cast<const uint4 *>(stage + lane * 128 + ((c ^ (lane & 7)) << 4));
     __syncwarp();
 }
-
-// k-blocks that share one 32-bit scale word per row: four for 1x128 / 128x128
-// scales (G = 16: a word holds four k-blocks' bytes), one for MX (G = 4: a
-// word holds the four 32-K slots of one k-block).
-template <int G>
-__device__ __forceinline__ constexpr int kScaleGroupKb() { return G == 16 ? 4 : 1; }
 
 // SPLIT: the split-K instantiation (work units of one K part of a tile).
 template <int G, bool SPLIT>
