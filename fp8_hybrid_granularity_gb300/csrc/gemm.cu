@@ -1148,45 +1148,53 @@ __global__ void __launch_bounds__(W_THREADS, 1)
 }
 
 // ---------------------------------------------------------- CTA-pair variant
-// Tile 256 x 256 computed by a pair of CTAs (a cluster of two) with
+// Tile 256 x 224 computed by a pair of CTAs (a cluster of two) with
 // tcgen05.mma.cta_group::2: each CTA holds its 128 rows of A and its half
-// (128 rows) of B in its own shared memory, the MMA issued by the even CTA
+// (112 rows) of B in its own shared memory, the MMA issued by the even CTA
 // reads both, and each CTA's tensor memory receives its 128 rows of the
-// accumulator.  A stage is then 32 KB per CTA for 128 x 256 x 128 MACs per
-// SM (the 128 x 256 kernel needs 48 KB for the same work), so six stages fit:
-// five stages of operand loads in flight while one is consumed, against two
-// in the 256 x 224 kernel, to hide the latency of a loaded L2.
+// accumulator.  A stage is then 30 KB per CTA for 128 x 224 x 128 MACs per
+// SM, so six stages fit (five in flight while one is consumed, against two
+// 60 KB stages in the 256 x 224 single-CTA kernel), and the accumulator's
+// 224 columns fit twice in tensor memory: the epilogue drains one tile while
+// the MMAs of the next run into the other buffer.
 //   Both CTAs: warp 0 TMA producer (its own A and B halves; completion counted
-//   on the even CTA's stage barrier), warp 2 scale loader (its 128 A rows and
-//   all 256 B rows into its own shared memory; arrivals on the even CTA's
-//   barrier), warps 4-7 epilogue of its 128 rows.  Even CTA: warp 1 issues the
-//   scale-factor copies and MMAs for the pair and commits to both CTAs'
-//   barriers.  Tensor memory (both CTAs): accumulator columns 0-255, then per
-//   stage 4 columns of A scales and 8 of B scales.
-constexpr int PR_BM = 256, PR_BN = 256, PR_STAGES = 6;
-constexpr uint32_t PR_A_TILE = 128 * BK;   // per CTA
-constexpr uint32_t PR_B_TILE = 128 * BK;   // per CTA (its half of B)
+//   on the even CTA's stage barrier), warps 2 and 3 scale loaders (this CTA's
+//   128 A rows; all 224 B rows), writing one buffer of an eight-deep ring per
+//   scale group (four k-blocks for 1x128 / 128x128 scales, one for MX) and
+//   arriving on their own CTA's barrier, warps 4-7 epilogue of its 128 rows.
+//   Even CTA: warp 1 copies each scale group into tensor memory and issues the
+//   MMAs for the pair, committing to both CTAs' barriers.  Odd CTA: warp 1
+//   forwards each filled scale buffer to the even CTA (one cluster-scope
+//   release arrival from a warp with no loads in flight, so the arrival does
+//   not wait for the scale warps' look-ahead loads).
+//   Tensor memory (both CTAs): accumulators at columns 0 and 224, then three
+//   slots of 4 columns of A scales and 8 of B scales.
+constexpr int PR_BM = 256, PR_BN = 224, PR_STAGES = 6, PR_NSF = 8;
+constexpr int PR_THREADS = 256;
+constexpr uint32_t PR_A_TILE = 128 * BK;            // per CTA
+constexpr uint32_t PR_B_TILE = (PR_BN / 2) * BK;    // per CTA (its half of B)
 constexpr uint32_t PR_SFA_TILE = 512, PR_SFB_TILE = 1024;
-constexpr uint32_t PR_SFA_COL = 256;                     // + 4 * stage
-constexpr uint32_t PR_SFB_COL = 256 + 4 * PR_STAGES;     // + 8 * stage
+constexpr uint32_t PR_SFA_COL = 2 * PR_BN;          // + 4 * slot
+constexpr uint32_t PR_SFB_COL = 2 * PR_BN + 12;     // + 8 * slot
 constexpr uint32_t PR_OFF_A = 0;
 constexpr uint32_t PR_OFF_B = PR_OFF_A + PR_STAGES * PR_A_TILE;
 constexpr uint32_t PR_OFF_SFA = PR_OFF_B + PR_STAGES * PR_B_TILE;
-constexpr uint32_t PR_OFF_SFB = PR_OFF_SFA + PR_STAGES * PR_SFA_TILE;
-constexpr uint32_t PR_OFF_BAR = PR_OFF_SFB + PR_STAGES * PR_SFB_TILE;
+constexpr uint32_t PR_OFF_SFB = PR_OFF_SFA + PR_NSF * PR_SFA_TILE;
+constexpr uint32_t PR_OFF_BAR = PR_OFF_SFB + PR_NSF * PR_SFB_TILE;
 // barriers from PR_OFF_BAR (8 bytes each): full[6] at 0 (operand bytes of both
-// CTAs; even CTA), empty[6] at 48 (each CTA), sf[6] at 96 (scale words of both
-// CTAs, one arrival per scale warp; even CTA), tfull 144 (each CTA), tempty
-// 152 (one arrival per epilogue warp of both CTAs; even CTA), drain 160.
-// Cross-CTA arrivals carry cluster-scope release semantics, so each warp
-// arrives once, after __syncwarp, rather than once per lane.
-constexpr uint32_t PR_BAR_EMPTY = 48, PR_BAR_SF = 96, PR_BAR_TFULL = 144, PR_BAR_TEMPTY = 152,
-                   PR_BAR_DRAIN = 160;
-constexpr uint32_t PR_OFF_TMEM_SLOT = PR_OFF_BAR + 168;
-constexpr uint32_t PR_OFF_ABORT = PR_OFF_BAR + 172;
-constexpr uint32_t PR_OFF_EPI = PR_OFF_BAR + 256;
+// CTAs; even CTA), empty[6] at 48 (each CTA), sf_local[8] at 96 (this CTA's
+// scale words written; 64 arrivals), sf_peer[8] at 160 (the odd CTA's words
+// written, forwarded; even CTA), sf_empty[8] at 224 (the pair's copy of the
+// buffer done; each CTA), tfull[2] at 288 (each CTA), tempty[2] at 304 (one
+// arrival per epilogue warp of both CTAs; even CTA), drain 320.
+constexpr uint32_t PR_BAR_EMPTY = 48, PR_BAR_SFL = 96, PR_BAR_SFP = 160, PR_BAR_SFE = 224,
+                   PR_BAR_TFULL = 288, PR_BAR_TEMPTY = 304, PR_BAR_DRAIN = 320;
+constexpr uint32_t PR_OFF_TMEM_SLOT = PR_OFF_BAR + 336;
+constexpr uint32_t PR_OFF_ABORT = PR_OFF_BAR + 340;
+constexpr uint32_t PR_OFF_EPI = PR_OFF_BAR + 384;
 constexpr uint32_t PR_SMEM_BYTES = PR_OFF_EPI + 4 * EPI_WARP_BYTES + 1024;
-static_assert(PR_SFB_COL + 8 * PR_STAGES <= TMEM_COLS, "tensor memory overflow");
+static_assert(PR_B_TILE % 1024 == 0, "B stage must keep the 128-byte swizzle's 1 KB alignment");
+static_assert(PR_SFB_COL + 8 * 3 <= TMEM_COLS, "tensor memory overflow");
 static_assert(PR_SMEM_BYTES <= 232448, "shared memory overflow");
 
 // Wait on a barrier of this CTA whose arrivals may come from the other CTA of
@@ -1213,10 +1221,10 @@ __device__ bool wait_phase_pair(uint32_t bar, uint32_t parity, uint64_t limit,
     }
 }
 
-// Pair tile t -> (m-block of 256 rows, n-block of 256 columns); the same
+// Pair tile t -> (m-block of 256 rows, n-block of 224 columns); the same
 // grouped order as the other kernels.
 template <int G>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(PR_THREADS, 1)
     k_gemm_pair(const __grid_constant__ CUtensorMap tmap_a,
                 const __grid_constant__ CUtensorMap tmap_b, const KParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1225,7 +1233,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t *gbase = smem_raw + (base - raw);
     const uint32_t sA = base + PR_OFF_A, sB = base + PR_OFF_B;
     const uint32_t sSFA = base + PR_OFF_SFA, sSFB = base + PR_OFF_SFB, sBAR = base + PR_OFF_BAR;
-    const uint32_t empty = sBAR + PR_BAR_EMPTY, sfbar = sBAR + PR_BAR_SF;
+    const uint32_t empty = sBAR + PR_BAR_EMPTY, sf_local = sBAR + PR_BAR_SFL,
+                   sf_peer = sBAR + PR_BAR_SFP, sf_empty = sBAR + PR_BAR_SFE;
     const uint32_t tfull = sBAR + PR_BAR_TFULL, tempty = sBAR + PR_BAR_TEMPTY,
                    drain = sBAR + PR_BAR_DRAIN;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + PR_OFF_TMEM_SLOT);
@@ -1238,17 +1247,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint64_t drain_limit = 2000000ull;
     // the even CTA's barriers, as seen from either CTA
     const uint32_t full_l = ptx::map_shared_rank(sBAR, 0);
-    const uint32_t sf_l = ptx::map_shared_rank(sfbar, 0);
+    const uint32_t sf_peer_l = ptx::map_shared_rank(sf_peer, 0);
     const uint32_t tempty_l = ptx::map_shared_rank(tempty, 0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < PR_STAGES; ++s) {
             ptx::mbar_init(sBAR + 8 * s, 1);        // even CTA's expect_tx (both CTAs' bytes)
             ptx::mbar_init(empty + 8 * s, 1);       // the pair's commit
-            ptx::mbar_init(sfbar + 8 * s, 2);       // one arrival per CTA's scale warp
         }
-        ptx::mbar_init(tfull, 1);
-        ptx::mbar_init(tempty, 8);                  // one arrival per epilogue warp of both CTAs
+        for (int i = 0; i < PR_NSF; ++i) {
+            ptx::mbar_init(sf_local + 8 * i, 64);   // every lane of both scale warps
+            ptx::mbar_init(sf_peer + 8 * i, 1);     // the odd CTA's forwarder
+            ptx::mbar_init(sf_empty + 8 * i, 1);    // the pair's commit after the copy
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(tfull + 8 * b, 1);
+            ptx::mbar_init(tempty + 8 * b, 8);      // one arrival per epilogue warp of both CTAs
+        }
         ptx::mbar_init(drain, 1);
         *abort_flag = 0u;
         ptx::fence_mbar_init();
@@ -1273,7 +1288,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tile_coords(tile, p.num_mb, p.num_nb, mb, nb);
             for (int kb = 0; kb < p.nk; ++kb) {
                 const uint32_t s = it % PR_STAGES, ph = (it / PR_STAGES) & 1u;
-                ok = wait_phase_pair(empty + 8 * s, ph ^ 1u, limit, abort_flag, p.err, WHO_PRODUCER);
+                ok = wait_phase(empty + 8 * s, ph ^ 1u, limit, abort_flag, p.err, WHO_PRODUCER);
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) break;
                 if (lane == 0) {
@@ -1282,7 +1297,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ptx::tma_load_2d_pair(sA + s * PR_A_TILE, &tmap_a, full_l + 8 * s, kb * BK,
                                           mb * PR_BM + static_cast<int>(rank) * 128);
                     ptx::tma_load_2d_pair(sB + s * PR_B_TILE, &tmap_b, full_l + 8 * s, kb * BK,
-                                          nb * PR_BN + static_cast<int>(rank) * 128);
+                                          nb * PR_BN + static_cast<int>(rank) * (PR_BN / 2));
                 }
                 __syncwarp();
                 ++it;
@@ -1293,8 +1308,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (leader) {
             const uint32_t nd = it < static_cast<uint32_t>(PR_STAGES) ? it : static_cast<uint32_t>(PR_STAGES);
             for (uint32_t i = it - nd; i < it; ++i)
-                wait_phase_pair(sBAR + 8 * (i % PR_STAGES), (i / PR_STAGES) & 1u, drain_limit,
-                                abort_flag, p.err, WHO_PRODUCER, false);
+                wait_phase(sBAR + 8 * (i % PR_STAGES), (i / PR_STAGES) & 1u, drain_limit,
+                           abort_flag, p.err, WHO_PRODUCER, false);
         }
         // A CTA that stopped early cannot tell which of its last copies the
         // even CTA's barriers have counted; it gives them the drain bound to
@@ -1304,78 +1319,105 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             while (ptx::globaltimer() - t0 < drain_limit) {
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 && leader) {
         // ------------------------------------------- MMA issuer (even CTA)
-        if (leader) {
-            uint32_t it = 0, tcount = 0;
-            bool ok = true;
-            for (int tile = pair; tile < p.num_tiles && ok; tile += npairs) {
-                ok = wait_phase_pair(tempty, (tcount & 1u) ^ 1u, limit, abort_flag, p.err, WHO_MMA);
+        // Scale groups come through the ring in order (sfi); each is copied
+        // into one of three tensor-memory slots when its first k-block comes
+        // up, and its buffer is released by the copy's commit.
+        uint32_t it = 0, tcount = 0, sfi = 0, tslot = 0;
+        bool ok = true;
+        for (int tile = pair; tile < p.num_tiles && ok; tile += npairs) {
+            const uint32_t b = tcount & 1u, use = tcount >> 1;
+            ok = wait_phase_pair(tempty + 8 * b, (use & 1u) ^ 1u, limit, abort_flag, p.err, WHO_MMA);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const uint32_t dacc = tmem + b * PR_BN;
+            for (int kb = 0; kb < p.nk; ++kb) {
+                const uint32_t s = it % PR_STAGES, ph = (it / PR_STAGES) & 1u;
+                const bool new_group = kb % kScaleGroupKb<G>() == 0;
+                const uint32_t sl = sfi % PR_NSF, sph = (sfi / PR_NSF) & 1u;
+                ok = wait_phase(sBAR + 8 * s, ph, limit, abort_flag, p.err, WHO_MMA) &&
+                     (!new_group ||
+                      (wait_phase(sf_local + 8 * sl, sph, limit, abort_flag, p.err, WHO_MMA) &&
+                       wait_phase_pair(sf_peer + 8 * sl, sph, limit, abort_flag, p.err, WHO_MMA)));
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) break;
                 ptx::tc_fence_after();
-                for (int kb = 0; kb < p.nk; ++kb) {
-                    const uint32_t s = it % PR_STAGES, ph = (it / PR_STAGES) & 1u;
-                    ok = wait_phase_pair(sBAR + 8 * s, ph, limit, abort_flag, p.err, WHO_MMA) &&
-                         wait_phase_pair(sfbar + 8 * s, ph, limit, abort_flag, p.err, WHO_MMA);
-                    ok = __all_sync(0xFFFFFFFFu, ok);
-                    if (!ok) break;
-                    ptx::tc_fence_after();
-                    if (lane == 0) {
-                        // scale words copied once per four k-blocks for 1x128 /
-                        // 128x128 scales (two alternating slots), every stage for MX
-                        const uint32_t slot = G == 16 ? static_cast<uint32_t>((kb >> 2) & 1) : s;
-                        const uint32_t tsfa = tmem + PR_SFA_COL + 4 * slot;
-                        const uint32_t tsfb = tmem + PR_SFB_COL + 8 * slot;
-                        if (G != 16 || (kb & 3) == 0) {
-                            ptx::tc_cp_32x128b_warpx4_pair(tsfa, desc_sf(sSFA + s * PR_SFA_TILE));
-                            ptx::tc_cp_32x128b_warpx4_pair(tsfb, desc_sf(sSFB + s * PR_SFB_TILE));
-                            ptx::tc_cp_32x128b_warpx4_pair(tsfb + 4, desc_sf(sSFB + s * PR_SFB_TILE + 512));
-                        }
-                        const uint64_t ad = desc_sw128(sA + s * PR_A_TILE);
-                        const uint64_t bd = desc_sw128(sB + s * PR_B_TILE);
-#pragma unroll
-                        for (int j = 0; j < BK / 32; ++j) {
-                            const uint32_t idesc = p.idesc | (sf_id(p.gran_a, kb, j) << 29) |
-                                                   (sf_id(p.gran_b, kb, j) << 4);
-                            ptx::tc_mma_mxf8_pair(tmem + ACC_COL, ad + 2 * j, bd + 2 * j, idesc, tsfa,
-                                                  tsfb, (kb | j) != 0 ? 1u : 0u);
-                        }
-                        ptx::tc_commit_pair(empty + 8 * s, 0x3);   // frees the stage in both CTAs
+                if (new_group) tslot = sfi % 3;
+                if (lane == 0) {
+                    const uint32_t tsfa = tmem + PR_SFA_COL + 4 * tslot;
+                    const uint32_t tsfb = tmem + PR_SFB_COL + 8 * tslot;
+                    if (new_group) {
+                        ptx::tc_cp_32x128b_warpx4_pair(tsfa, desc_sf(sSFA + sl * PR_SFA_TILE));
+                        ptx::tc_cp_32x128b_warpx4_pair(tsfb, desc_sf(sSFB + sl * PR_SFB_TILE));
+                        ptx::tc_cp_32x128b_warpx4_pair(tsfb + 4, desc_sf(sSFB + sl * PR_SFB_TILE + 512));
+                        ptx::tc_commit_pair(sf_empty + 8 * sl, 0x3);   // the buffer, both CTAs
                     }
-                    __syncwarp();
-                    ++it;
+                    const uint64_t ad = desc_sw128(sA + s * PR_A_TILE);
+                    const uint64_t bd = desc_sw128(sB + s * PR_B_TILE);
+#pragma unroll
+                    for (int j = 0; j < BK / 32; ++j) {
+                        const uint32_t idesc = p.idesc | (sf_id(p.gran_a, kb, j) << 29) |
+                                               (sf_id(p.gran_b, kb, j) << 4);
+                        ptx::tc_mma_mxf8_pair(dacc, ad + 2 * j, bd + 2 * j, idesc, tsfa, tsfb,
+                                              (kb | j) != 0 ? 1u : 0u);
+                    }
+                    ptx::tc_commit_pair(empty + 8 * s, 0x3);   // frees the stage in both CTAs
                 }
-                if (!ok) break;
-                if (lane == 0) ptx::tc_commit_pair(tfull, 0x3);
                 __syncwarp();
-                ++tcount;
+                if (new_group) ++sfi;
+                ++it;
             }
-            if (lane == 0) ptx::tc_commit_pair(drain, 0x1);
+            if (!ok) break;
+            if (lane == 0) ptx::tc_commit_pair(tfull + 8 * b, 0x3);
             __syncwarp();
-            wait_phase_pair(drain, 0u, drain_limit, abort_flag, p.err, WHO_MMA, false);
+            ++tcount;
         }
-    } else if (warp == 2) {
-        // ------------------------------------------------------ scale loader
-        // this CTA's 128 A rows and all 256 B rows of the pair tile
+        if (lane == 0) ptx::tc_commit_pair(drain, 0x1);
+        __syncwarp();
+        wait_phase(drain, 0u, drain_limit, abort_flag, p.err, WHO_MMA, false);
+    } else if (warp == 1) {
+        // ------------------------------------ scale-buffer forwarder (odd CTA)
+        uint32_t sfi = 0;
+        bool ok = true;
+        for (int tile = pair; tile < p.num_tiles && ok; tile += npairs) {
+            for (int kb = 0; kb < p.nk; kb += kScaleGroupKb<G>()) {
+                const uint32_t sl = sfi % PR_NSF, sph = (sfi / PR_NSF) & 1u;
+                ok = wait_phase(sf_local + 8 * sl, sph, limit, abort_flag, p.err, WHO_SCALES);
+                ok = __all_sync(0xFFFFFFFFu, ok);
+                if (!ok) break;
+                if (lane == 0) ptx::mbar_arrive_cluster(sf_peer_l + 8 * sl);
+                __syncwarp();
+                ++sfi;
+            }
+        }
+    } else if (warp == 2 || warp == 3) {
+        // ------------------------------------------------- scale loaders
+        // warp 2: this CTA's 128 A rows, warp 3: the tile's 224 B rows
+        // (padded to 256); each keeps its rows' words for one group of G
+        // k-blocks in registers with the next group's loads in flight.
+        const bool is_a = warp == 2;
         uint32_t it = 0;
         bool ok = true;
         const int ngrp = (p.nk + G - 1) / G;
         int tile = pair, grp = 0;
-        ScaleGroup cur, nxt;
-        KParams q = p;    // A rows offset to this CTA's half of the pair tile
-        auto load = [&](ScaleGroup &g, int t, int gr) {
+        WScaleRows cur, nxt;
+        auto load = [&](WScaleRows &g, int t, int gr) {
             int mb, nb;
             tile_coords(t, p.num_mb, p.num_nb, mb, nb);
+            if (is_a) {
 #pragma unroll
-            for (int a = 0; a < 4; ++a) {
-                const int64_t m = static_cast<int64_t>(mb) * PR_BM + rank * 128 + 32 * a + lane;
-                load_row_scales<G>(q.sa, q.ld_sa, q.gran_a, m, gr, q.nk, true, g.a[a]);
-            }
+                for (int a = 0; a < 4; ++a) {
+                    const int64_t m = static_cast<int64_t>(mb) * PR_BM + rank * 128 + 32 * a + lane;
+                    load_row_scales<G>(p.sa, p.ld_sa, p.gran_a, m, gr, p.nk, true, g.w[a]);
+                }
+            } else {
 #pragma unroll
-            for (int h = 0; h < 8; ++h) {
-                const int64_t n = static_cast<int64_t>(nb) * PR_BN + 32 * h + lane;
-                load_row_scales<G>(q.sb, q.ld_sb, q.gran_b, n, gr, q.nk, n < q.N, g.b[h]);
+                for (int h = 0; h < 8; ++h) {
+                    const int64_t n = static_cast<int64_t>(nb) * PR_BN + 32 * h + lane;
+                    load_row_scales<G>(p.sb, p.ld_sb, p.gran_b, n, gr, p.nk, h < 7 && n < p.N, g.w[h]);
+                }
             }
         };
         if (tile < p.num_tiles) load(cur, tile, 0);
@@ -1388,24 +1430,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (ntile < p.num_tiles) load(nxt, ntile, ngrp_next);
 #pragma unroll
             for (int t = 0; t < G; ++t) {
-                if (G * grp + t >= p.nk || !ok) break;
+                const int kb = G * grp + t;
+                if (kb >= p.nk || !ok) break;
+                if (kb % kScaleGroupKb<G>() != 0) continue;
                 constexpr int kWordStep = G / 4;
                 const int wi = t / kWordStep;
-                const uint32_t s = it % PR_STAGES, ph = (it / PR_STAGES) & 1u;
-                ok = wait_phase_pair(empty + 8 * s, ph ^ 1u, limit, abort_flag, p.err, WHO_SCALES);
+                const uint32_t sl = it % PR_NSF, sph = (it / PR_NSF) & 1u;
+                ok = wait_phase(sf_empty + 8 * sl, sph ^ 1u, limit, abort_flag, p.err, WHO_SCALES);
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) break;
-                const uint32_t dA = sSFA + s * PR_SFA_TILE + lane * 16;
-                const uint32_t dB = sSFB + s * PR_SFB_TILE + lane * 16;
-                st_shared_v4(dA, cur.a[0][wi], cur.a[1][wi], cur.a[2][wi], cur.a[3][wi]);
-                st_shared_v4(dB, cur.b[0][wi], cur.b[1][wi], cur.b[2][wi], cur.b[3][wi]);
-                st_shared_v4(dB + 512, cur.b[4][wi], cur.b[5][wi], cur.b[6][wi], cur.b[7][wi]);
-                // every lane's words visible to the tensor core's copy, then
-                // one cluster-scope arrival for the warp
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0 && !(p.inject == 1 && it == 0 && leader))
-                    ptx::mbar_arrive_cluster(sf_l + 8 * s);
+                if (is_a) {
+                    st_shared_v4(sSFA + sl * PR_SFA_TILE + lane * 16, cur.w[0][wi], cur.w[1][wi],
+                                 cur.w[2][wi], cur.w[3][wi]);
+                } else {
+                    const uint32_t d = sSFB + sl * PR_SFB_TILE + lane * 16;
+                    st_shared_v4(d, cur.w[0][wi], cur.w[1][wi], cur.w[2][wi], cur.w[3][wi]);
+                    st_shared_v4(d + 512, cur.w[4][wi], cur.w[5][wi], cur.w[6][wi], cur.w[7][wi]);
+                }
+                if (!(p.inject == 1 && it == 0 && leader && is_a)) {
+                    ptx::fence_proxy_async_smem();
+                    ptx::mbar_arrive(sf_local + 8 * sl);
+                }
                 ++it;
             }
             cur = nxt;
@@ -1420,64 +1465,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int tile = pair; tile < p.num_tiles; tile += npairs) {
             int mb, nb;
             tile_coords(tile, p.num_mb, p.num_nb, mb, nb);
-            bool ok = wait_phase_pair(tfull, tcount & 1u, limit, abort_flag, p.err, WHO_EPILOGUE);
+            const uint32_t b = tcount & 1u;
+            bool ok = wait_phase(tfull + 8 * b, (tcount >> 1) & 1u, limit, abort_flag, p.err,
+                                 WHO_EPILOGUE);
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) break;
             ptx::tc_fence_after();
             const int64_t row0 = static_cast<int64_t>(mb) * PR_BM + rank * 128 + qw * 32;
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(qw * 32) << 16) + ACC_COL;
-            if (!p.out_fp32 && !p.accumulate) {
-                uint32_t packed[PR_BN / 2];
-#pragma unroll
-                for (int chunk = 0; chunk < PR_BN / 32; chunk += 2) {
-                    uint32_t r[32], r2[32];
-                    ptx::tmem_ld_32x32b_x32(taddr + chunk * 32, r);
-                    ptx::tmem_ld_32x32b_x32(taddr + chunk * 32 + 32, r2);
-                    ptx::tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        packed[chunk * 16 + e] =
-                            ptx::cvt_bf16x2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
-                        packed[chunk * 16 + 16 + e] =
-                            ptx::cvt_bf16x2(__uint_as_float(r2[2 * e]), __uint_as_float(r2[2 * e + 1]));
-                    }
-                }
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive_cluster(tempty_l);
-#pragma unroll
-                for (int pc = 0; pc < PR_BN / 64; ++pc) {
-                    const int64_t n0 = static_cast<int64_t>(nb) * PR_BN + pc * 64;
-                    if (n0 >= p.N) continue;
-                    uint4 v[8];
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        v[c] = make_uint4(packed[pc * 32 + 4 * c], packed[pc * 32 + 4 * c + 1],
-                                          packed[pc * 32 + 4 * c + 2], packed[pc * 32 + 4 * c + 3]);
-                    store_piece(stage, v, lane,
-                                reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.c) + row0 * p.ldc + n0),
-                                p.ldc * 2);
-                }
-                ++tcount;
-                continue;
-            }
-            // FP32 out, or accumulation into C: 64 columns at a time
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(qw * 32) << 16) + b * PR_BN;
+            if (p.out_fp32 || p.accumulate) {
+                // FP32 out, or accumulation into C: 32 columns at a time; the
+                // accumulator buffer is released after its last columns are read
 #pragma unroll 1
-            for (int pc = 0; pc < PR_BN / 64; ++pc) {
-                uint32_t r0[32], r1[32];
-                ptx::tmem_ld_32x32b_x32(taddr + pc * 64, r0);
-                ptx::tmem_ld_32x32b_x32(taddr + pc * 64 + 32, r1);
-                ptx::tmem_wait_ld();
-                if (pc == PR_BN / 64 - 1) {
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive_cluster(tempty_l);
-                }
-                const int64_t n0 = static_cast<int64_t>(nb) * PR_BN + pc * 64;
-                if (n0 >= p.N) continue;
-                if (p.out_fp32) {
-                    auto piece = [&](const uint32_t(&rr)[32], int64_t col) {
-                        uint8_t *g = reinterpret_cast<uint8_t *>(static_cast<float *>(p.c) + row0 * p.ldc + col);
+                for (int chunk = 0; chunk < PR_BN / 32; ++chunk) {
+                    uint32_t rr[32];
+                    ptx::tmem_ld_32x32b_x32(taddr + chunk * 32, rr);
+                    ptx::tmem_wait_ld();
+                    if (chunk == PR_BN / 32 - 1) {
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive_cluster(tempty_l + 8 * b);
+                    }
+                    const int64_t n0 = static_cast<int64_t>(nb) * PR_BN + chunk * 32;
+                    if (n0 >= p.N) continue;
+                    if (p.out_fp32) {
+                        uint8_t *g = reinterpret_cast<uint8_t *>(static_cast<float *>(p.c) + row0 * p.ldc + n0);
                         uint4 v[8];
                         if (p.accumulate) {
                             load_piece(stage, v, lane, g, p.ldc * 4);
@@ -1493,26 +1505,67 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 v[c] = make_uint4(rr[4 * c], rr[4 * c + 1], rr[4 * c + 2], rr[4 * c + 3]);
                         }
                         store_piece(stage, v, lane, g, p.ldc * 4);
-                    };
-                    piece(r0, n0);
-                    piece(r1, n0 + 32);
-                } else {
-                    uint8_t *g = reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.c) + row0 * p.ldc + n0);
-                    uint4 v[8];
-                    load_piece(stage, v, lane, g, p.ldc * 2);
-                    auto add8 = [](const uint32_t *f32, const uint4 &old) {
-                        return make_uint4(
-                            ptx::cvt_bf16x2(__uint_as_float(f32[0]) + bf16_lo(old.x), __uint_as_float(f32[1]) + bf16_hi(old.x)),
-                            ptx::cvt_bf16x2(__uint_as_float(f32[2]) + bf16_lo(old.y), __uint_as_float(f32[3]) + bf16_hi(old.y)),
-                            ptx::cvt_bf16x2(__uint_as_float(f32[4]) + bf16_lo(old.z), __uint_as_float(f32[5]) + bf16_hi(old.z)),
-                            ptx::cvt_bf16x2(__uint_as_float(f32[6]) + bf16_lo(old.w), __uint_as_float(f32[7]) + bf16_hi(old.w)));
-                    };
+                    } else {
+                        // BF16 with accumulation: add in FP32, round once
+                        uint8_t *g = reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.c) + row0 * p.ldc + n0);
+                        uint4 v[4];
+                        load_piece64(stage, v, lane, g, p.ldc * 2);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        v[c] = add8(r0 + 8 * c, v[c]);
-                        v[c + 4] = add8(r1 + 8 * c, v[c + 4]);
+                        for (int c = 0; c < 4; ++c) {
+                            v[c] = make_uint4(
+                                ptx::cvt_bf16x2(__uint_as_float(rr[8 * c]) + bf16_lo(v[c].x),
+                                                __uint_as_float(rr[8 * c + 1]) + bf16_hi(v[c].x)),
+                                ptx::cvt_bf16x2(__uint_as_float(rr[8 * c + 2]) + bf16_lo(v[c].y),
+                                                __uint_as_float(rr[8 * c + 3]) + bf16_hi(v[c].y)),
+                                ptx::cvt_bf16x2(__uint_as_float(rr[8 * c + 4]) + bf16_lo(v[c].z),
+                                                __uint_as_float(rr[8 * c + 5]) + bf16_hi(v[c].z)),
+                                ptx::cvt_bf16x2(__uint_as_float(rr[8 * c + 6]) + bf16_lo(v[c].w),
+                                                __uint_as_float(rr[8 * c + 7]) + bf16_hi(v[c].w)));
+                        }
+                        store_piece64(stage, v, lane, g, p.ldc * 2);
                     }
+                }
+                ++tcount;
+                continue;
+            }
+            // BF16 out: 64 columns at a time (three pieces, then the last 32);
+            // N is a multiple of 128 and the tile starts at a multiple of 224,
+            // so a piece can straddle N by exactly 32 columns: it is then
+            // written as a half piece.  With two accumulator buffers the MMAs
+            // of the next tile do not wait for this one, so the buffer is
+            // released after its last columns are read.
+#pragma unroll 1
+            for (int pc = 0; pc < 4; ++pc) {
+                uint32_t r0[32], r1[32];
+                ptx::tmem_ld_32x32b_x32(taddr + pc * 64, r0);
+                if (pc < 3) ptx::tmem_ld_32x32b_x32(taddr + pc * 64 + 32, r1);
+                ptx::tmem_wait_ld();
+                if (pc == 3) {
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive_cluster(tempty_l + 8 * b);
+                }
+                const int64_t n0 = static_cast<int64_t>(nb) * PR_BN + pc * 64;
+                if (n0 >= p.N) continue;
+                uint8_t *g = reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.c) + row0 * p.ldc + n0);
+                uint4 v[8];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    v[c] = make_uint4(ptx::cvt_bf16x2(__uint_as_float(r0[8 * c]), __uint_as_float(r0[8 * c + 1])),
+                                      ptx::cvt_bf16x2(__uint_as_float(r0[8 * c + 2]), __uint_as_float(r0[8 * c + 3])),
+                                      ptx::cvt_bf16x2(__uint_as_float(r0[8 * c + 4]), __uint_as_float(r0[8 * c + 5])),
+                                      ptx::cvt_bf16x2(__uint_as_float(r0[8 * c + 6]), __uint_as_float(r0[8 * c + 7])));
+                if (pc < 3 && n0 + 64 <= p.N) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        v[4 + c] = make_uint4(ptx::cvt_bf16x2(__uint_as_float(r1[8 * c]), __uint_as_float(r1[8 * c + 1])),
+                                              ptx::cvt_bf16x2(__uint_as_float(r1[8 * c + 2]), __uint_as_float(r1[8 * c + 3])),
+                                              ptx::cvt_bf16x2(__uint_as_float(r1[8 * c + 4]), __uint_as_float(r1[8 * c + 5])),
+                                              ptx::cvt_bf16x2(__uint_as_float(r1[8 * c + 6]), __uint_as_float(r1[8 * c + 7])));
                     store_piece(stage, v, lane, g, p.ldc * 2);
+                } else {
+                    const uint4(&h)[4] = *reinterpret_cast<const uint4(*)[4]>(&v[0]);
+                    store_piece64(stage, h, lane, g, p.ldc * 2);
                 }
             }
             ++tcount;
@@ -1681,7 +1734,7 @@ int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
     std::memset(&ta, 0, sizeof(ta));
     std::memset(&tb, 0, sizeof(tb));
     if (!make_tmap(&ta, g.a_codes, g.M, g.K, g.lda, paired ? 128 : (wide ? WBM : BM))) return 1;
-    if (!make_tmap(&tb, g.b_codes, g.N, g.K, g.ldb, paired ? 128 : (wide ? WBN : BN))) return 1;
+    if (!make_tmap(&tb, g.b_codes, g.N, g.K, g.ldb, paired ? PR_BN / 2 : (wide ? WBN : BN))) return 1;
 
     KParams p;
     p.M = static_cast<int>(g.M);
@@ -1730,7 +1783,7 @@ int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
         if (pairs > p.num_tiles) pairs = p.num_tiles;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
-        cfg.blockDim = dim3(NUM_THREADS);
+        cfg.blockDim = dim3(PR_THREADS);
         cfg.dynamicSmemBytes = PR_SMEM_BYTES;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
