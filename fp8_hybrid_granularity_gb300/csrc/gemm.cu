@@ -1148,53 +1148,57 @@ __global__ void __launch_bounds__(W_THREADS, 1)
 }
 
 // ---------------------------------------------------------- CTA-pair variant
-// Tile 256 x 224 computed by a pair of CTAs (a cluster of two) with
-// tcgen05.mma.cta_group::2: each CTA holds its 128 rows of A and its half
-// (112 rows) of B in its own shared memory, the MMA issued by the even CTA
-// reads both, and each CTA's tensor memory receives its 128 rows of the
-// accumulator.  A stage is then 30 KB per CTA for 128 x 224 x 128 MACs per
-// SM, so six stages fit (five in flight while one is consumed, against two
-// 60 KB stages in the 256 x 224 single-CTA kernel), and the accumulator's
-// 224 columns fit twice in tensor memory: the epilogue drains one tile while
-// the MMAs of the next run into the other buffer.
-//   Both CTAs: warp 0 TMA producer (its own A and B halves; completion counted
-//   on the even CTA's stage barrier), warps 2 and 3 scale loaders (this CTA's
-//   128 A rows; all 224 B rows), writing one buffer of an eight-deep ring per
-//   scale group (four k-blocks for 1x128 / 128x128 scales, one for MX) and
-//   arriving on their own CTA's barrier, warps 4-7 epilogue of its 128 rows.
-//   Even CTA: warp 1 copies each scale group into tensor memory and issues the
-//   MMAs for the pair, committing to both CTAs' barriers.  Odd CTA: warp 1
-//   forwards each filled scale buffer to the even CTA (one cluster-scope
-//   release arrival from a warp with no loads in flight, so the arrival does
-//   not wait for the scale warps' look-ahead loads).
+// Tile 256 x 448 computed by a pair of CTAs (a cluster of two) with
+// tcgen05.mma.cta_group::2: per 32-K step two M = 256, N = 224 MMAs, one per
+// half of the tile's columns.  Each CTA holds its 128 rows of A and, of each
+// column half, its 112 rows of B in its own shared memory; the MMAs issued by
+// the even CTA read both CTAs' operands, and each CTA's tensor memory
+// receives its 128 rows of the 256 x 448 accumulator (two 224-column
+// accumulators).  A stage is then 44 KB per CTA for 128 x 448 x 128 MACs per
+// SM (the single-CTA 256 x 224 kernel needs 60 KB for the same work): four
+// stages fit, three in flight while one is consumed, and each SM reads 27 %
+// fewer operand bytes per MAC from L2.
+//   Both CTAs: warp 0 TMA producer (its A rows and B rows; completion counted
+//   on the even CTA's stage barrier), warps 2 and 3 scale loaders (warp 2:
+//   this CTA's 128 A rows and the first column half's 224 B rows; warp 3: the
+//   second half's), writing one buffer of a four-deep ring per scale group
+//   (four k-blocks for 1x128 / 128x128 scales, one for MX), warps 4-11
+//   epilogue (two per tensor-memory lane quarter, one per accumulator).
+//   Even CTA: warp 1 copies each scale group into tensor memory and issues
+//   the MMAs for the pair, committing to both CTAs' barriers.  Odd CTA: warp
+//   1 forwards each filled scale buffer to the even CTA (one cluster-scope
+//   release arrival from a warp with no loads in flight).
+//   The MMA issuer and the producer run on one lane: an MMA, a commit or a
+//   completed barrier wait each take tens of cycles to issue, and a 32-K
+//   step of this tile lasts 224 cycles.
 //   Tensor memory (both CTAs): accumulators at columns 0 and 224, then three
-//   slots of 4 columns of A scales and 8 of B scales.
-constexpr int PR_BM = 256, PR_BN = 224, PR_STAGES = 6, PR_NSF = 8;
-constexpr int PR_THREADS = 256;
-constexpr uint32_t PR_A_TILE = 128 * BK;            // per CTA
-constexpr uint32_t PR_B_TILE = (PR_BN / 2) * BK;    // per CTA (its half of B)
-constexpr uint32_t PR_SFA_TILE = 512, PR_SFB_TILE = 1024;
-constexpr uint32_t PR_SFA_COL = 2 * PR_BN;          // + 4 * slot
-constexpr uint32_t PR_SFB_COL = 2 * PR_BN + 12;     // + 8 * slot
-constexpr uint32_t PR_OFF_A = 0;
-constexpr uint32_t PR_OFF_B = PR_OFF_A + PR_STAGES * PR_A_TILE;
-constexpr uint32_t PR_OFF_SFA = PR_OFF_B + PR_STAGES * PR_B_TILE;
+//   slots of 4 columns of A scales and 16 of B scales (8 per column half).
+constexpr int PR_BM = 256, PR_BN = 448, PR_HN = 224, PR_STAGES = 4, PR_NSF = 4;
+constexpr int PR_THREADS = 384;
+constexpr uint32_t PR_A_TILE = 128 * BK;                 // per CTA
+constexpr uint32_t PR_BH_TILE = (PR_HN / 2) * BK;        // per CTA and column half
+constexpr uint32_t PR_STAGE = PR_A_TILE + 2 * PR_BH_TILE;
+constexpr uint32_t PR_SFA_TILE = 512, PR_SFB_TILE = 2048;
+constexpr uint32_t PR_SFA_COL = PR_BN;                   // + 4 * slot
+constexpr uint32_t PR_SFB_COL = PR_BN + 12;              // + 16 * slot
+constexpr uint32_t PR_OFF_SFA = PR_STAGES * PR_STAGE;
 constexpr uint32_t PR_OFF_SFB = PR_OFF_SFA + PR_NSF * PR_SFA_TILE;
 constexpr uint32_t PR_OFF_BAR = PR_OFF_SFB + PR_NSF * PR_SFB_TILE;
-// barriers from PR_OFF_BAR (8 bytes each): full[6] at 0 (operand bytes of both
-// CTAs; even CTA), empty[6] at 48 (each CTA), sf_local[8] at 96 (this CTA's
-// scale words written; 64 arrivals), sf_peer[8] at 160 (the odd CTA's words
-// written, forwarded; even CTA), sf_empty[8] at 224 (the pair's copy of the
-// buffer done; each CTA), tfull[2] at 288 (each CTA), tempty[2] at 304 (one
-// arrival per epilogue warp of both CTAs; even CTA), drain 320.
-constexpr uint32_t PR_BAR_EMPTY = 48, PR_BAR_SFL = 96, PR_BAR_SFP = 160, PR_BAR_SFE = 224,
-                   PR_BAR_TFULL = 288, PR_BAR_TEMPTY = 304, PR_BAR_DRAIN = 320;
-constexpr uint32_t PR_OFF_TMEM_SLOT = PR_OFF_BAR + 336;
-constexpr uint32_t PR_OFF_ABORT = PR_OFF_BAR + 340;
-constexpr uint32_t PR_OFF_EPI = PR_OFF_BAR + 384;
-constexpr uint32_t PR_SMEM_BYTES = PR_OFF_EPI + 4 * EPI_WARP_BYTES + 1024;
-static_assert(PR_B_TILE % 1024 == 0, "B stage must keep the 128-byte swizzle's 1 KB alignment");
-static_assert(PR_SFB_COL + 8 * 3 <= TMEM_COLS, "tensor memory overflow");
+// barriers from PR_OFF_BAR (8 bytes each): full[4] at 0 (operand bytes of both
+// CTAs; even CTA), empty[4] at 32 (each CTA), sf_full[4] at 64 (scale words
+// written: this CTA's 64 scale-warp lanes, plus on the even CTA the odd CTA's
+// forwarder), sf_empty[4] at 96 (the pair's copy of the buffer done; each
+// CTA), tfull 128 (each CTA), tempty 136 (one arrival per epilogue warp of
+// both CTAs; even CTA), drain 144.
+constexpr uint32_t PR_BAR_EMPTY = 32, PR_BAR_SFF = 64, PR_BAR_SFE = 96, PR_BAR_TFULL = 128,
+                   PR_BAR_TEMPTY = 136, PR_BAR_DRAIN = 144;
+constexpr uint32_t PR_OFF_TMEM_SLOT = PR_OFF_BAR + 160;
+constexpr uint32_t PR_OFF_ABORT = PR_OFF_BAR + 164;
+constexpr uint32_t PR_OFF_EPI = PR_OFF_BAR + 256;
+constexpr uint32_t PR_SMEM_BYTES = PR_OFF_EPI + 8 * EPI_WARP_BYTES + 1024;
+static_assert(PR_A_TILE % 1024 == 0 && PR_BH_TILE % 1024 == 0,
+              "operand tiles must keep the 128-byte swizzle's 1 KB alignment");
+static_assert(PR_SFB_COL + 16 * 3 <= TMEM_COLS, "tensor memory overflow");
 static_assert(PR_SMEM_BYTES <= 232448, "shared memory overflow");
 
 // Wait on a barrier of this CTA whose arrivals may come from the other CTA of
@@ -1221,7 +1225,12 @@ __device__ bool wait_phase_pair(uint32_t bar, uint32_t parity, uint64_t limit,
     }
 }
 
-// Pair tile t -> (m-block of 256 rows, n-block of 224 columns); the same
+// One lane's scale words for one group of G k-blocks: up to 12 rows.
+struct PairScaleRows {
+    uint32_t w[12][4];
+};
+
+// Pair tile t -> (m-block of 256 rows, n-block of 448 columns); the same
 // grouped order as the other kernels.
 template <int G>
 __global__ void __launch_bounds__(PR_THREADS, 1)
@@ -1231,10 +1240,9 @@ __global__ void __launch_bounds__(PR_THREADS, 1)
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
-    const uint32_t sA = base + PR_OFF_A, sB = base + PR_OFF_B;
     const uint32_t sSFA = base + PR_OFF_SFA, sSFB = base + PR_OFF_SFB, sBAR = base + PR_OFF_BAR;
-    const uint32_t empty = sBAR + PR_BAR_EMPTY, sf_local = sBAR + PR_BAR_SFL,
-                   sf_peer = sBAR + PR_BAR_SFP, sf_empty = sBAR + PR_BAR_SFE;
+    const uint32_t empty = sBAR + PR_BAR_EMPTY, sf_full = sBAR + PR_BAR_SFF,
+                   sf_empty = sBAR + PR_BAR_SFE;
     const uint32_t tfull = sBAR + PR_BAR_TFULL, tempty = sBAR + PR_BAR_TEMPTY,
                    drain = sBAR + PR_BAR_DRAIN;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + PR_OFF_TMEM_SLOT);
@@ -1247,7 +1255,7 @@ __global__ void __launch_bounds__(PR_THREADS, 1)
     const uint64_t drain_limit = 2000000ull;
     // the even CTA's barriers, as seen from either CTA
     const uint32_t full_l = ptx::map_shared_rank(sBAR, 0);
-    const uint32_t sf_peer_l = ptx::map_shared_rank(sf_peer, 0);
+    const uint32_t sf_full_l = ptx::map_shared_rank(sf_full, 0);
     const uint32_t tempty_l = ptx::map_shared_rank(tempty, 0);
 
     if (threadIdx.x == 0) {
@@ -1256,14 +1264,11 @@ __global__ void __launch_bounds__(PR_THREADS, 1)
             ptx::mbar_init(empty + 8 * s, 1);       // the pair's commit
         }
         for (int i = 0; i < PR_NSF; ++i) {
-            ptx::mbar_init(sf_local + 8 * i, 64);   // every lane of both scale warps
-            ptx::mbar_init(sf_peer + 8 * i, 1);     // the odd CTA's forwarder
+            ptx::mbar_init(sf_full + 8 * i, leader ? 65 : 64);
             ptx::mbar_init(sf_empty + 8 * i, 1);    // the pair's commit after the copy
         }
-        for (int b = 0; b < 2; ++b) {
-            ptx::mbar_init(tfull + 8 * b, 1);
-            ptx::mbar_init(tempty + 8 * b, 8);      // one arrival per epilogue warp of both CTAs
-        }
+        ptx::mbar_init(tfull, 1);
+        ptx::mbar_init(tempty, 16);                 // one arrival per epilogue warp of both CTAs
         ptx::mbar_init(drain, 1);
         *abort_flag = 0u;
         ptx::fence_mbar_init();
@@ -1281,153 +1286,159 @@ __global__ void __launch_bounds__(PR_THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
-        uint32_t it = 0;
-        bool ok = true;
-        for (int tile = pair; tile < p.num_tiles && ok; tile += npairs) {
-            int mb, nb;
-            tile_coords(tile, p.num_mb, p.num_nb, mb, nb);
-            for (int kb = 0; kb < p.nk; ++kb) {
-                const uint32_t s = it % PR_STAGES, ph = (it / PR_STAGES) & 1u;
-                ok = wait_phase(empty + 8 * s, ph ^ 1u, limit, abort_flag, p.err, WHO_PRODUCER);
-                ok = __all_sync(0xFFFFFFFFu, ok);
-                if (!ok) break;
-                if (lane == 0) {
-                    if (leader)
-                        ptx::mbar_arrive_expect_tx(sBAR + 8 * s, 2 * (PR_A_TILE + PR_B_TILE));
-                    ptx::tma_load_2d_pair(sA + s * PR_A_TILE, &tmap_a, full_l + 8 * s, kb * BK,
-                                          mb * PR_BM + static_cast<int>(rank) * 128);
-                    ptx::tma_load_2d_pair(sB + s * PR_B_TILE, &tmap_b, full_l + 8 * s, kb * BK,
-                                          nb * PR_BN + static_cast<int>(rank) * (PR_BN / 2));
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = pair; tile < p.num_tiles && ok; tile += npairs) {
+                int mb, nb;
+                tile_coords(tile, p.num_mb, p.num_nb, mb, nb);
+                const int arow = mb * PR_BM + static_cast<int>(rank) * 128;
+                const int brow = nb * PR_BN + static_cast<int>(rank) * (PR_HN / 2);
+                for (int kb = 0; kb < p.nk; ++kb) {
+                    const uint32_t s = it % PR_STAGES, ph = (it / PR_STAGES) & 1u;
+                    ok = wait_phase(empty + 8 * s, ph ^ 1u, limit, abort_flag, p.err, WHO_PRODUCER);
+                    if (!ok) break;
+                    const uint32_t st = base + s * PR_STAGE;
+                    if (leader) ptx::mbar_arrive_expect_tx(sBAR + 8 * s, 2 * PR_STAGE);
+                    ptx::tma_load_2d_pair(st, &tmap_a, full_l + 8 * s, kb * BK, arow);
+                    ptx::tma_load_2d_pair(st + PR_A_TILE, &tmap_b, full_l + 8 * s, kb * BK, brow);
+                    ptx::tma_load_2d_pair(st + PR_A_TILE + PR_BH_TILE, &tmap_b, full_l + 8 * s, kb * BK,
+                                          brow + PR_HN);
+                    ++it;
                 }
-                __syncwarp();
-                ++it;
+            }
+            // the even CTA waits until the last loads of both CTAs have landed;
+            // the cluster barrier below keeps the odd CTA resident until then
+            if (leader) {
+                const uint32_t nd = it < static_cast<uint32_t>(PR_STAGES) ? it : static_cast<uint32_t>(PR_STAGES);
+                for (uint32_t i = it - nd; i < it; ++i)
+                    wait_phase(sBAR + 8 * (i % PR_STAGES), (i / PR_STAGES) & 1u, drain_limit, abort_flag,
+                               p.err, WHO_PRODUCER, false);
+            }
+            // A CTA that stopped early cannot tell which of its last copies the
+            // even CTA's barriers have counted; it gives them the drain bound
+            // to land (copies take microseconds) before the pair may leave.
+            if (!ok || *abort_flag) {
+                const uint64_t t0 = ptx::globaltimer();
+                while (ptx::globaltimer() - t0 < drain_limit) {
+                }
             }
         }
-        // the even CTA waits until the last loads of both CTAs have landed; the
-        // cluster barrier below keeps the odd CTA resident until then
-        if (leader) {
-            const uint32_t nd = it < static_cast<uint32_t>(PR_STAGES) ? it : static_cast<uint32_t>(PR_STAGES);
-            for (uint32_t i = it - nd; i < it; ++i)
-                wait_phase(sBAR + 8 * (i % PR_STAGES), (i / PR_STAGES) & 1u, drain_limit,
-                           abort_flag, p.err, WHO_PRODUCER, false);
-        }
-        // A CTA that stopped early cannot tell which of its last copies the
-        // even CTA's barriers have counted; it gives them the drain bound to
-        // land (copies take microseconds) before the pair may leave.
-        if (!ok || *abort_flag) {
-            const uint64_t t0 = ptx::globaltimer();
-            while (ptx::globaltimer() - t0 < drain_limit) {
-            }
-        }
+        __syncwarp();
     } else if (warp == 1 && leader) {
         // ------------------------------------------- MMA issuer (even CTA)
         // Scale groups come through the ring in order (sfi); each is copied
         // into one of three tensor-memory slots when its first k-block comes
         // up, and its buffer is released by the copy's commit.
-        uint32_t it = 0, tcount = 0, sfi = 0, tslot = 0;
-        bool ok = true;
-        for (int tile = pair; tile < p.num_tiles && ok; tile += npairs) {
-            const uint32_t b = tcount & 1u, use = tcount >> 1;
-            ok = wait_phase_pair(tempty + 8 * b, (use & 1u) ^ 1u, limit, abort_flag, p.err, WHO_MMA);
-            ok = __all_sync(0xFFFFFFFFu, ok);
-            if (!ok) break;
-            ptx::tc_fence_after();
-            const uint32_t dacc = tmem + b * PR_BN;
-            for (int kb = 0; kb < p.nk; ++kb) {
-                const uint32_t s = it % PR_STAGES, ph = (it / PR_STAGES) & 1u;
-                const bool new_group = kb % kScaleGroupKb<G>() == 0;
-                const uint32_t sl = sfi % PR_NSF, sph = (sfi / PR_NSF) & 1u;
-                ok = wait_phase(sBAR + 8 * s, ph, limit, abort_flag, p.err, WHO_MMA) &&
-                     (!new_group ||
-                      (wait_phase(sf_local + 8 * sl, sph, limit, abort_flag, p.err, WHO_MMA) &&
-                       wait_phase_pair(sf_peer + 8 * sl, sph, limit, abort_flag, p.err, WHO_MMA)));
-                ok = __all_sync(0xFFFFFFFFu, ok);
+        if (lane == 0) {
+            uint32_t it = 0, tcount = 0, sfi = 0, tslot = 0;
+            bool ok = true;
+            for (int tile = pair; tile < p.num_tiles && ok; tile += npairs) {
+                ok = wait_phase_pair(tempty, (tcount & 1u) ^ 1u, limit, abort_flag, p.err, WHO_MMA);
                 if (!ok) break;
                 ptx::tc_fence_after();
-                if (new_group) tslot = sfi % 3;
-                if (lane == 0) {
-                    const uint32_t tsfa = tmem + PR_SFA_COL + 4 * tslot;
-                    const uint32_t tsfb = tmem + PR_SFB_COL + 8 * tslot;
+                for (int kb = 0; kb < p.nk; ++kb) {
+                    const uint32_t s = it % PR_STAGES, ph = (it / PR_STAGES) & 1u;
+                    const bool new_group = kb % kScaleGroupKb<G>() == 0;
+                    const uint32_t sl = sfi % PR_NSF, sph = (sfi / PR_NSF) & 1u;
+                    ok = wait_phase(sBAR + 8 * s, ph, limit, abort_flag, p.err, WHO_MMA) &&
+                         (!new_group ||
+                          wait_phase_pair(sf_full + 8 * sl, sph, limit, abort_flag, p.err, WHO_MMA));
+                    if (!ok) break;
+                    ptx::tc_fence_after();
                     if (new_group) {
+                        tslot = sfi % 3;
+                        const uint32_t tsfa = tmem + PR_SFA_COL + 4 * tslot;
+                        const uint32_t tsfb = tmem + PR_SFB_COL + 16 * tslot;
+                        const uint32_t bsf = sSFB + sl * PR_SFB_TILE;
                         ptx::tc_cp_32x128b_warpx4_pair(tsfa, desc_sf(sSFA + sl * PR_SFA_TILE));
-                        ptx::tc_cp_32x128b_warpx4_pair(tsfb, desc_sf(sSFB + sl * PR_SFB_TILE));
-                        ptx::tc_cp_32x128b_warpx4_pair(tsfb + 4, desc_sf(sSFB + sl * PR_SFB_TILE + 512));
+                        ptx::tc_cp_32x128b_warpx4_pair(tsfb, desc_sf(bsf));
+                        ptx::tc_cp_32x128b_warpx4_pair(tsfb + 4, desc_sf(bsf + 512));
+                        ptx::tc_cp_32x128b_warpx4_pair(tsfb + 8, desc_sf(bsf + 1024));
+                        ptx::tc_cp_32x128b_warpx4_pair(tsfb + 12, desc_sf(bsf + 1536));
                         ptx::tc_commit_pair(sf_empty + 8 * sl, 0x3);   // the buffer, both CTAs
+                        ++sfi;
                     }
-                    const uint64_t ad = desc_sw128(sA + s * PR_A_TILE);
-                    const uint64_t bd = desc_sw128(sB + s * PR_B_TILE);
+                    const uint32_t tsfa = tmem + PR_SFA_COL + 4 * tslot;
+                    const uint32_t tsfb = tmem + PR_SFB_COL + 16 * tslot;
+                    const uint32_t st = base + s * PR_STAGE;
+                    const uint64_t ad = desc_sw128(st);
+                    const uint64_t bd0 = desc_sw128(st + PR_A_TILE);
+                    const uint64_t bd1 = desc_sw128(st + PR_A_TILE + PR_BH_TILE);
 #pragma unroll
                     for (int j = 0; j < BK / 32; ++j) {
                         const uint32_t idesc = p.idesc | (sf_id(p.gran_a, kb, j) << 29) |
                                                (sf_id(p.gran_b, kb, j) << 4);
-                        ptx::tc_mma_mxf8_pair(dacc, ad + 2 * j, bd + 2 * j, idesc, tsfa, tsfb,
-                                              (kb | j) != 0 ? 1u : 0u);
+                        const uint32_t acc = (kb | j) != 0 ? 1u : 0u;
+                        ptx::tc_mma_mxf8_pair(tmem, ad + 2 * j, bd0 + 2 * j, idesc, tsfa, tsfb, acc);
+                        ptx::tc_mma_mxf8_pair(tmem + PR_HN, ad + 2 * j, bd1 + 2 * j, idesc, tsfa, tsfb + 8,
+                                              acc);
                     }
                     ptx::tc_commit_pair(empty + 8 * s, 0x3);   // frees the stage in both CTAs
+                    ++it;
                 }
-                __syncwarp();
-                if (new_group) ++sfi;
-                ++it;
+                if (!ok) break;
+                ptx::tc_commit_pair(tfull, 0x3);
+                ++tcount;
             }
-            if (!ok) break;
-            if (lane == 0) ptx::tc_commit_pair(tfull + 8 * b, 0x3);
-            __syncwarp();
-            ++tcount;
+            ptx::tc_commit_pair(drain, 0x1);
+            wait_phase(drain, 0u, drain_limit, abort_flag, p.err, WHO_MMA, false);
         }
-        if (lane == 0) ptx::tc_commit_pair(drain, 0x1);
         __syncwarp();
-        wait_phase(drain, 0u, drain_limit, abort_flag, p.err, WHO_MMA, false);
     } else if (warp == 1) {
         // ------------------------------------ scale-buffer forwarder (odd CTA)
-        uint32_t sfi = 0;
-        bool ok = true;
-        for (int tile = pair; tile < p.num_tiles && ok; tile += npairs) {
-            for (int kb = 0; kb < p.nk; kb += kScaleGroupKb<G>()) {
-                const uint32_t sl = sfi % PR_NSF, sph = (sfi / PR_NSF) & 1u;
-                ok = wait_phase(sf_local + 8 * sl, sph, limit, abort_flag, p.err, WHO_SCALES);
-                ok = __all_sync(0xFFFFFFFFu, ok);
-                if (!ok) break;
-                if (lane == 0) ptx::mbar_arrive_cluster(sf_peer_l + 8 * sl);
-                __syncwarp();
-                ++sfi;
+        if (lane == 0) {
+            uint32_t sfi = 0;
+            bool ok = true;
+            for (int tile = pair; tile < p.num_tiles && ok; tile += npairs) {
+                for (int kb = 0; kb < p.nk; kb += kScaleGroupKb<G>()) {
+                    const uint32_t sl = sfi % PR_NSF, sph = (sfi / PR_NSF) & 1u;
+                    ok = wait_phase(sf_full + 8 * sl, sph, limit, abort_flag, p.err, WHO_SCALES);
+                    if (!ok) break;
+                    ptx::mbar_arrive_cluster(sf_full_l + 8 * sl);
+                    ++sfi;
+                }
             }
         }
+        __syncwarp();
     } else if (warp == 2 || warp == 3) {
         // ------------------------------------------------- scale loaders
-        // warp 2: this CTA's 128 A rows, warp 3: the tile's 224 B rows
-        // (padded to 256); each keeps its rows' words for one group of G
-        // k-blocks in registers with the next group's loads in flight.
-        const bool is_a = warp == 2;
+        // warp 2: this CTA's 128 A rows (words 0-3) and the first column
+        // half's 224 B rows, padded to 256 (words 4-11); warp 3: the second
+        // half's B rows (words 0-7).  Each loads its rows' words for one group
+        // of G k-blocks (four ring buffers) after writing the previous
+        // group's; the ring covers the loads' latency.
+        const bool w2 = warp == 2;
         uint32_t it = 0;
         bool ok = true;
         const int ngrp = (p.nk + G - 1) / G;
         int tile = pair, grp = 0;
-        WScaleRows cur, nxt;
-        auto load = [&](WScaleRows &g, int t, int gr) {
+        PairScaleRows cur;
+        auto load = [&](PairScaleRows &g, int t, int gr) {
             int mb, nb;
             tile_coords(t, p.num_mb, p.num_nb, mb, nb);
-            if (is_a) {
+            const int64_t nbase = static_cast<int64_t>(nb) * PR_BN;
+            if (w2) {
 #pragma unroll
                 for (int a = 0; a < 4; ++a) {
                     const int64_t m = static_cast<int64_t>(mb) * PR_BM + rank * 128 + 32 * a + lane;
                     load_row_scales<G>(p.sa, p.ld_sa, p.gran_a, m, gr, p.nk, true, g.w[a]);
                 }
+#pragma unroll
+                for (int h = 0; h < 8; ++h) {
+                    const int64_t n = nbase + 32 * h + lane;
+                    load_row_scales<G>(p.sb, p.ld_sb, p.gran_b, n, gr, p.nk, h < 7 && n < p.N, g.w[4 + h]);
+                }
             } else {
 #pragma unroll
                 for (int h = 0; h < 8; ++h) {
-                    const int64_t n = static_cast<int64_t>(nb) * PR_BN + 32 * h + lane;
+                    const int64_t n = nbase + PR_HN + 32 * h + lane;
                     load_row_scales<G>(p.sb, p.ld_sb, p.gran_b, n, gr, p.nk, h < 7 && n < p.N, g.w[h]);
                 }
             }
         };
-        if (tile < p.num_tiles) load(cur, tile, 0);
         while (tile < p.num_tiles && ok) {
-            int ntile = tile, ngrp_next = grp + 1;
-            if (ngrp_next == ngrp) {
-                ntile += npairs;
-                ngrp_next = 0;
-            }
-            if (ntile < p.num_tiles) load(nxt, ntile, ngrp_next);
+            load(cur, tile, grp);
 #pragma unroll
             for (int t = 0; t < G; ++t) {
                 const int kb = G * grp + t;
@@ -1439,54 +1450,56 @@ __global__ void __launch_bounds__(PR_THREADS, 1)
                 ok = wait_phase(sf_empty + 8 * sl, sph ^ 1u, limit, abort_flag, p.err, WHO_SCALES);
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) break;
-                if (is_a) {
+                const uint32_t dB = sSFB + sl * PR_SFB_TILE + lane * 16;
+                if (w2) {
                     st_shared_v4(sSFA + sl * PR_SFA_TILE + lane * 16, cur.w[0][wi], cur.w[1][wi],
                                  cur.w[2][wi], cur.w[3][wi]);
+                    st_shared_v4(dB, cur.w[4][wi], cur.w[5][wi], cur.w[6][wi], cur.w[7][wi]);
+                    st_shared_v4(dB + 512, cur.w[8][wi], cur.w[9][wi], cur.w[10][wi], cur.w[11][wi]);
                 } else {
-                    const uint32_t d = sSFB + sl * PR_SFB_TILE + lane * 16;
-                    st_shared_v4(d, cur.w[0][wi], cur.w[1][wi], cur.w[2][wi], cur.w[3][wi]);
-                    st_shared_v4(d + 512, cur.w[4][wi], cur.w[5][wi], cur.w[6][wi], cur.w[7][wi]);
+                    st_shared_v4(dB + 1024, cur.w[0][wi], cur.w[1][wi], cur.w[2][wi], cur.w[3][wi]);
+                    st_shared_v4(dB + 1536, cur.w[4][wi], cur.w[5][wi], cur.w[6][wi], cur.w[7][wi]);
                 }
-                if (!(p.inject == 1 && it == 0 && leader && is_a)) {
+                if (!(p.inject == 1 && it == 0 && leader && w2)) {
                     ptx::fence_proxy_async_smem();
-                    ptx::mbar_arrive(sf_local + 8 * sl);
+                    ptx::mbar_arrive(sf_full + 8 * sl);
                 }
                 ++it;
             }
-            cur = nxt;
-            tile = ntile;
-            grp = ngrp_next;
+            if (++grp == ngrp) {
+                grp = 0;
+                tile += npairs;
+            }
         }
     } else if (warp >= 4) {
         // --------------------------------------------------------- epilogue
-        const int qw = warp & 3;
-        uint8_t *stage = gbase + PR_OFF_EPI + qw * EPI_WARP_BYTES;
+        const int q = warp & 3, half = (warp - 4) >> 2, ew = warp - 4;
+        uint8_t *stage = gbase + PR_OFF_EPI + ew * EPI_WARP_BYTES;
         uint32_t tcount = 0;
         for (int tile = pair; tile < p.num_tiles; tile += npairs) {
             int mb, nb;
             tile_coords(tile, p.num_mb, p.num_nb, mb, nb);
-            const uint32_t b = tcount & 1u;
-            bool ok = wait_phase(tfull + 8 * b, (tcount >> 1) & 1u, limit, abort_flag, p.err,
-                                 WHO_EPILOGUE);
+            bool ok = wait_phase(tfull, tcount & 1u, limit, abort_flag, p.err, WHO_EPILOGUE);
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) break;
             ptx::tc_fence_after();
-            const int64_t row0 = static_cast<int64_t>(mb) * PR_BM + rank * 128 + qw * 32;
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(qw * 32) << 16) + b * PR_BN;
+            const int64_t row0 = static_cast<int64_t>(mb) * PR_BM + rank * 128 + q * 32;
+            const int64_t col0 = static_cast<int64_t>(nb) * PR_BN + half * PR_HN;
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + half * PR_HN;
             if (p.out_fp32 || p.accumulate) {
                 // FP32 out, or accumulation into C: 32 columns at a time; the
-                // accumulator buffer is released after its last columns are read
+                // accumulator is released after its last columns are read
 #pragma unroll 1
-                for (int chunk = 0; chunk < PR_BN / 32; ++chunk) {
+                for (int chunk = 0; chunk < PR_HN / 32; ++chunk) {
                     uint32_t rr[32];
                     ptx::tmem_ld_32x32b_x32(taddr + chunk * 32, rr);
                     ptx::tmem_wait_ld();
-                    if (chunk == PR_BN / 32 - 1) {
+                    if (chunk == PR_HN / 32 - 1) {
                         ptx::tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) ptx::mbar_arrive_cluster(tempty_l + 8 * b);
+                        if (lane == 0) ptx::mbar_arrive_cluster(tempty_l);
                     }
-                    const int64_t n0 = static_cast<int64_t>(nb) * PR_BN + chunk * 32;
+                    const int64_t n0 = col0 + chunk * 32;
                     if (n0 >= p.N) continue;
                     if (p.out_fp32) {
                         uint8_t *g = reinterpret_cast<uint8_t *>(static_cast<float *>(p.c) + row0 * p.ldc + n0);
@@ -1528,44 +1541,57 @@ __global__ void __launch_bounds__(PR_THREADS, 1)
                 ++tcount;
                 continue;
             }
-            // BF16 out: 64 columns at a time (three pieces, then the last 32);
-            // N is a multiple of 128 and the tile starts at a multiple of 224,
-            // so a piece can straddle N by exactly 32 columns: it is then
-            // written as a half piece.  With two accumulator buffers the MMAs
-            // of the next tile do not wait for this one, so the buffer is
-            // released after its last columns are read.
-#pragma unroll 1
-            for (int pc = 0; pc < 4; ++pc) {
-                uint32_t r0[32], r1[32];
-                ptx::tmem_ld_32x32b_x32(taddr + pc * 64, r0);
-                if (pc < 3) ptx::tmem_ld_32x32b_x32(taddr + pc * 64 + 32, r1);
+            // BF16 out: the warp's 224 columns converted first, the
+            // accumulator released, then written in 64-column pieces (N is a
+            // multiple of 128 and a column half starts at a multiple of 32,
+            // so a piece can straddle N by exactly 32 columns: it is then a
+            // half piece) and a last 32-column half piece
+            uint32_t packed[PR_HN / 2];
+#pragma unroll
+            for (int chunk = 0; chunk < PR_HN / 16; ++chunk) {
+                uint32_t rr[16];
+                ptx::tmem_ld_32x32b_x16(taddr + chunk * 16, rr);
                 ptx::tmem_wait_ld();
-                if (pc == 3) {
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive_cluster(tempty_l + 8 * b);
-                }
-                const int64_t n0 = static_cast<int64_t>(nb) * PR_BN + pc * 64;
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    packed[chunk * 8 + e] =
+                        ptx::cvt_bf16x2(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_cluster(tempty_l);
+#pragma unroll
+            for (int pc = 0; pc < PR_HN / 64; ++pc) {        // three 64-column pieces
+                const int64_t n0 = col0 + pc * 64;
                 if (n0 >= p.N) continue;
                 uint8_t *g = reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.c) + row0 * p.ldc + n0);
-                uint4 v[8];
+                if (n0 + 64 <= p.N) {
+                    uint4 v[8];
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    v[c] = make_uint4(ptx::cvt_bf16x2(__uint_as_float(r0[8 * c]), __uint_as_float(r0[8 * c + 1])),
-                                      ptx::cvt_bf16x2(__uint_as_float(r0[8 * c + 2]), __uint_as_float(r0[8 * c + 3])),
-                                      ptx::cvt_bf16x2(__uint_as_float(r0[8 * c + 4]), __uint_as_float(r0[8 * c + 5])),
-                                      ptx::cvt_bf16x2(__uint_as_float(r0[8 * c + 6]), __uint_as_float(r0[8 * c + 7])));
-                if (pc < 3 && n0 + 64 <= p.N) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        v[4 + c] = make_uint4(ptx::cvt_bf16x2(__uint_as_float(r1[8 * c]), __uint_as_float(r1[8 * c + 1])),
-                                              ptx::cvt_bf16x2(__uint_as_float(r1[8 * c + 2]), __uint_as_float(r1[8 * c + 3])),
-                                              ptx::cvt_bf16x2(__uint_as_float(r1[8 * c + 4]), __uint_as_float(r1[8 * c + 5])),
-                                              ptx::cvt_bf16x2(__uint_as_float(r1[8 * c + 6]), __uint_as_float(r1[8 * c + 7])));
+                    for (int c = 0; c < 8; ++c)
+                        v[c] = make_uint4(packed[pc * 32 + 4 * c], packed[pc * 32 + 4 * c + 1],
+                                          packed[pc * 32 + 4 * c + 2], packed[pc * 32 + 4 * c + 3]);
                     store_piece(stage, v, lane, g, p.ldc * 2);
                 } else {
-                    const uint4(&h)[4] = *reinterpret_cast<const uint4(*)[4]>(&v[0]);
-                    store_piece64(stage, h, lane, g, p.ldc * 2);
+                    uint4 v[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        v[c] = make_uint4(packed[pc * 32 + 4 * c], packed[pc * 32 + 4 * c + 1],
+                                          packed[pc * 32 + 4 * c + 2], packed[pc * 32 + 4 * c + 3]);
+                    store_piece64(stage, v, lane, g, p.ldc * 2);
+                }
+            }
+            {                                                // the last 32 columns
+                const int64_t n0 = col0 + 192;
+                if (n0 < p.N) {
+                    uint4 v[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        v[c] = make_uint4(packed[96 + 4 * c], packed[96 + 4 * c + 1],
+                                          packed[96 + 4 * c + 2], packed[96 + 4 * c + 3]);
+                    store_piece64(stage, v, lane,
+                                  reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.c) + row0 * p.ldc + n0),
+                                  p.ldc * 2);
                 }
             }
             ++tcount;
@@ -1734,7 +1760,7 @@ int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
     std::memset(&ta, 0, sizeof(ta));
     std::memset(&tb, 0, sizeof(tb));
     if (!make_tmap(&ta, g.a_codes, g.M, g.K, g.lda, paired ? 128 : (wide ? WBM : BM))) return 1;
-    if (!make_tmap(&tb, g.b_codes, g.N, g.K, g.ldb, paired ? PR_BN / 2 : (wide ? WBN : BN))) return 1;
+    if (!make_tmap(&tb, g.b_codes, g.N, g.K, g.ldb, paired ? PR_HN / 2 : (wide ? WBN : BN))) return 1;
 
     KParams p;
     p.M = static_cast<int>(g.M);
@@ -1764,7 +1790,7 @@ int launch_gemm_scaled(const GemmArgs &g, cudaStream_t stream) {
     // bits 17-22, UE8M0 scale type in bit 23, M >> 4 in bits 24-28; the
     // scale-factor byte ids (bits 4-5 for B, 29-30 for A) are set per MMA.
     // (the pair kernel's MMA spans M = 256 rows of both CTAs)
-    p.idesc = (1u << 23) | (static_cast<uint32_t>(tbn >> 3) << 17) |
+    p.idesc = (1u << 23) | (static_cast<uint32_t>((paired ? PR_HN : tbn) >> 3) << 17) |
               (static_cast<uint32_t>((paired ? PR_BM : BM) >> 4) << 24) |
               (static_cast<uint32_t>(g.fmt_a) << 7) | (static_cast<uint32_t>(g.fmt_b) << 10);
     p.wait_limit_ns = g.wait_limit_ns;

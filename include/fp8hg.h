@@ -454,7 +454,7 @@ int fp8_gemm_scaled_q(int op, const fp8hg_operand *a, const fp8hg_operand *b, ui
  *                  complete: a host-chosen, GPU-safe way to exercise the
  *                  timeout path in tests.
  *   tile           0 = the library's choice.  1 = 128 x 256 tiles.  2 = 256 x 224
- *                  tiles (two accumulators per B stage).  3 = 256 x 256 tiles
+ *                  tiles (two accumulators per B stage).  3 = 256 x 448 tiles
  *                  computed by a pair of CTAs (a two-CTA cluster sharing the
  *                  MMA).  2 and 3 are honoured when M is a multiple of 256,
  *                  else FP8HG_ERR_UNSUPPORTED.  The result does not depend on

@@ -166,7 +166,7 @@ def _gemm_operands(M, N, K):
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("accumulate", [False, True])
 def test_gemm_output_canary(cuda_lib, tile, dtype, accumulate):
-    """N = 384 ends inside every tile shape's last n-tile (256 + 128, 224 + 160)."""
+    """N = 384 ends inside every tile shape's last n-tile (256 + 128, 224 + 160, 448)."""
     M, N, K = 256, 384, 256
     a, b, (c_ref, s_abs) = _gemm_operands(M, N, K)
     cbuf, c = canvas(M, N, N + 64, dtype=dtype)

@@ -44,10 +44,13 @@ CASES = [
     (WGRAD, (GRAN_1x128, E4M3, "act"), (GRAN_1x128, E5M2, "grad"), 256, 640, 640),
     (DGRAD, (GRAN_ROW, E5M2, "grad"), (GRAN_128x128, E5M2, "weight"), 512, 256, 384),
     (FPROP, (GRAN_MX32, E4M3, "normal"), (GRAN_MX32, E5M2, "mx_ln"), 256, 256, 384),
+    # several n-tiles of every shape, the last one ragged (1152 = 2 x 448 + 256 =
+    # 5 x 224 + 32 = 4 x 256 + 128)
+    (FPROP, (GRAN_ROW, E4M3, "act"), (GRAN_128x128, E4M3, "weight"), 512, 1152, 384),
 ]
 
 
-TILES = [1, 2, 3]   # 128 x 256 tiles; 256 x 224 tiles with two accumulators; CTA pairs (256 x 256)
+TILES = [1, 2, 3]   # 128 x 256 tiles; 256 x 224 tiles with two accumulators; CTA pairs (256 x 448)
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: f"op{c[0]}-{c[1][0]}{c[1][1]}-{c[2][0]}{c[2][1]}-{c[3]}x{c[4]}x{c[5]}")
@@ -70,7 +73,7 @@ def test_gemm_matches_oracle(cuda_lib, case, out_dtype, tile):
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 def test_gemm_accumulate(cuda_lib, tile, out_dtype):
     """C = A1 B^T, then C += A2 B^T; N = 384 leaves a ragged last tile for
-    both tile shapes (384 = 256 + 128 = 224 + 160)."""
+    every tile shape (384 = 256 + 128 = 224 + 160; 384 < 448)."""
     M, N, K = 256, 384, 512
     qa, sa = _operand("act", M, K, GRAN_1x128, E4M3, 1)
     qb, sb = _operand("weight", N, K, GRAN_128x128, E4M3, 2)
