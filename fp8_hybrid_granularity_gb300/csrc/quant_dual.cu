@@ -22,7 +22,7 @@
 // b + G, ... (G = grid), so the tiles of a stripe are taken by neighbouring
 // CTAs in the same round of the grid, or in two consecutive rounds.  Each
 // CTA prefetches its next tile into a private shared-memory region by
-// cp.async while it works on steps 2 and 3 of the current one.  A CTA waits in step 3 only
+// cp.async as soon as step 1 is counted, while it works on steps 2 and 3.  A CTA waits in step 3 only
 // for first steps of the same round or of the next round's first CTAs, which
 // never wait themselves on a later round while the stripe is at most G tiles
 // wide (checked by the launcher), so the waits cannot form a cycle.  Every
@@ -195,6 +195,18 @@ __global__ void __launch_bounds__(kDThreads, 4)
             for (int p = 0; p < 4; ++p) sm.cred[warp][p][v] = cp[p];
         }
         __syncthreads();
+        if (tid == 0) {
+            // release: one fence, after the barrier, orders every thread's
+            // token maxima of this tile before the count (a fence in every
+            // thread would stall each of them on its own outstanding stores)
+            __threadfence();
+            if (!withhold) atomicAdd(done + stripe, 1u);
+            withhold = false;
+        }
+        // every thread has its block in registers: the next tile's copies go
+        // out now (thread 0's after its fence, which would otherwise wait for
+        // them) and land while this tile is finished
+        if (t + gridDim.x < n1) issue(t + gridDim.x);
         // 2. column scales and the transposed codes (staged in shared memory)
         uint32_t cbyte = 0;   // column tid's scale byte (tid < 128), stored after the count
         if (tid < kDC) {
@@ -225,17 +237,6 @@ __global__ void __launch_bounds__(kDThreads, 4)
             sm.codes[c][(g ^ (c >> 3)) & 15] = w;   // token group g of column c
         }
         __syncthreads();
-        if (tid == 0) {
-            // release: one fence, after the barrier, orders every thread's
-            // token maxima of this tile before the count (a fence in every
-            // thread would stall each of them on its own outstanding stores)
-            __threadfence();
-            if (!withhold) atomicAdd(done + stripe, 1u);
-            withhold = false;
-        }
-        // the next tile's copies, issued after the fence so that it does not
-        // wait for them
-        if (t + gridDim.x < n1) issue(t + gridDim.x);
         if (tid < kDC) st[(c0 + tid) * ld_st + stripe] = static_cast<uint8_t>(cbyte);
         // transposed rows: column c, tokens 16 h .. 16 h + 15 (two token groups)
 #pragma unroll
