@@ -43,6 +43,7 @@ environment, N replicas are started here, one process per local GPU.
 from __future__ import annotations
 
 import argparse
+import functools
 import hashlib
 import json
 import os
@@ -94,7 +95,8 @@ def _parse(argv=None):
     ap.add_argument("--split", type=int, default=1,
                     help="K parts of the gemm_shape case (1 = no split, 0 = the library's choice)")
     ap.add_argument("--tile", type=int, default=0,
-                    help="GEMM tile of a --kernel case (0 = the library's choice; see fp8hg_gemm_opts)")
+                    help="GEMM tile of a --kernel case or of every GEMM of a step config "
+                         "(0 = the library's choice; see fp8hg_gemm_opts)")
     return ap.parse_args(argv)
 
 
@@ -184,6 +186,7 @@ class StepBase:
     QUANT_NAMES: list = []
     WORKLOAD = ""
     DESC: dict = {}
+    TILE = 0      # GEMM tile of every GEMM in the step (0 = the library's choice)
 
     def __init__(self, torch, f, device):
         self.torch, self.f, self.dev = torch, f, device
@@ -338,7 +341,7 @@ class LinearStep7B(StepBase):
             for n in self.ACTS:
                 _, qt, fmt = tok[n]
                 L.timed("quant", lambda: f.fp8_quant_token(i[n], 128, fmt, True, out=qt))
-        g = f.fp8_gemm_scaled
+        g = functools.partial(f.fp8_gemm_scaled, tile=self.TILE)
         L.timed("gemm", lambda: g(f.FPROP, self.xq, W["W_gate"][0], out=o["Y_gate"]))
         L.finished("Y_gate")
         L.timed("gemm", lambda: g(f.FPROP, self.xq, W["W_up"][0], out=o["Y_up"]))
@@ -397,7 +400,7 @@ class FpropStep(StepBase):
             L.timed("quant", lambda: f.fp8_quant_token(i[a], 0, f.E4M3, out=q))
         for w, a in self.gemms:
             L.timed("gemm", lambda: f.fp8_gemm_scaled(f.FPROP, self.aq[a], self.wq[w],
-                                                      out=self.out[f"Y_{w}"]))
+                                                      out=self.out[f"Y_{w}"], tile=self.TILE))
             L.finished(f"Y_{w}")
 
 
@@ -450,7 +453,7 @@ class Mxfp8Step(StepBase):
             L.timed("quant", lambda: f.fp8_quant_mx32(self.inp[n], f.E4M3, clamp_count=self.clamps,
                                                       out=self.q[n]))
         L.timed("gemm", lambda: f.fp8_gemm_scaled(f.FPROP, self.q["A"], self.q["B"],
-                                                  out=self.out["C"]))
+                                                  out=self.out["C"], tile=self.TILE))
         L.finished("C")
 
 
@@ -940,6 +943,7 @@ def run_step_config(args, torch, dist, fp8hg, workloads, ri, dev, peaks):
     cls = STEPS[args.config]
     if hasattr(cls, "ACT_QUANT"):
         cls.ACT_QUANT = args.act_quant
+    cls.TILE = args.tile
     step = cls(torch, fp8hg, workloads, dev, seed_offset=rank)
     torch.cuda.synchronize()
 
@@ -1055,8 +1059,9 @@ def run_step_config(args, torch, dist, fp8hg, workloads, ri, dev, peaks):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     mhz = clk.get("sm_mhz")
     at_clock = TENSOR_FLOP_PER_CYCLE_SM * sms * mhz * 1e6 / 1e12 if mhz else None
-    gemm_kernel = ("k_gemm_wide" if args.config == "linear_step_7b" else
-                   "fp8_gemm_scaled (k_gemm_wide or k_gemm_mxf8 by the library's tile rule)")
+    gemm_kernel = {1: "k_gemm_mxf8", 2: "k_gemm_wide", 3: "k_gemm_pair"}.get(
+        cls.TILE, "k_gemm_wide" if args.config == "linear_step_7b" else
+        "fp8_gemm_scaled (k_gemm_wide or k_gemm_mxf8 by the library's tile rule)")
     return {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -1065,11 +1070,12 @@ def run_step_config(args, torch, dist, fp8hg, workloads, ri, dev, peaks):
         "config": dict({"workload": cls.WORKLOAD, "name": args.config,
                         "gemms_per_step": ng, "quant_launches_per_step": nq,
                         "l2": L2_NOTE[args.config], "launch": launch,
-                        "act_quant": getattr(cls, "ACT_QUANT", None),
+                        "act_quant": getattr(cls, "ACT_QUANT", None), "gemm_tile": cls.TILE,
                         "parallelism": "replicas" if world > 1 else "single GPU"}, **cls.DESC),
         "roofline": {"bound": "tensor", "kernel": gemm_kernel, "achieved": gemm_tf,
                      "peak": fp8_peak, "unit": "TFLOP/s", "frac": gemm_tf / fp8_peak,
-                     "traffic": _gemm_traffic() if args.config == "linear_step_7b" else None,
+                     "traffic": (_gemm_traffic() if args.config == "linear_step_7b" and cls.TILE in (0, 2)
+                                 else None),
                      "peak_source": peak_src,
                      "per_launch_flop": step.flop / ng, "avg_launch_ms": gemm_step_ms / ng,
                      "clock_normalised": {"sm_mhz": mhz, "sms": sms,
