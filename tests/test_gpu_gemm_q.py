@@ -7,8 +7,10 @@ oracle's fp64 sum by accumulation order, so two kinds of check are used:
     equal the oracle's quantization of C bit for bit;
   * general products: every scale byte is the oracle's round-up exponent of
     the group's amax (or its neighbour when the amax lies within the GEMM
-    tolerance of a power-of-two boundary), and every dequantized code lies
-    within the GEMM tolerance plus half an FP8 step of the oracle's C.
+    tolerance of a power-of-two boundary), and every code is the oracle's
+    round-to-nearest-even encoding of some value within the GEMM tolerance of
+    the oracle's C under that scale: the encoder is monotonic, so the code
+    must lie between the encodings of (C - tol) / 2^e and (C + tol) / 2^e.
 """
 import numpy as np
 import pytest
@@ -99,6 +101,14 @@ def check_quantized_output(codes, scales, c_ref, s_abs, fmt, what):
             bad = ~(err <= bound)
             assert not bad.any(), (f"{what}: row {i} col {128 * g + np.argmax(bad)}: "
                                    f"{x_hat[bad][0]} vs {c_ref[i, cs][bad][0]}")
+            # the code is the RNE encoding of a value within tolerance of C
+            enc = lambda y: dec[oracle.fp8_encode(float(y), fmt, True)]
+            lo = np.array([enc(y) for y in (c_ref[i, cs] - tol[i, cs]) * 2.0 ** -e])
+            hi = np.array([enc(y) for y in (c_ref[i, cs] + tol[i, cs]) * 2.0 ** -e])
+            got = dec[codes[i, cs]]
+            bad = ~((lo <= got) & (got <= hi))
+            assert not bad.any(), (f"{what}: row {i} col {128 * g + np.argmax(bad)}: code value "
+                                   f"{got[bad][0]} outside [{lo[bad][0]}, {hi[bad][0]}]")
 
 
 @pytest.mark.parametrize("fmt_c", [E4M3, E5M2])
