@@ -70,8 +70,8 @@ TENSOR_FLOP_PER_CYCLE_SM = 16384      # dense FP8 MMA rate of one SM (128x256x32
 # step's three GEMM classes (gate-like, down-like, weight gradient; three
 # launches each), captured with ncu; valid only for the gemm.cu it was taken
 # on; any other source gives traffic null.
-GEMM_TRAFFIC = {"gemm_sha256": "6dc2437b861cd63de90d68a50992035937bfe48a88f510ee53cde609252005f2",
-                "bytes_per_launch": 1.1150e9}
+GEMM_TRAFFIC = {"gemm_sha256": "cfb1fec6a8fe3f5981b2cf22206f4748ec5517e80f3789a677abb1059653518a",
+                "bytes_per_launch": 1.1149e9}
 
 
 def _parse(argv=None):
