@@ -81,11 +81,14 @@ def test_block128_full_size(data):
         assert int(qt.scales()[cb, rb]) == int(sto[0, 0])
 
 
-def test_fprop_down_gemm_full_size(data):
+# tile 0: the library's choice (the 256 x 224 kernel at these shapes, as the
+# step runs); tile 3: the CTA-pair kernel (256 x 448 tiles, opt-in)
+@pytest.mark.parametrize("tile", [0, 3])
+def test_fprop_down_gemm_full_size(data, tile):
     """Y = H W_down^T, M=16384, K=18944, N=3584; 256 sampled outputs."""
     h, w = data["H"], data["W_down"]
     y = fp8hg.fp8_gemm_scaled(fp8hg.FPROP, fp8hg.fp8_quant_token(h, 0, E4M3),
-                              fp8hg.fp8_quant_block128(w, E4M3))
+                              fp8hg.fp8_quant_block128(w, E4M3), tile=tile)
     assert fp8hg.fp8hg_get_device_error() == 0
     rng = np.random.default_rng(3)
     ii = rng.choice(M, 16, replace=False)
@@ -136,14 +139,17 @@ def _dgrad_ref(dy, w, ii, b, jj, fmt_dy):
                                  I.ravel(), J.ravel())
 
 
-def test_dgrad_down_gemm_full_size(data):
+@pytest.mark.parametrize("tile", [0, 3])
+def test_dgrad_down_gemm_full_size(data, tile):
     """dH = dY_down W_down as the step runs it: A = dY_down [16384, 3584] per
     token E5M2, B = W_down^T [18944, 3584] (the transposed block copy);
-    contraction 3584, N = 18944, BF16 out; 192 sampled outputs."""
+    contraction 3584, N = 18944, BF16 out; 192 sampled outputs, including the
+    last 128-column block (inside the ragged last n-tile of both tile shapes:
+    18944 = 84 x 224 + 128 = 42 x 448 + 128)."""
     dy, w = data["dY_down"], data["W_down"]
     a = fp8hg.fp8_quant_token(dy, 0, E5M2)
     _, bt = fp8hg.fp8_quant_block128(w, E4M3, transposed_copy=True)
-    dh = fp8hg.fp8_gemm_scaled(fp8hg.DGRAD, a, bt)
+    dh = fp8hg.fp8_gemm_scaled(fp8hg.DGRAD, a, bt, tile=tile)
     assert dh.shape == (M, MLP)
     assert fp8hg.fp8hg_get_device_error() == 0
     rng = np.random.default_rng(5)
