@@ -8,16 +8,19 @@
   linear_step_7b  one Qwen2.5-7B-shaped MLP block (gate, up, down) at
                   M = 16384 tokens, hidden 3584, MLP width 18944, run through
                   the C ABI:
-                    quantize  W_gate, W_up, W_down   128x128 blocks, E4M3 (+ transposed copies)
+                    quantize  W_gate, W_up, W_down   128x128 blocks, E4M3 (+ transposed copies),
+                                                     one batched launch
                               X, H                   per token, E4M3
                               dY_gate, dY_up, dY_down per token, E5M2
                               X^T, H^T, dY^T (x3)    1x128 groups along tokens (wgrad layout)
                     fprop     Y_g = X W_g^T, Y_u = X W_u^T, Y_d = H W_d^T      (BF16 out)
                     dgrad     dX = dY_g W_g + dY_u W_u (accumulated), dH = dY_d W_d (BF16)
                     wgrad     dW_g = dY_g^T X, dW_u = dY_u^T X, dW_d = dY_d^T H  (FP32 out)
-                  13 quantizer launches + 9 GEMM launches per step.
+                  6 quantizer launches (both activation layouts from one read
+                  each; 11 with --act-quant separate) + 9 GEMM launches per step.
   fprop_1p5b      Qwen2.5-1.5B layer fprop at M = 8192: X, H per token, the
-                  gate / up / down / QKV weights in 128x128 blocks, four GEMMs.
+                  gate / up / down / QKV weights in 128x128 blocks (one batched
+                  launch), four GEMMs.
   tiny_fprop      X [256 x 512] per token, W [512 x 512] blocks, one GEMM.
   mxfp8_4096      MXFP8: A, B [4096 x 4096] (layer-norm-like and normal rows)
                   quantized in 32-element blocks (clamps counted), C = A B^T.
@@ -266,10 +269,10 @@ class LinearStep7B(StepBase):
     ACTS = ("X", "H", "dY_gate", "dY_up", "dY_down")
     # dual: each activation's per-token and transposed 1x128 codes from one
     # read (fp8_quant_token_dual); separate: one quantizer call per layout
-    QUANT_NAMES_DUAL = ["W_gate_blk", "W_up_blk", "W_down_blk", "X_dual", "H_dual", "dYg_dual",
-                        "dYu_dual", "dYd_dual"]
-    QUANT_NAMES_SEPARATE = ["W_gate_blk", "W_up_blk", "W_down_blk", "X_tok", "H_tok", "dYg_tok",
-                            "dYu_tok", "dYd_tok", "X_t", "H_t", "dYg_t", "dYu_t", "dYd_t"]
+    # the three weights in one batched launch (fp8_quant_block128_batch)
+    QUANT_NAMES_DUAL = ["W_blk_batch", "X_dual", "H_dual", "dYg_dual", "dYu_dual", "dYd_dual"]
+    QUANT_NAMES_SEPARATE = ["W_blk_batch", "X_tok", "H_tok", "dYg_tok", "dYu_tok", "dYd_tok",
+                            "X_t", "H_t", "dYg_t", "dYu_t", "dYd_t"]
     ACT_QUANT = "dual"
     WORKLOAD = (f"linear_step_7b: Qwen2.5-7B MLP block (gate/up/down) fprop+dgrad+wgrad, "
                 f"M={M_TOK} tokens, hidden {HID}, MLP {MLP}; per-token E4M3 activations, "
@@ -321,10 +324,10 @@ class LinearStep7B(StepBase):
     def launches(self, L):
         f, i, o, W = self.f, self.inp, self.out, self.wq
         E4, E5 = f.E4M3, f.E5M2
-        for n in ("W_gate", "W_up", "W_down"):
-            w, wt = W[n]
-            L.need(n)
-            L.timed("quant", lambda: f.fp8_quant_block128(i[n], E4, True, out=w, out_t=wt))
+        wn = ("W_gate", "W_up", "W_down")
+        L.need(*wn)
+        L.timed("quant", lambda: f.fp8_quant_block128_batch([i[n] for n in wn], E4, True,
+                                                            outs=[W[n] for n in wn]))
         tok = {"X": (self.xq, self.xt, E4), "H": (self.hq, self.ht, E4)}
         tok.update({n: (self.dyq[n], self.dyt[n], E5) for n in ("dY_gate", "dY_up", "dY_down")})
         if self.dual:
@@ -382,7 +385,10 @@ class FpropStep(StepBase):
         self.gemms = gemms
         self.out = {f"Y_{w}": torch.empty((self.inp[a].shape[0], self.inp[w].shape[0]),
                                           dtype=torch.bfloat16, device=device) for w, a in gemms}
-        self.QUANT_NAMES = [f"{w}_blk" for w in weights] + [f"{a}_tok" for a in acts]
+        # several weights: one batched launch (fp8_quant_block128_batch)
+        self.batch_w = len(weights) > 1
+        self.QUANT_NAMES = (["W_blk_batch"] if self.batch_w else [f"{w}_blk" for w in weights]) + \
+            [f"{a}_tok" for a in acts]
         self.GEMM_NAMES = [f"fprop_{w}" for w, _ in gemms]
         self.quant_bytes = (sum(_blk_bytes(self.inp[w].numel(), False) for w in weights) +
                             sum(_tok_bytes(self.inp[a].numel(), self.inp[a].shape[0]) for a in acts))
@@ -392,9 +398,15 @@ class FpropStep(StepBase):
 
     def launches(self, L):
         f, i = self.f, self.inp
-        for w, q in self.wq.items():
-            L.need(w)
-            L.timed("quant", lambda: f.fp8_quant_block128(i[w], f.E4M3, out=q))
+        if self.batch_w:
+            ws = list(self.wq)
+            L.need(*ws)
+            L.timed("quant", lambda: f.fp8_quant_block128_batch(
+                [i[w] for w in ws], f.E4M3, outs=[(self.wq[w], None) for w in ws]))
+        else:
+            for w, q in self.wq.items():
+                L.need(w)
+                L.timed("quant", lambda: f.fp8_quant_block128(i[w], f.E4M3, out=q))
         for a, q in self.aq.items():
             L.need(a)
             L.timed("quant", lambda: f.fp8_quant_token(i[a], 0, f.E4M3, out=q))

@@ -109,6 +109,7 @@ def load_library(build_if_stale: bool = True):
         lib.fp8_gemm_scaled_f32s_ex.argtypes = [I, ctypes.POINTER(Operand),
                                                 ctypes.POINTER(Operand), P, I64, I, P, P]
         lib.fp8_quant_block128.argtypes = [P, I64, I64, I64, I, P, I64, P, I64, P, I64, P, I64, P]
+        lib.fp8_quant_block128_batch.argtypes = [P, I, I, P]
         lib.fp8_quant_mx32.argtypes = [P, I64, I64, I64, I, P, I64, P, I64, P, P]
         lib.fp8_quant_mx32_monitor.argtypes = [P, I64, I64, I64, I, P, I64, P, I64, P, P, P]
         lib.fp8_requant_t.argtypes = [P, I64, I64, I64, P, I64, I, I, I, P, I64, P, I64, P]
@@ -284,6 +285,45 @@ def fp8_quant_block128(x, fmt: int = E4M3, transposed_copy: bool = False, out=No
     if transposed_copy:
         return out, out_t
     return out
+
+
+BATCH_MAX = 8   # FP8HG_BATCH_MAX
+
+
+class _Block128Job(ctypes.Structure):
+    """fp8hg_block128_job of the C header."""
+    _fields_ = [("x", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("ld_x", ctypes.c_int64), ("q", ctypes.c_void_p), ("ld_q", ctypes.c_int64),
+                ("scale", ctypes.c_void_p), ("ld_s", ctypes.c_int64), ("q_t", ctypes.c_void_p),
+                ("ld_qt", ctypes.c_int64), ("scale_t", ctypes.c_void_p), ("ld_st", ctypes.c_int64)]
+
+
+def fp8_quant_block128_batch(xs, fmt: int = E4M3, transposed_copy: bool = False, outs=None,
+                             stream=None):
+    """fp8_quant_block128 on up to BATCH_MAX tensors in one launch.  Returns a
+    list with, per tensor, what fp8_quant_block128 returns.  outs: optional
+    list of preallocated (QTensor, QTensor or None) pairs (alloc_block128)."""
+    if len(xs) > BATCH_MAX:
+        raise ValueError(f"at most {BATCH_MAX} tensors per batch")
+    jobs = (_Block128Job * max(len(xs), 1))()
+    res = []
+    for i, x in enumerate(xs):
+        _check_bf16(x)
+        rows, cols = x.shape
+        if outs is not None and outs[i] is not None:
+            out, out_t = outs[i]
+        else:
+            out, out_t = alloc_block128(rows, cols, fmt, transposed_copy, x.device)
+        qt = out_t.codes if transposed_copy else None
+        st = out_t.scale if transposed_copy else None
+        jobs[i] = _Block128Job(_ptr(x), rows, cols, x.stride(0), _ptr(out.codes),
+                               out.codes.stride(0), _ptr(out.scale), out.scale.stride(0),
+                               _ptr(qt), qt.stride(0) if qt is not None else 0,
+                               _ptr(st), st.stride(0) if st is not None else 0)
+        res.append((out, out_t) if transposed_copy else out)
+    rc = lib().fp8_quant_block128_batch(ctypes.addressof(jobs), len(xs), fmt, _stream(stream))
+    _check(rc, "fp8_quant_block128_batch")
+    return res
 
 
 def alloc_block128(rows: int, cols: int, fmt: int = E4M3, transposed_copy: bool = False,

@@ -237,6 +237,39 @@ int fp8_quant_block128(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld
                                                          static_cast<cudaStream_t>(stream)));
 }
 
+int fp8_quant_block128_batch(const fp8hg_block128_job *jobs, int n, int fmt, void *stream) {
+    if (n < 0 || n > FP8HG_BATCH_MAX) return FP8HG_ERR_INVALID_ARG;
+    if (n == 0) return FP8HG_OK;
+    if (!jobs) return FP8HG_ERR_INVALID_ARG;
+    static_assert(FP8HG_BATCH_MAX <= fp8hg::kBlock128BatchMax, "batch table too small");
+    fp8hg::Block128Batch b{};
+    int64_t blocks = 0;
+    int trans = -1;
+    for (int i = 0; i < n; ++i) {
+        const fp8hg_block128_job &j = jobs[i];
+        int st = check_quant_common(j.x, j.rows, j.cols, j.ld_x, fmt, j.q, j.ld_q, j.scale);
+        if (st != FP8HG_OK) return st;
+        if (j.rows == 0 || j.cols == 0) continue;   // nothing read or written
+        if ((j.q_t == nullptr) != (j.scale_t == nullptr)) return FP8HG_ERR_INVALID_ARG;
+        const int t = j.q_t != nullptr;
+        if (trans >= 0 && t != trans) return FP8HG_ERR_INVALID_ARG;
+        trans = t;
+        if (j.rows % 128 || j.cols % 128) return FP8HG_ERR_SHAPE;
+        if (j.ld_x < j.cols || j.ld_q < j.cols || j.ld_s < j.cols / 128) return FP8HG_ERR_INVALID_ARG;
+        if (t) {
+            if (!aligned(j.q_t, 16) || j.ld_qt % 16) return FP8HG_ERR_ALIGNMENT;
+            if (j.ld_qt < j.rows || j.ld_st < j.rows / 128) return FP8HG_ERR_INVALID_ARG;
+        }
+        fp8hg::Block128Job &k = b.job[b.n++];
+        k = {j.x, j.ld_x, j.q, j.ld_q, j.scale, j.ld_s, j.q_t, j.ld_qt, j.scale_t, j.ld_st,
+             j.cols / 128, blocks};
+        blocks += (j.rows / 128) * (j.cols / 128);
+        if (blocks > 0x7FFFFFFF) return FP8HG_ERR_SHAPE;
+    }
+    return status_from_cuda(fp8hg::launch_quant_block128_batch(b, blocks, fmt, trans == 1,
+                                                               static_cast<cudaStream_t>(stream)));
+}
+
 int fp8_quant_mx32(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, int fmt, uint8_t *q,
                    int64_t ld_q, uint8_t *scale, int64_t ld_s, unsigned long long *clamp_count,
                    void *stream) {

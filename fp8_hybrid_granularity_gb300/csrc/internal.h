@@ -63,6 +63,28 @@ cudaError_t launch_requant_t(const uint8_t *q, int64_t rows, int64_t cols, int64
                              int fmt_out, uint8_t *qt, int64_t ld_qt, uint8_t *st, int64_t ld_st,
                              const WaitOpts &w, cudaStream_t stream);
 
+// Up to kBlock128BatchMax tensors' block quantization in one launch.
+constexpr int kBlock128BatchMax = 8;
+struct Block128Job {
+    const uint16_t *x;
+    int64_t ld_x;
+    uint8_t *q;
+    int64_t ld_q;
+    uint8_t *s;
+    int64_t ld_s;
+    uint8_t *qt;             // transposed copy (every job or none)
+    int64_t ld_qt;
+    uint8_t *st;
+    int64_t ld_st;
+    int64_t cbs;             // column blocks: cols / 128
+    int64_t first;           // the job's first block in the launch's grid
+};
+struct Block128Batch {
+    Block128Job job[kBlock128BatchMax];
+    int n;
+};
+cudaError_t launch_quant_block128_batch(const Block128Batch &b, int64_t blocks, int fmt, bool trans,
+                                        cudaStream_t stream);
 cudaError_t launch_quant_block128(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
                                   int fmt, uint8_t *q, int64_t ld_q, uint8_t *s, int64_t ld_s,
                                   uint8_t *qt, int64_t ld_qt, uint8_t *st, int64_t ld_st,

@@ -635,17 +635,17 @@ __device__ __forceinline__ void transpose4x4(uint32_t a0, uint32_t a1, uint32_t 
     c[3] = __byte_perm(t1, t3, 0x7632);
 }
 
-// One CTA per 128x128 block; thread (rsub, csub) owns an 8x8 sub-block.
+// One CTA per 128x128 block (rb, cb); thread (rsub, csub) owns an 8x8
+// sub-block.
 template <int FMT, bool TRANS, int SM>
-__global__ void __launch_bounds__(256) k_quant_block128(const uint16_t *__restrict__ x,
-                                                        int64_t ld_x, uint8_t *__restrict__ q,
-                                                        int64_t ld_q, uint8_t *__restrict__ s,
-                                                        int64_t ld_s, uint8_t *__restrict__ qt,
-                                                        int64_t ld_qt, uint8_t *__restrict__ st,
-                                                        int64_t ld_st) {
+__device__ __forceinline__ void block128_body(const uint16_t *__restrict__ x, int64_t ld_x,
+                                              uint8_t *__restrict__ q, int64_t ld_q,
+                                              uint8_t *__restrict__ s, int64_t ld_s,
+                                              uint8_t *__restrict__ qt, int64_t ld_qt,
+                                              uint8_t *__restrict__ st, int64_t ld_st,
+                                              int64_t rb, int64_t cb) {
     __shared__ uint32_t red[8];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t rb = blockIdx.y, cb = blockIdx.x;
     const int rsub = tid >> 4, csub = tid & 15;
     const int64_t r_first = rb * 128 + rsub * 8, c_first = cb * 128 + csub * 8;
     const uint16_t *xb = x + r_first * ld_x + c_first;
@@ -703,6 +703,30 @@ __global__ void __launch_bounds__(256) k_quant_block128(const uint16_t *__restri
             *reinterpret_cast<uint4 *>(qt + (c0 + row) * ld_qt + r0 + c16 * 16) = make_uint4(a.x, a.y, b.x, b.y);
         }
     }
+}
+
+template <int FMT, bool TRANS, int SM>
+__global__ void __launch_bounds__(256) k_quant_block128(const uint16_t *__restrict__ x,
+                                                        int64_t ld_x, uint8_t *__restrict__ q,
+                                                        int64_t ld_q, uint8_t *__restrict__ s,
+                                                        int64_t ld_s, uint8_t *__restrict__ qt,
+                                                        int64_t ld_qt, uint8_t *__restrict__ st,
+                                                        int64_t ld_st) {
+    block128_body<FMT, TRANS, SM>(x, ld_x, q, ld_q, s, ld_s, qt, ld_qt, st, ld_st, blockIdx.y,
+                                  blockIdx.x);
+}
+
+// Several tensors' 128x128 blocks in one grid: CTA b belongs to the last job
+// whose first block is <= b, and takes that job's block b - first (row-major
+// over the job's block grid).
+template <int FMT, bool TRANS, int SM>
+__global__ void __launch_bounds__(256) k_quant_block128_batch(const __grid_constant__ Block128Batch bt) {
+    int j = bt.n - 1;
+    while (j > 0 && static_cast<int64_t>(blockIdx.x) < bt.job[j].first) --j;
+    const Block128Job &jb = bt.job[j];
+    const int64_t local = static_cast<int64_t>(blockIdx.x) - jb.first;
+    block128_body<FMT, TRANS, SM>(jb.x, jb.ld_x, jb.q, jb.ld_q, jb.s, jb.ld_s, jb.qt, jb.ld_qt,
+                                  jb.st, jb.ld_st, local / jb.cbs, local % jb.cbs);
 }
 
 // ------------------------------------------------------------------ launchers
@@ -1042,6 +1066,20 @@ cudaError_t launch_quant_block128(const uint16_t *x, int64_t rows, int64_t cols,
     else
         launch_block128_t<FMT_E5M2, SCALE_UE8M0>(x, rows, cols, ld_x, q, ld_q, s, ld_s, qt, ld_qt,
                                                  st, ld_st, stream);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_block128_batch(const Block128Batch &b, int64_t blocks, int fmt, bool trans,
+                                        cudaStream_t stream) {
+    if (b.n == 0 || blocks == 0) return cudaSuccess;
+    const dim3 grid(static_cast<unsigned>(blocks));
+    if (fmt == FMT_E4M3) {
+        if (trans) k_quant_block128_batch<FMT_E4M3, true, SCALE_UE8M0><<<grid, 256, 0, stream>>>(b);
+        else k_quant_block128_batch<FMT_E4M3, false, SCALE_UE8M0><<<grid, 256, 0, stream>>>(b);
+    } else {
+        if (trans) k_quant_block128_batch<FMT_E5M2, true, SCALE_UE8M0><<<grid, 256, 0, stream>>>(b);
+        else k_quant_block128_batch<FMT_E5M2, false, SCALE_UE8M0><<<grid, 256, 0, stream>>>(b);
+    }
     return cudaGetLastError();
 }
 

@@ -222,6 +222,41 @@ int fp8_quant_block128(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld
                        int64_t ld_qt, uint8_t *scale_t, int64_t ld_st, void *stream);
 
 /*
+ * fp8_quant_block128_batch — fp8_quant_block128 on up to FP8HG_BATCH_MAX
+ * tensors in one launch (for example every weight of a layer, re-quantized
+ * each training step), all in the same format.  Each job's codes, scales and
+ * optional transposed copy are exactly those fp8_quant_block128 writes for
+ * that tensor alone.
+ *
+ * Passage: as fp8_quant_block128.
+ *
+ *   jobs     n job descriptions (host memory, read during the call only);
+ *            fields as the arguments of fp8_quant_block128
+ *   n        0 .. FP8HG_BATCH_MAX (0: nothing to do)
+ *   fmt      FP8HG_E4M3 or FP8HG_E5M2, for every job
+ * Requirements: each job as fp8_quant_block128 requires; the transposed copy
+ * is asked for by every job or by none (q_t and scale_t all NULL or all
+ * non-NULL), else FP8HG_ERR_INVALID_ARG; jobs with rows or cols 0 are
+ * skipped.  The outputs of different jobs must not overlap.  Every job is
+ * checked before anything is launched: on an error nothing is written.
+ */
+#define FP8HG_BATCH_MAX 8
+typedef struct {
+    const uint16_t *x;
+    int64_t rows, cols, ld_x;
+    uint8_t *q;
+    int64_t ld_q;
+    uint8_t *scale;
+    int64_t ld_s;
+    uint8_t *q_t;
+    int64_t ld_qt;
+    uint8_t *scale_t;
+    int64_t ld_st;
+} fp8hg_block128_job;
+
+int fp8_quant_block128_batch(const fp8hg_block128_job *jobs, int n, int fmt, void *stream);
+
+/*
  * fp8_quant_mx32 — MXFP8 quantizer: 32 consecutive elements of a row share
  * one E8M0 scale 2^e with e = floor(log2 amax) - emax (emax = 8 for E4M3,
  * 15 for E5M2), clamped to [-127, 127]; codes are the saturating

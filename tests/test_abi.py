@@ -16,7 +16,7 @@ EXPECTED = {"fp8_quant_token", "fp8_quant_block128", "fp8_quant_mx32", "fp8_quan
             "fp8_quant_token_ex", "fp8_requant_t_ex", "fp8_gemm_scaled_f32s_ex",
             "fp8_quant_token_dual", "fp8_quant_token_dual_workspace",
             "fp8_quant_token_dual_noalloc", "fp8_gemm_scaled_splitk",
-            "fp8_gemm_splitk_workspace"}
+            "fp8_gemm_splitk_workspace", "fp8_quant_block128_batch"}
 
 OK, INVALID, ALIGN, SHAPE, UNSUP = 0, 1, 2, 3, 4
 FAKE = 0x10000  # never dereferenced: every call below fails validation first
@@ -72,6 +72,38 @@ def test_block128_and_mx_validation(lib):
     assert mon(FAKE, 4, 64, 64, E4M3, FAKE, 64, FAKE, 2, FAKE, FAKE + 2, None) == ALIGN
     assert mon(FAKE, 4, 64, 64, E4M3, FAKE, 64, FAKE, 1, FAKE, None, None) == INVALID  # ld_s
     assert mon(FAKE, 0, 64, 64, E4M3, FAKE, 64, FAKE, 2, FAKE, None, None) == OK       # empty
+
+
+def test_block128_batch_validation(lib):
+    """Every job is checked before anything is launched; none of these reaches
+    the device (the ones that pass validation have no blocks to launch)."""
+    J = fp8hg._Block128Job
+
+    def job(rows=128, cols=128, ld_x=128, q=FAKE, ld_q=128, s=FAKE, ld_s=1, qt=None, ld_qt=0,
+            st=None, ld_st=0, x=FAKE):
+        return J(x, rows, cols, ld_x, q, ld_q, s, ld_s, qt, ld_qt, st, ld_st)
+
+    def call(*jobs, n=None, fmt=E4M3):
+        arr = (J * max(len(jobs), 1))(*jobs)
+        return lib.fp8_quant_block128_batch(ctypes.addressof(arr), len(jobs) if n is None else n,
+                                            fmt, None)
+
+    assert call(n=0) == OK                                    # nothing to do
+    assert call(job(), n=-1) == INVALID
+    assert call(*[job()] * 9) == INVALID                      # more than FP8HG_BATCH_MAX
+    assert lib.fp8_quant_block128_batch(None, 1, E4M3, None) == INVALID
+    assert call(job(), fmt=7) == INVALID
+    assert call(job(rows=0), job(cols=0)) == OK               # empty jobs are skipped
+    assert call(job(), job(rows=100)) == SHAPE                # the second job's shape
+    assert call(job(), job(x=FAKE + 8)) == ALIGN
+    assert call(job(), job(ld_x=64)) == INVALID               # ld_x < cols
+    assert call(job(), job(ld_s=0)) == INVALID
+    assert call(job(qt=FAKE, ld_qt=128)) == INVALID           # q_t without scale_t
+    # the transposed copy for every job or for none
+    assert call(job(qt=FAKE, ld_qt=128, st=FAKE, ld_st=1), job()) == INVALID
+    assert call(job(qt=FAKE + 4, ld_qt=128, st=FAKE, ld_st=1)) == ALIGN
+    assert call(job(qt=FAKE, ld_qt=136, st=FAKE, ld_st=1)) == ALIGN       # ld_qt % 16 != 0
+    assert call(job(qt=FAKE, ld_qt=112, st=FAKE, ld_st=1)) == INVALID     # ld_qt < rows
 
 
 def test_requant_validation(lib):

@@ -93,6 +93,37 @@ def test_quant_block128(cuda_lib, fmt, rows, cols, trans):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("trans", [False, True])
+def test_quant_block128_batch(cuda_lib, fmt, trans):
+    """Several tensors in one launch (shapes of one, a few and many blocks, one
+    of them a strided column slice, one with a NaN block, an empty one): each
+    tensor's codes, scales and transposed copy equal the oracle's for that
+    tensor alone."""
+    shapes = [(384, 640), (128, 128), (256, 1536), (128, 256), (0, 256), (1280, 384)]
+    xs_bits = [_bits("weight", r, c, 1000 + i + fmt) if r else np.zeros((0, c), np.uint16)
+               for i, (r, c) in enumerate(shapes)]
+    xs_bits[0] = xs_bits[0].copy()
+    xs_bits[0][130, 5] = 0x7FC0                              # one NaN block
+    xs = [bits_to_cuda(b) if b.shape[0] else torch.empty(b.shape, dtype=torch.bfloat16, device="cuda")
+          for b in xs_bits]
+    wide = _bits("weight", 128, 512, 4242 + fmt)             # strided: the middle 256 columns
+    xs.append(bits_to_cuda(wide)[:, 128:384])
+    xs_bits.append(np.ascontiguousarray(wide[:, 128:384]))
+    res = fp8hg.fp8_quant_block128_batch(xs, fmt, transposed_copy=trans)
+    assert fp8hg.fp8hg_get_device_error() == 0
+    for i, (b, r) in enumerate(zip(xs_bits, res)):
+        if b.shape[0] == 0:
+            continue
+        q, s, qt, st = oracle.quant_block128(b, fmt, transposed_copy=trans)
+        g = r[0] if trans else r
+        assert_codes_equal(np_u8(g.scales()), s, f"job {i} scale")
+        assert_codes_equal(np_u8(g.codes), q, f"job {i} codes")
+        if trans:
+            assert_codes_equal(np_u8(r[1].scales()), st, f"job {i} scale_t")
+            assert_codes_equal(np_u8(r[1].codes), qt, f"job {i} codes_t")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("kind,rows,cols", [("mx_ln", 64, 4096), ("mx_ln_clamp", 64, 4096),
                                             ("act", 33, 96), ("act", 1, 32)])
 def test_quant_mx32(cuda_lib, fmt, kind, rows, cols):
