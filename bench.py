@@ -439,19 +439,28 @@ class TinyFprop(FpropStep):
 class Mxfp8Step(StepBase):
     INPUT_ORDER = ["A", "B"]
     GEMM_NAMES = ["mx_gemm"]
-    QUANT_NAMES = ["A_mx32", "B_mx32"]
+    QUANT_NAMES = ["AB_mx32"]
     WORKLOAD = ("mxfp8_4096: A, B [4096x4096] MXFP8 E4M3 (32-element blocks, E8M0 floor scales, "
                 "saturating), rows [0,2048) layer-norm-like 1 +- 1e-3, rows [2048,4096) N(0,1); "
-                "C = A B^T in BF16")
+                "C = A B^T in BF16; A and B stored as the halves of one [8192x4096] buffer and "
+                "quantized by one call")
     DESC = {"m": 4096, "n": 4096, "k": 4096, "block": 32}
 
     def __init__(self, torch, f, workloads, device, seed_offset=0):
         super().__init__(torch, f, device)
         spec = workloads.WORKLOADS["mxfp8_4096"]
         seed = replicas.replica_seed(spec["seed"], seed_offset)
-        self.inp = {n: workloads.make_tensor(kind, r, c, seed, n, device=device)
-                    for (n, kind, r, c) in spec["tensors"] if n in ("A", "B")}
-        self.q = {n: f.alloc_mx32(4096, 4096, f.E4M3, device) for n in ("A", "B")}
+        # A and B live in the two halves of one [8192 x 4096] buffer and are
+        # quantized by one call (each element still every step); the GEMM
+        # reads the two halves of the codes and scales
+        self.ab = torch.empty((8192, 4096), dtype=torch.bfloat16, device=device)
+        self.inp = {"A": self.ab[:4096], "B": self.ab[4096:]}
+        for (n, kind, r, c) in spec["tensors"]:
+            if n in ("A", "B"):
+                self.inp[n].copy_(workloads.make_tensor(kind, r, c, seed, n, device=device))
+        self.qab = f.alloc_mx32(8192, 4096, f.E4M3, device)
+        self.q = {n: f.QTensor(self.qab.codes[h], self.qab.scale[h], f.E4M3, f.GRAN_MX32, 4096 // 32)
+                  for n, h in (("A", slice(0, 4096)), ("B", slice(4096, 8192)))}
         self.clamps = torch.zeros(1, dtype=torch.int64, device=device)
         self.out = {"C": torch.empty((4096, 4096), dtype=torch.bfloat16, device=device)}
         self.quant_bytes = 2 * (3.0 * 4096 * 4096 + 4096 * 4096 / 32.0)
@@ -460,10 +469,9 @@ class Mxfp8Step(StepBase):
 
     def launches(self, L):
         f = self.f
-        for n in ("A", "B"):
-            L.need(n)
-            L.timed("quant", lambda: f.fp8_quant_mx32(self.inp[n], f.E4M3, clamp_count=self.clamps,
-                                                      out=self.q[n]))
+        L.need("A", "B")
+        L.timed("quant", lambda: f.fp8_quant_mx32(self.ab, f.E4M3, clamp_count=self.clamps,
+                                                  out=self.qab))
         L.timed("gemm", lambda: f.fp8_gemm_scaled(f.FPROP, self.q["A"], self.q["B"],
                                                   out=self.out["C"], tile=self.TILE))
         L.finished("C")
