@@ -84,8 +84,8 @@ def _parse(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--launch", default="eager", choices=["eager", "graph"],
-                    help="timed steps replayed from one CUDA graph, or launched one by one")
+    ap.add_argument("--launch", default="graph", choices=["eager", "graph"],
+                    help="timed steps replayed from one CUDA graph (default), or launched one by one")
     ap.add_argument("--act-quant", default="dual", choices=["dual", "separate"],
                     help="7B step: both activation layouts from one read, or one call each")
     ap.add_argument("--no-e2e", action="store_true")
@@ -199,20 +199,23 @@ class StepBase:
         self.out_bytes = sum(t.numel() * t.element_size() for t in self.out.values())
         self.flop = float(sum(self.gemm_flop))
 
-    def run(self, ev=None, ready=None, done=None, external=False):
+    def run(self, ev=None, ready=None, done=None, external=False, mark=None):
         """Enqueue one step on the current stream.  ev: optional list that
         receives (kind, start_event, end_event) per launch.  ready: optional
         {input name: event}, waited on before the first launch that reads the
         input.  done: optional dict that receives {output name: event},
         recorded after the output's last write.  external: the timing events
-        are recorded as event nodes of a graph being captured."""
-        self.launches(_Launcher(self.torch, ev, ready, done, external))
+        are recorded as event nodes of a graph being captured.  mark:
+        optional list that receives one event recorded before the step's
+        first GEMM (every step quantizes first, then multiplies)."""
+        self.launches(_Launcher(self.torch, ev, ready, done, external, mark))
 
 
 class _Launcher:
-    def __init__(self, torch, ev, ready, done, external=False):
+    def __init__(self, torch, ev, ready, done, external=False, mark=None):
         self.torch, self.ev, self.ready, self.done, self.waited = torch, ev, ready, done, set()
         self.ekw = {"enable_timing": True, "external": True} if external else {"enable_timing": True}
+        self.mark = mark        # list: receives one event recorded before the first GEMM
 
     def need(self, *names):
         if self.ready is None:
@@ -231,6 +234,10 @@ class _Launcher:
             self.done[n] = e
 
     def timed(self, kind, fn):
+        if self.mark is not None and kind == "gemm" and not self.mark:
+            e = self.torch.cuda.Event(**self.ekw)
+            e.record()
+            self.mark.append(e)
         if self.ev is None:
             fn()
             return
@@ -978,43 +985,47 @@ def run_step_config(args, torch, dist, fp8hg, workloads, ri, dev, peaks):
         raise RuntimeError("device error during warm-up")
     barrier()
 
-    # ---------------- timed region: K steps, every launch bracketed by events.
-    # Steps whose tensors fit in L2 (tiny, MX) are timed one by one, each
-    # after a 512 MB write that flushes L2 and outside the step's own events.
+    # ---------------- timed region: K steps as a user runs them, with three
+    # events per step (start, before the first GEMM, end): an event pair
+    # around every launch would cost the small configs 7-40 % (each record
+    # orders the stream, so a launch can no longer start while the one before
+    # drains).  The quantizers' time and the GEMMs' mean launch time come from
+    # these marks; the per-launch breakdown from an instrumented pass after.
+    # Steps whose tensors fit in L2 (tiny, MX) are each preceded by a 512 MB
+    # write that flushes L2, outside the step's events.
     flush = (torch.empty(512 * 2 ** 20 // 4, dtype=torch.float32, device=dev)
              if args.config in L2_FLUSHED else None)
 
-    def enqueue_timed(events, per_step, external):
+    def enqueue_timed(per_step, external):
         for _ in range(args.steps):
             if flush is not None:
                 flush.fill_(1.0)
-                a = torch.cuda.Event(enable_timing=True, external=external)
-                b = torch.cuda.Event(enable_timing=True, external=external)
-                a.record()
-                step.run(events, external=external)
-                b.record()
-                per_step.append((a, b))
-            else:
-                step.run(events, external=external)
+            a = torch.cuda.Event(enable_timing=True, external=external)
+            b = torch.cuda.Event(enable_timing=True, external=external)
+            mark = []
+            a.record()
+            step.run(external=external, mark=mark)
+            b.record()
+            per_step.append((a, mark[0], b))
 
-    # Graph launch: the K timed steps are captured once, with each launch's
-    # timing events as event nodes, and the timed region is one replay.
+    # Graph launch: the K timed steps are captured once, with the events as
+    # event nodes, and the timed region is one replay.
     launch = args.launch
     graph = None
     if launch == "graph":
         try:
-            events, per_step = [], []
+            per_step = []
             graph = torch.cuda.CUDAGraph()
             side = torch.cuda.Stream()
             side.wait_stream(torch.cuda.current_stream())
             with torch.cuda.graph(graph, stream=side):
-                enqueue_timed(events, per_step, True)
+                enqueue_timed(per_step, True)
             graph.replay()                      # untimed: uploads the graph
             barrier()
         except (TypeError, RuntimeError) as e:  # no external events in this torch
             graph, launch = None, f"eager (graph capture failed: {type(e).__name__})"
     if graph is None:
-        events, per_step = [], []
+        per_step = []
     clocks = ClockSampler(ri.local).start()
     time.sleep(0.2)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -1023,30 +1034,40 @@ def run_step_config(args, torch, dist, fp8hg, workloads, ri, dev, peaks):
     if graph is not None:
         graph.replay()
     else:
-        enqueue_timed(events, per_step, False)
+        enqueue_timed(per_step, False)
     t_end.record()
     barrier()
     if flush is None:
         ms = t_start.elapsed_time(t_end) / args.steps
     else:
-        ms = sum(a.elapsed_time(b) for a, b in per_step) / args.steps
+        ms = sum(a.elapsed_time(b) for a, _, b in per_step) / args.steps
     clk = clocks.stop()
-    del flush
     status = fp8hg.fp8hg_get_device_error()
     if status != 0:
         raise RuntimeError(f"device error: {fp8hg.fp8hg_status_str(status)}")
     ms = replicas.max_over_ranks(ms, dist, dev)
 
     ng, nq = len(step.GEMM_NAMES), len(step.QUANT_NAMES)
-    gemm_ms = [a.elapsed_time(b) for k, a, b in events if k == "gemm"]
-    quant_ms = [a.elapsed_time(b) for k, a, b in events if k == "quant"]
-    per_gemm = [sum(gemm_ms[j::ng]) / args.steps for j in range(ng)]
-    per_quant = [sum(quant_ms[j::nq]) / args.steps for j in range(nq)]
-    gemm_step_ms = sum(per_gemm)
-    quant_step_ms = sum(per_quant)
+    quant_step_ms = sum(a.elapsed_time(m) for a, m, _ in per_step) / args.steps
+    gemm_step_ms = sum(m.elapsed_time(b) for _, m, b in per_step) / args.steps
     value = replicas.job_throughput(world, step.flop, ms)
     gemm_tf = step.flop / (gemm_step_ms * 1e-3) / 1e12
     quant_gbs = step.quant_bytes / (quant_step_ms * 1e-3) / 1e9
+
+    # per-launch breakdown: an instrumented pass (an event pair around every
+    # launch), outside the timed region
+    events = []
+    n_inst = max(1, min(args.steps, 10))
+    for _ in range(n_inst):
+        if flush is not None:
+            flush.fill_(1.0)
+        step.run(events)
+    torch.cuda.synchronize()
+    del flush
+    gemm_ms = [a.elapsed_time(b) for k, a, b in events if k == "gemm"]
+    quant_ms = [a.elapsed_time(b) for k, a, b in events if k == "quant"]
+    per_gemm = [sum(gemm_ms[j::ng]) / n_inst for j in range(ng)]
+    per_quant = [sum(quant_ms[j::nq]) / n_inst for j in range(nq)]
 
     e2e = None
     if not args.no_e2e:
@@ -1098,6 +1119,8 @@ def run_step_config(args, torch, dist, fp8hg, workloads, ri, dev, peaks):
                                  else None),
                      "peak_source": peak_src,
                      "per_launch_flop": step.flop / ng, "avg_launch_ms": gemm_step_ms / ng,
+                     "timing": ("GEMM phase of every timed step (first GEMM to step end, "
+                                "CUDA events on the launching stream) / GEMMs per step"),
                      "clock_normalised": {"sm_mhz": mhz, "sms": sms,
                                           "flop_per_cycle_sm": TENSOR_FLOP_PER_CYCLE_SM,
                                           "peak_at_clock": at_clock,
@@ -1115,7 +1138,10 @@ def run_step_config(args, torch, dist, fp8hg, workloads, ri, dev, peaks):
                                     if getattr(step, "dual", False) else
                                     "per call: 2 B read + 1 B written per element + scales")},
         "per_launch_ms": {"gemm": dict(zip(step.GEMM_NAMES, [round(x, 4) for x in per_gemm])),
-                          "quant": dict(zip(step.QUANT_NAMES, [round(x, 4) for x in per_quant]))},
+                          "quant": dict(zip(step.QUANT_NAMES, [round(x, 4) for x in per_quant])),
+                          "note": (f"instrumented pass of {n_inst} steps after the timed region "
+                                   "(an event pair around every launch); the timed region "
+                                   "records only step start, first GEMM and step end")},
         "gpu_launches": (ng + nq) * args.steps,
         "clocks": clk,
         "fp8_peak_probe": probe,
