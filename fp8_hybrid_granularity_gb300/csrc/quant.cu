@@ -139,15 +139,19 @@ __global__ void __launch_bounds__(kRowThreads) k_quant_row(const uint16_t *__res
 // (MX 32): one scale per group of GV consecutive 16-byte vectors; thread tid
 // holds vectors tid + i * blockDim.x, so a group is GV consecutive lanes
 // (blockDim.x is a multiple of 32) and is reduced with lane shuffles.
-template <int FMT, int NV, int SM, int GV>
+// COUNT (MX groups only): add the row's saturated elements to *cnt, one
+// atomic per CTA and none for a row without any.
+template <int FMT, int NV, int SM, int GV, bool COUNT = false>
 __global__ void __launch_bounds__(512) k_quant_row_regs(const uint16_t *__restrict__ x, int nvec,
                                                         int64_t ld_x, uint8_t *__restrict__ q,
                                                         int64_t ld_q, uint8_t *__restrict__ s,
-                                                        int64_t ld_s) {
+                                                        int64_t ld_s,
+                                                        unsigned long long *__restrict__ cnt = nullptr) {
     __shared__ uint32_t red[16];
     __shared__ uint32_t bcast;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nwarps = blockDim.x >> 5;
+    if (COUNT && tid == 0) bcast = 0u;
     const int64_t row = blockIdx.x;
     const uint4 *xr = reinterpret_cast<const uint4 *>(x + row * ld_x);
     uint2 *qr = reinterpret_cast<uint2 *>(q + row * ld_q);
@@ -161,7 +165,7 @@ __global__ void __launch_bounds__(512) k_quant_row_regs(const uint16_t *__restri
             m = max(m, bf16_abs_max8(v[i]));
         }
     }
-    uint32_t unused = 0;
+    uint32_t unused = 0, nsat = 0;
     if constexpr (GV > 0) {
         // nvec is a multiple of GV, so a group is either wholly inside the
         // row or wholly past it; every lane reaches the shuffles
@@ -175,9 +179,16 @@ __global__ void __launch_bounds__(512) k_quant_row_regs(const uint16_t *__restri
             if (ok) {
                 const GroupScale<FMT, SM> gs(g);
                 qr[c] = gs.nan ? make_uint2(kNanCodes, kNanCodes)
-                               : quant8<FMT, false>(v[i], gs.mul, unused);
+                               : quant8<FMT, COUNT>(v[i], gs.mul, COUNT ? nsat : unused);
                 if ((tid % GV) == 0) gs.store(s, row * ld_s + c / GV);
             }
+        }
+        if constexpr (COUNT) {
+            nsat = __reduce_add_sync(0xFFFFFFFFu, nsat);
+            __syncthreads();   // the counter's reset is visible
+            if (lane == 0 && nsat) atomicAdd(&bcast, nsat);
+            __syncthreads();
+            if (tid == 0 && bcast) atomicAdd(cnt, static_cast<unsigned long long>(bcast));
         }
         return;
     }
@@ -770,9 +781,10 @@ int resident_blocks(K kernel, int threads) {
     return n;
 }
 
-template <int FMT, int SM, int GV = 0>
+template <int FMT, int SM, int GV = 0, bool COUNT = false>
 cudaError_t launch_row_regs(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, uint8_t *q,
-                       int64_t ld_q, uint8_t *s, int64_t ld_s, cudaStream_t stream) {
+                       int64_t ld_q, uint8_t *s, int64_t ld_s, cudaStream_t stream,
+                       unsigned long long *cnt = nullptr) {
     const int nvec = static_cast<int>(cols / 8);
     // Vectors per thread NV and threads T (T * NV covers the row, T <= 512):
     // the largest NV that keeps at least 96 threads per row and wastes at
@@ -815,11 +827,11 @@ cudaError_t launch_row_regs(const uint16_t *x, int64_t rows, int64_t cols, int64
         return cudaGetLastError();
     }
     switch (best_nv) {
-    case 1: k_quant_row_regs<FMT, 1, SM, GV><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
-    case 2: k_quant_row_regs<FMT, 2, SM, GV><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
-    case 4: k_quant_row_regs<FMT, 4, SM, GV><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
-    case 8: k_quant_row_regs<FMT, 8, SM, GV><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
-    default: k_quant_row_regs<FMT, 16, SM, GV><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s); break;
+    case 1: k_quant_row_regs<FMT, 1, SM, GV, COUNT><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s, cnt); break;
+    case 2: k_quant_row_regs<FMT, 2, SM, GV, COUNT><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s, cnt); break;
+    case 4: k_quant_row_regs<FMT, 4, SM, GV, COUNT><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s, cnt); break;
+    case 8: k_quant_row_regs<FMT, 8, SM, GV, COUNT><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s, cnt); break;
+    default: k_quant_row_regs<FMT, 16, SM, GV, COUNT><<<grid, best_t, 0, stream>>>(x, nvec, ld_x, q, ld_q, s, ld_s, cnt); break;
     }
     return cudaGetLastError();
 }
@@ -963,6 +975,12 @@ cudaError_t launch_quant_mx32(const uint16_t *x, int64_t rows, int64_t cols, int
                               unsigned long long *cnt, cudaStream_t stream) {
     if (rows == 0 || cols == 0) return cudaSuccess;
     const MxCounters c{cnt, nullptr, nullptr};
+    if (cnt && cols * 2 <= 8192)   // short rows with the clamp count
+        return fmt == FMT_E4M3
+                   ? launch_row_regs<FMT_E4M3, SCALE_MX, 4, true>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
+                                                                stream, cnt)
+                   : launch_row_regs<FMT_E5M2, SCALE_MX, 4, true>(x, rows, cols, ld_x, q, ld_q, s, ld_s,
+                                                                stream, cnt);
     if (cnt) {
         return fmt == FMT_E4M3
                    ? launch_groups<FMT_E4M3, 4, SCALE_MX, true>(x, rows, cols, ld_x, q, ld_q, s, ld_s,

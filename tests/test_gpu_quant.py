@@ -125,7 +125,9 @@ def test_quant_block128_batch(cuda_lib, fmt, trans):
 
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("kind,rows,cols", [("mx_ln", 64, 4096), ("mx_ln_clamp", 64, 4096),
-                                            ("act", 33, 96), ("act", 1, 32)])
+                                            ("act", 33, 96), ("act", 1, 32),
+                                            # rows longer than 8 KB: the multi-row kernel
+                                            ("mx_ln_clamp", 16, 4608), ("act", 5, 8224)])
 def test_quant_mx32(cuda_lib, fmt, kind, rows, cols):
     x = _bits(kind, rows, cols, rows + cols + fmt).copy()
     if rows > 5:
