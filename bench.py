@@ -257,10 +257,6 @@ def _g128_bytes(n_el):             # 1x128 groups (either direction): + 1 B per 
     return 3.0 * n_el + n_el / 128.0
 
 
-def _dual_bytes(n_el, rows):       # one read, both outputs: 2 + 1 + 1 B per element + scales
-    return 4.0 * n_el + rows + n_el / 128.0
-
-
 def _dual_bytes(n_el, rows):        # both layouts from one read: 2 B read + 2 x 1 B written
     return 4.0 * n_el + rows + n_el / 128.0
 
