@@ -20,7 +20,8 @@
                   each; 11 with --act-quant separate) + 9 GEMM launches per step.
   fprop_1p5b      Qwen2.5-1.5B layer fprop at M = 8192: X, H per token, the
                   gate / up / down / QKV weights in 128x128 blocks (one batched
-                  launch), four GEMMs.
+                  launch, gate and up written into one stacked buffer), three
+                  GEMMs: gate and up as one (--gate-up separate: four GEMMs).
   tiny_fprop      X [256 x 512] per token, W [512 x 512] blocks, one GEMM.
   mxfp8_4096      MXFP8: A, B [4096 x 4096] (layer-norm-like and normal rows)
                   quantized in 32-element blocks (clamps counted), C = A B^T.
@@ -88,6 +89,9 @@ def _parse(argv=None):
                     help="timed steps replayed from one CUDA graph (default), or launched one by one")
     ap.add_argument("--act-quant", default="dual", choices=["dual", "separate"],
                     help="7B step: both activation layouts from one read, or one call each")
+    ap.add_argument("--gate-up", default="merged", choices=["merged", "separate"],
+                    help="1.5B forward: the gate and up projections as one GEMM over their "
+                         "stacked weights, or one GEMM each")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-peak-probe", action="store_true")
@@ -371,9 +375,14 @@ class LinearStep7B(StepBase):
 class FpropStep(StepBase):
     """Forward linears only: activations per token, weights in 128x128 blocks
     (no transposed copy), one BF16 GEMM per weight.  gemms: list of
-    (weight name, activation name)."""
+    (weight name, activation name).  merge: groups of weights applied to the
+    same activation (the MLP's gate and up projections) whose codes are
+    written into one buffer, one after another, and multiplied by one GEMM
+    whose output holds the group's outputs side by side (MERGE = False: one
+    GEMM each)."""
+    MERGE = True
 
-    def __init__(self, torch, f, workloads, device, workload, gemms, seed_offset=0):
+    def __init__(self, torch, f, workloads, device, workload, gemms, seed_offset=0, merge=()):
         super().__init__(torch, f, device)
         spec = workloads.WORKLOADS[workload]
         seed = replicas.replica_seed(spec["seed"], seed_offset)
@@ -385,18 +394,35 @@ class FpropStep(StepBase):
         E4 = f.E4M3
         self.wq = {w: f.alloc_block128(*self.inp[w].shape, E4, False, device)[0] for w in weights}
         self.aq = {a: f.alloc_token(*self.inp[a].shape, 0, E4, False, device) for a in acts}
-        self.gemms = gemms
-        self.out = {f"Y_{w}": torch.empty((self.inp[a].shape[0], self.inp[w].shape[0]),
-                                          dtype=torch.bfloat16, device=device) for w, a in gemms}
+        # the B operand of each GEMM: one weight's codes, or a merged group's
+        self.bq = dict(self.wq)
+        run = list(gemms)
+        for group in (merge if self.MERGE else ()):
+            a = dict(gemms)[group[0]]
+            rows = [self.inp[w].shape[0] for w in group]
+            cols = self.inp[group[0]].shape[1]
+            both, _ = f.alloc_block128(sum(rows), cols, E4, False, device)
+            r0 = 0
+            for w, r in zip(group, rows):
+                self.wq[w] = f.QTensor(both.codes[r0:r0 + r], both.scale[r0 // 128:(r0 + r) // 128],
+                                       E4, f.GRAN_128x128, cols // 128)
+                del self.bq[w]
+                r0 += r
+            name = "+".join(group)
+            self.bq[name] = both
+            run = [(name, a)] + [(w, x) for w, x in run if w not in group]
+        self.gemms = run
+        self.out = {f"Y_{w}": torch.empty((self.inp[a].shape[0], self.bq[w].codes.shape[0]),
+                                          dtype=torch.bfloat16, device=device) for w, a in run}
         # several weights: one batched launch (fp8_quant_block128_batch)
         self.batch_w = len(weights) > 1
         self.QUANT_NAMES = (["W_blk_batch"] if self.batch_w else [f"{w}_blk" for w in weights]) + \
             [f"{a}_tok" for a in acts]
-        self.GEMM_NAMES = [f"fprop_{w}" for w, _ in gemms]
+        self.GEMM_NAMES = [f"fprop_{w}" for w, _ in run]
         self.quant_bytes = (sum(_blk_bytes(self.inp[w].numel(), False) for w in weights) +
                             sum(_tok_bytes(self.inp[a].numel(), self.inp[a].shape[0]) for a in acts))
-        self.gemm_flop = [2.0 * self.inp[a].shape[0] * self.inp[w].shape[0] * self.inp[a].shape[1]
-                          for w, a in gemms]
+        self.gemm_flop = [2.0 * self.inp[a].shape[0] * self.bq[w].codes.shape[0] * self.inp[a].shape[1]
+                          for w, a in run]
         self._sizes()
 
     def launches(self, L):
@@ -414,20 +440,21 @@ class FpropStep(StepBase):
             L.need(a)
             L.timed("quant", lambda: f.fp8_quant_token(i[a], 0, f.E4M3, out=q))
         for w, a in self.gemms:
-            L.timed("gemm", lambda: f.fp8_gemm_scaled(f.FPROP, self.aq[a], self.wq[w],
+            L.timed("gemm", lambda: f.fp8_gemm_scaled(f.FPROP, self.aq[a], self.bq[w],
                                                       out=self.out[f"Y_{w}"], tile=self.TILE))
             L.finished(f"Y_{w}")
 
 
 class Fprop1p5B(FpropStep):
     WORKLOAD = ("fprop_1p5b: Qwen2.5-1.5B layer fprop, M=8192 tokens, hidden 1536, MLP 8960, "
-                "QKV 2048; per-token E4M3 activations, 128x128-block E4M3 weights, BF16 out")
+                "QKV 2048; per-token E4M3 activations, 128x128-block E4M3 weights, BF16 out; "
+                "gate and up projections as one GEMM over their stacked weights")
     DESC = {"tokens": 8192, "hidden": 1536, "mlp": 8960, "qkv": 2048}
 
     def __init__(self, torch, f, workloads, device, seed_offset=0):
         super().__init__(torch, f, workloads, device, "fprop_1p5b",
                          [("W_gate", "X"), ("W_up", "X"), ("W_down", "H"), ("W_qkv", "X")],
-                         seed_offset)
+                         seed_offset, merge=(("W_gate", "W_up"),))
 
 
 class TinyFprop(FpropStep):
@@ -966,6 +993,8 @@ def run_step_config(args, torch, dist, fp8hg, workloads, ri, dev, peaks):
     cls = STEPS[args.config]
     if hasattr(cls, "ACT_QUANT"):
         cls.ACT_QUANT = args.act_quant
+    if hasattr(cls, "MERGE"):
+        cls.MERGE = args.gate_up == "merged"
     cls.TILE = args.tile
     step = cls(torch, fp8hg, workloads, dev, seed_offset=rank)
     torch.cuda.synchronize()
@@ -1108,6 +1137,8 @@ def run_step_config(args, torch, dist, fp8hg, workloads, ri, dev, peaks):
                         "gemms_per_step": ng, "quant_launches_per_step": nq,
                         "l2": L2_NOTE[args.config], "launch": launch,
                         "act_quant": getattr(cls, "ACT_QUANT", None), "gemm_tile": cls.TILE,
+                        "gate_up": (("merged" if cls.MERGE else "separate")
+                                    if args.config == "fprop_1p5b" else None),
                         "parallelism": "replicas" if world > 1 else "single GPU"}, **cls.DESC),
         "roofline": {"bound": "tensor", "kernel": gemm_kernel, "achieved": gemm_tf,
                      "peak": fp8_peak, "unit": "TFLOP/s", "frac": gemm_tf / fp8_peak,

@@ -71,6 +71,32 @@ def test_fprop_1p5b_layers(cuda_lib, a_name, w_name):
     check_gemm(*_sampled_fprop(a, w, E4M3, rng), f"fprop {w_name}")
 
 
+@pytest.mark.parametrize("tile", [0, 2])
+def test_fprop_1p5b_gate_up_stacked(cuda_lib, tile):
+    """The gate and up weights quantized by one batched call into the two
+    halves of one stacked buffer, then one GEMM over the stack: its output
+    holds the two projections side by side, the same bytes as one GEMM per
+    weight (both halves' tiles are the separate GEMMs' tiles), and sampled
+    outputs of the up half agree with the oracle."""
+    x = workloads.workload_tensor("fprop_1p5b", "X", device="cuda")
+    wg = workloads.workload_tensor("fprop_1p5b", "W_gate", device="cuda")
+    wu = workloads.workload_tensor("fprop_1p5b", "W_up", device="cuda")
+    n, k = wg.shape
+    both, _ = fp8hg.alloc_block128(2 * n, k, E4M3, False, x.device)
+    halves = [fp8hg.QTensor(both.codes[h * n:(h + 1) * n], both.scale[h * n // 128:(h + 1) * n // 128],
+                            E4M3, GRAN_128x128, k // 128) for h in (0, 1)]
+    fp8hg.fp8_quant_block128_batch([wg, wu], E4M3, outs=[(q, None) for q in halves])
+    xq = fp8hg.fp8_quant_token(x, 0, E4M3)
+    y = fp8hg.fp8_gemm_scaled(fp8hg.FPROP, xq, both, tile=tile)
+    yg = fp8hg.fp8_gemm_scaled(fp8hg.FPROP, xq, fp8hg.fp8_quant_block128(wg, E4M3), tile=tile)
+    yu = fp8hg.fp8_gemm_scaled(fp8hg.FPROP, xq, fp8hg.fp8_quant_block128(wu, E4M3), tile=tile)
+    assert fp8hg.fp8hg_get_device_error() == 0
+    assert torch.equal(y[:, :n], yg) and torch.equal(y[:, n:], yu)
+    rng = np.random.default_rng(23)
+    c_gpu, c_ref, s_abs = _sampled_fprop(x, wu, E4M3, rng)
+    check_gemm(c_gpu, c_ref, s_abs, "stacked up half (via the separate GEMM)")
+
+
 def test_dgrad_1p5b_e5m2(cuda_lib):
     """dX = dY W_gate: dY [8192, 8960] per token E5M2, B = W_gate^T from the
     block quantizer's transposed copy."""
