@@ -703,6 +703,42 @@ __device__ __forceinline__ void load_rows_wide(WScaleRows &g, const KParams &p, 
     }
 }
 
+// A piece of the wide kernel's packed BF16 rows (lane l: row l, words OFF ..
+// OFF + W - 1 of its packed row; W = 32 for 64 columns, 16 for 32) written
+// as whole row segments through the staging area.  The packed registers
+// are read in place, so the piece needs no second copy of them.
+template <int OFF, int W>
+__device__ __forceinline__ void store_packed(uint8_t *stage, const uint32_t (&pk)[WBN / 2], int lane,
+                                             uint8_t *g_row0, int64_t ld_bytes) {
+    constexpr int V = W / 4;   // 16-byte chunks per row
+#pragma unroll
+    for (int c = 0; c < V; ++c)
+        *reinterpret_cast<uint4 *>(stage + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+            make_uint4(pk[OFF + 4 * c], pk[OFF + 4 * c + 1], pk[OFF + 4 * c + 2], pk[OFF + 4 * c + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+        const int idx = i * 32 + lane, r = idx / V, c = idx % V;
+        *reinterpret_cast<uint4 *>(g_row0 + r * ld_bytes + c * 16) =
+            *reinterpret_cast<const uint4 *>(stage + r * 128 + ((c ^ (r & 7)) << 4));
+    }
+    __syncwarp();
+}
+
+// Columns PC * 64 .. PC * 64 + 63 of a wide tile's BF16 rows (PC = 3: the
+// last 32 columns).  N is a multiple of 128 and the tile starts at a
+// multiple of 224, so a 64-column piece can straddle N by exactly 32
+// columns: it is then written as a 32-column half piece.
+template <int PC>
+__device__ __forceinline__ void store_wide_piece(uint8_t *stage, const uint32_t (&pk)[WBN / 2], int lane,
+                                                 const KParams &p, int64_t row0, int nb) {
+    const int64_t n0 = static_cast<int64_t>(nb) * WBN + PC * 64;
+    if (n0 >= p.N) return;
+    uint8_t *g = reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.c) + row0 * p.ldc + n0);
+    if (PC < WBN / 64 && n0 + 64 <= p.N) store_packed<PC * 32, 32>(stage, pk, lane, g, p.ldc * 2);
+    else store_packed<PC * 32, 16>(stage, pk, lane, g, p.ldc * 2);
+}
+
 // Half piece: 32 rows x 64 bytes through the staging area (lane l holds row
 // l's four 16-byte chunks).
 __device__ __forceinline__ void store_piece64(uint8_t *stage, const uint4 (&v)[4], int lane,
@@ -1099,43 +1135,10 @@ __global__ void __launch_bounds__(W_THREADS, 1)
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(tempty);
-            // N is a multiple of 128 and the tile starts at a multiple of 224,
-            // so a 64-column piece can straddle N by exactly 32 columns: it is
-            // then written as a 32-column half piece.
-#pragma unroll
-            for (int pc = 0; pc < WBN / 64; ++pc) {        // three 64-column pieces
-                const int64_t n0 = static_cast<int64_t>(nb) * WBN + pc * 64;
-                if (n0 >= p.N) continue;
-                uint8_t *g = reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.c) + row0 * p.ldc + n0);
-                if (n0 + 64 <= p.N) {
-                    uint4 v[8];
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        v[c] = make_uint4(packed[pc * 32 + 4 * c], packed[pc * 32 + 4 * c + 1],
-                                          packed[pc * 32 + 4 * c + 2], packed[pc * 32 + 4 * c + 3]);
-                    store_piece(stage, v, lane, g, p.ldc * 2);
-                } else {
-                    uint4 v[4];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        v[c] = make_uint4(packed[pc * 32 + 4 * c], packed[pc * 32 + 4 * c + 1],
-                                          packed[pc * 32 + 4 * c + 2], packed[pc * 32 + 4 * c + 3]);
-                    store_piece64(stage, v, lane, g, p.ldc * 2);
-                }
-            }
-            {                                               // the last 32 columns
-                const int64_t n0 = static_cast<int64_t>(nb) * WBN + 192;
-                if (n0 < p.N) {
-                    uint4 v[4];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        v[c] = make_uint4(packed[96 + 4 * c], packed[96 + 4 * c + 1],
-                                          packed[96 + 4 * c + 2], packed[96 + 4 * c + 3]);
-                    store_piece64(stage, v, lane,
-                                  reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.c) + row0 * p.ldc + n0),
-                                  p.ldc * 2);
-                }
-            }
+            store_wide_piece<0>(stage, packed, lane, p, row0, nb);
+            store_wide_piece<1>(stage, packed, lane, p, row0, nb);
+            store_wide_piece<2>(stage, packed, lane, p, row0, nb);
+            store_wide_piece<3>(stage, packed, lane, p, row0, nb);
             ++tcount;
         }
     }
