@@ -74,8 +74,8 @@ TENSOR_FLOP_PER_CYCLE_SM = 16384      # dense FP8 MMA rate of one SM (128x256x32
 # step's three GEMM classes (gate-like, down-like, weight gradient; three
 # launches each), captured with ncu; valid only for the gemm.cu it was taken
 # on; any other source gives traffic null.
-GEMM_TRAFFIC = {"gemm_sha256": "0ca546b4aa18e666ecf4a056c5af882a53a8c11205d463379979a65a65b2d860",
-                "bytes_per_launch": 1.1029e9}
+GEMM_TRAFFIC = {"gemm_sha256": "049612a6325dec498219e97a8dba1ce109ceac11442ef70db564936bb2264adb",
+                "bytes_per_launch": 1.1031e9}
 
 
 def _parse(argv=None):

@@ -725,14 +725,14 @@ __device__ __forceinline__ void store_packed(uint8_t *stage, const uint32_t (&pk
     __syncwarp();
 }
 
-// Columns PC * 64 .. PC * 64 + 63 of a wide tile's BF16 rows (PC = 3: the
-// last 32 columns).  N is a multiple of 128 and the tile starts at a
-// multiple of 224, so a 64-column piece can straddle N by exactly 32
-// columns: it is then written as a 32-column half piece.
+// Columns col0 + PC * 64 .. + 63 of 224 packed BF16 columns (PC = 3: the
+// last 32 columns).  N is a multiple of 128 and col0 a multiple of 32, so a
+// 64-column piece can straddle N by exactly 32 columns: it is then written
+// as a 32-column half piece.
 template <int PC>
 __device__ __forceinline__ void store_wide_piece(uint8_t *stage, const uint32_t (&pk)[WBN / 2], int lane,
-                                                 const KParams &p, int64_t row0, int nb) {
-    const int64_t n0 = static_cast<int64_t>(nb) * WBN + PC * 64;
+                                                 const KParams &p, int64_t row0, int64_t col0) {
+    const int64_t n0 = col0 + PC * 64;
     if (n0 >= p.N) return;
     uint8_t *g = reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.c) + row0 * p.ldc + n0);
     if (PC < WBN / 64 && n0 + 64 <= p.N) store_packed<PC * 32, 32>(stage, pk, lane, g, p.ldc * 2);
@@ -1135,10 +1135,11 @@ __global__ void __launch_bounds__(W_THREADS, 1)
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(tempty);
-            store_wide_piece<0>(stage, packed, lane, p, row0, nb);
-            store_wide_piece<1>(stage, packed, lane, p, row0, nb);
-            store_wide_piece<2>(stage, packed, lane, p, row0, nb);
-            store_wide_piece<3>(stage, packed, lane, p, row0, nb);
+            const int64_t col0 = static_cast<int64_t>(nb) * WBN;
+            store_wide_piece<0>(stage, packed, lane, p, row0, col0);
+            store_wide_piece<1>(stage, packed, lane, p, row0, col0);
+            store_wide_piece<2>(stage, packed, lane, p, row0, col0);
+            store_wide_piece<3>(stage, packed, lane, p, row0, col0);
             ++tcount;
         }
     }
@@ -1563,40 +1564,11 @@ __global__ void __launch_bounds__(PR_THREADS, 1)
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive_cluster(tempty_l);
-#pragma unroll
-            for (int pc = 0; pc < PR_HN / 64; ++pc) {        // three 64-column pieces
-                const int64_t n0 = col0 + pc * 64;
-                if (n0 >= p.N) continue;
-                uint8_t *g = reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.c) + row0 * p.ldc + n0);
-                if (n0 + 64 <= p.N) {
-                    uint4 v[8];
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        v[c] = make_uint4(packed[pc * 32 + 4 * c], packed[pc * 32 + 4 * c + 1],
-                                          packed[pc * 32 + 4 * c + 2], packed[pc * 32 + 4 * c + 3]);
-                    store_piece(stage, v, lane, g, p.ldc * 2);
-                } else {
-                    uint4 v[4];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        v[c] = make_uint4(packed[pc * 32 + 4 * c], packed[pc * 32 + 4 * c + 1],
-                                          packed[pc * 32 + 4 * c + 2], packed[pc * 32 + 4 * c + 3]);
-                    store_piece64(stage, v, lane, g, p.ldc * 2);
-                }
-            }
-            {                                                // the last 32 columns
-                const int64_t n0 = col0 + 192;
-                if (n0 < p.N) {
-                    uint4 v[4];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        v[c] = make_uint4(packed[96 + 4 * c], packed[96 + 4 * c + 1],
-                                          packed[96 + 4 * c + 2], packed[96 + 4 * c + 3]);
-                    store_piece64(stage, v, lane,
-                                  reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.c) + row0 * p.ldc + n0),
-                                  p.ldc * 2);
-                }
-            }
+            static_assert(PR_HN == WBN, "the pair kernel's column half has the wide tile's width");
+            store_wide_piece<0>(stage, packed, lane, p, row0, col0);
+            store_wide_piece<1>(stage, packed, lane, p, row0, col0);
+            store_wide_piece<2>(stage, packed, lane, p, row0, col0);
+            store_wide_piece<3>(stage, packed, lane, p, row0, col0);
             ++tcount;
         }
     }
